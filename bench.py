@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark: MLA DCP decode on one GB300 (replicas on N GPUs).
+
+One step = the whole hot path on one batch: the D shard decodes (split-KV
+schedule, paged gathers, QK^T + online softmax + PV, split combine) and the
+LSE merge.  The headline workload is plain decode: 64 requests, q_len 1,
+16 heads, context 4096, DCP D=2 (the D shards are D slices of one HBM).  The
+other benchmark workloads (plain decode D=1, MTP, long context, sparse +
+mixed) are measured the same way and reported under "configs".
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA DCP decode query tok/s; KV GB/s & TFLOP/s as % of GB300 roofline"
+UNIT = "query tok/s"
+ROW_BYTES = 576 * 2
+FLOPS_PER_KEY_ROW = 2 * (576 + 512)
+HEADLINE = "plain_decode_d2"
+DESCR = {
+    "tiny": "tiny: 4 requests, context {6,37,130,300}, q_len {4,1,2,2}, H=16, D=2, page 16, merge+W_UV",
+    "plain_decode_d1": "plain decode: batch 64, q_len 1, H=16, context 4096, D=1, page 64, merge to 512-wide",
+    "plain_decode_d2": "plain decode: batch 64, q_len 1, H=16, context 4096, D=2, page 64, merge to 512-wide",
+    "mtp": "MTP decode: batch 128, q_len 2, H=16, context U[1024,8192], D=4, page 64, merge+W_UV",
+    "long_context": "long context: batch 32, q_len 2, H=128, context U[16384,32768], D=8, page 64, merge+W_UV",
+    "sparse_mixed": "sparse+mixed: 96 requests q_len {1,2,4} + 4x64 prefill, H=64, context U[4096,65536], "
+                    "top-k 2048, D=4, page 64, merge+W_UV",
+}
+
+
+def peaks():
+    p = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p.update(hbm_gbs=float(m["hbm_gbs"]), bf16_tflops=float(m["bf16_tflops"]),
+                 bf16_tflops_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), source="measured")
+    return p
+
+
+# ------------------------------------------------------------ algorithmic work
+
+
+def work_of(w):
+    """Algorithmic KV bytes, FLOPs and merge bytes of one step of workload w."""
+    L = w.seq_lens.cpu().numpy().astype(np.int64)
+    qsl = w.query_start_loc.cpu().numpy().astype(np.int64)
+    D, H = w.dcp_world, w.num_heads
+    q_len = qsl[1:] - qsl[:-1]
+    kv_bytes_shard = []
+    flops = 0
+    if w.topk is None:
+        for r in range(D):
+            local = np.where(L > r, (L - r - 1) // D + 1, 0)
+            kv_bytes_shard.append(int(local.sum()) * ROW_BYTES)
+        # every token sees its visible prefix, over all shards together
+        vis = 0
+        for b in range(len(L)):
+            P = L[b] - q_len[b] + np.arange(q_len[b])
+            vis += int((P + 1).sum())
+        flops = vis * H * FLOPS_PER_KEY_ROW
+    else:
+        topk = w.topk.cpu().numpy()
+        valid = w.topk_valid.cpu().numpy()
+        pos = np.empty(w.num_tokens, np.int64)
+        for b in range(len(L)):
+            pos[qsl[b]:qsl[b + 1]] = L[b] - q_len[b] + np.arange(q_len[b])
+        K = topk.shape[1]
+        used = (np.arange(K)[None, :] < valid[:, None]) & (topk >= 0) & (topk <= pos[:, None])
+        for r in range(D):
+            kept = used & (topk % D == r)
+            kv_bytes_shard.append(int(kept.sum()) * ROW_BYTES)
+        flops = int(used.sum()) * H * FLOPS_PER_KEY_ROW
+    T = w.num_tokens
+    out_w = 128 if w.w_uv is not None else 512
+    merge_bytes = D * T * H * (512 * 4 + 4) + D * T * 4 + T * H * (out_w * 2 + 4)
+    if w.w_uv is not None:
+        merge_bytes += H * 512 * 128 * 2
+    q_bytes = T * H * 576 * 2
+    return dict(kv_bytes=sum(kv_bytes_shard), kv_bytes_shard=kv_bytes_shard, flops=flops, merge_bytes=merge_bytes,
+                q_bytes=q_bytes, tokens=T)
+
+
+# ------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
+    import mla_decode_attention_04_gb300 as mla
+    from mla_decode_attention_04_gb300 import pipeline, workloads as wl
+
+    w = wl.NAMED[name](device="cuda")
+    step = pipeline.step_for_workload(w)
+    work = work_of(w)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if l2_flush else None
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    rc, detail = mla.workspace_status(step.workspace)
+    if rc != mla.MLA_OK:
+        raise RuntimeError(f"device check {detail} in {name}")
+
+    D = w.dcp_world
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(D + 2)] for _ in range(steps)]
+    launches0 = mla.kernel_launch_count()
+    torch.cuda.synchronize()
+    for k in range(steps):
+        if flush is not None:
+            flush_l2(flush)
+        e = ev[k]
+        e[0].record(stream)
+        for r, (cache, bt) in enumerate(step.shards):
+            step_shard(step, r, cache, bt)
+            e[r + 1].record(stream)
+        step_merge(step)
+        e[D + 1].record(stream)
+    torch.cuda.synchronize()
+    launches = mla.kernel_launch_count() - launches0
+    step_ms = [e[0].elapsed_time(e[D + 1]) for e in ev]
+    decode_ms = [[e[r].elapsed_time(e[r + 1]) for r in range(D)] for e in ev]
+    merge_ms = [e[D].elapsed_time(e[D + 1]) for e in ev]
+    res = dict(name=name, w=w, step=step, work=work, step_ms=step_ms, decode_ms=decode_ms, merge_ms=merge_ms,
+               launches=launches)
+    if with_e2e:
+        res["e2e"] = time_e2e(w, step, steps, flush)
+    return res
+
+
+def step_shard(step, r, cache, bt):
+    import mla_decode_attention_04_gb300 as mla
+    if step.topk is not None:
+        mla.mla_sparse_dcp_decode(step.q_nope, step.q_pe, cache, bt, step.seq_lens, step.qsl, step.topk,
+                                  step.topk_valid, step.D, r, step.scale, out=step.partials[r], lse=step.lses[r],
+                                  local_counts=step.counts[r], workspace=step.workspace)
+    else:
+        mla.mla_dcp_decode(step.q_nope, step.q_pe, cache, bt, step.seq_lens, step.qsl, step.max_query_len,
+                           step.max_seq_len, step.D, r, step.scale, out=step.partials[r], lse=step.lses[r],
+                           row_counts=step.counts[r], num_splits=step.num_splits, workspace=step.workspace)
+
+
+def step_merge(step):
+    import mla_decode_attention_04_gb300 as mla
+    mla.dcp_lse_merge(step.partials, step.lses, step.counts, step.w_uv, out=step.out, lse_out=step.lse)
+
+
+def time_e2e(w, step, steps, flush):
+    """Same step through the public API with the per-step inputs (queries and
+    request metadata) copied from pinned host memory and the output read back;
+    the KV cache is device-resident state."""
+    hq_n = w.q_nope.cpu().pin_memory()
+    hq_p = w.q_pe.cpu().pin_memory()
+    hmeta = [t.cpu().pin_memory() for t in (w.seq_lens, w.query_start_loc)]
+    htabs = [s.block_table.cpu().pin_memory() for s in w.shards]
+    hsparse = [] if w.topk is None else [w.topk.cpu().pin_memory(), w.topk_valid.cpu().pin_memory()]
+    hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    dev_meta = [step.seq_lens, step.qsl]
+    dev_tabs = [s[1] for s in step.shards]
+    dev_sparse = [] if w.topk is None else [step.topk, step.topk_valid]
+    h2d = sum(t.numel() * t.element_size() for t in [hq_n, hq_p] + hmeta + htabs + hsparse)
+    d2h = hout.numel() * hout.element_size()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush_l2(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step.q_nope.copy_(hq_n, non_blocking=True)
+        step.q_pe.copy_(hq_p, non_blocking=True)
+        for d, h in zip(dev_meta + dev_tabs + dev_sparse, hmeta + htabs + hsparse):
+            d.copy_(h, non_blocking=True)
+        step.run()
+        hout.copy_(step.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    return dict(value=w.num_tokens / (ms * 1e-3), unit=UNIT, ms_per_step=ms, h2d_bytes_per_step=int(h2d),
+                d2h_bytes_per_step=int(d2h))
+
+
+def summarize(res, pk):
+    work = res["work"]
+    step_ms = statistics.median(res["step_ms"])
+    dec_ms = [statistics.median([d[r] for d in res["decode_ms"]]) for r in range(len(res["decode_ms"][0]))]
+    merge_ms = statistics.median(res["merge_ms"])
+    t_roof = max(work["kv_bytes"] / (pk["hbm_gbs"] * 1e9), work["flops"] / (pk["bf16_tflops"] * 1e12))
+    bound = "hbm" if work["kv_bytes"] / pk["hbm_gbs"] >= work["flops"] / (pk["bf16_tflops"] * 1e3) else "tensor"
+    dec_total = sum(dec_ms)
+    return dict(
+        ms_per_step=step_ms,
+        query_tok_s=work["tokens"] / (step_ms * 1e-3),
+        decode_ms=dec_ms, merge_ms=merge_ms,
+        kv_gbs=work["kv_bytes"] / (dec_total * 1e-3) / 1e9,
+        tflops=work["flops"] / (dec_total * 1e-3) / 1e12,
+        roofline_bound=bound,
+        roofline_ms=t_roof * 1e3,
+        step_roofline_frac=t_roof * 1e3 / step_ms,
+        decode_roofline_frac=t_roof * 1e3 / dec_total,
+        merge_gbs=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9,
+        merge_hbm_frac=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        kv_bytes=work["kv_bytes"], flops=work["flops"],
+    )
+
+
+def profile_traffic(kernel_tag):
+    """DRAM bytes per launch from a committed ncu summary, if it describes the
+    current kernel build; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel_tag)
+        if not ent:
+            return None
+        from mla_decode_attention_04_gb300 import build as b
+        if ent.get("source_digest") != b.source_digest():
+            return None
+        return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def run_ours(args):
+    import mla_decode_attention_04_gb300 as mla
+    from mla_decode_attention_04_gb300 import build as mla_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+    mla_build.build()
+    mla.load_library()
+    pk = peaks()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    clocks = clk.summary()
+    s = summarize(head, pk)
+    step_ms = s["ms_per_step"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    tokens = head["work"]["tokens"]
+    value = tokens * world / (step_ms * 1e-3)
+
+    configs = {}
+    if args.configs != "headline" and rank == 0:
+        names = [n for n in ("plain_decode_d1", "mtp", "long_context", "sparse_mixed")
+                 if args.configs == "all" or n in args.configs.split(",")]
+        for n in names:
+            r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)))
+            cs = summarize(r, pk)
+            configs[n] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cs.items()}
+            configs[n]["workload"] = DESCR[n]
+            del r
+            torch.cuda.empty_cache()
+
+    dec_ms = statistics.mean(statistics.median([d[r] for d in head["decode_ms"]])
+                             for r in range(len(head["decode_ms"][0])))
+    per_launch_bytes = head["work"]["kv_bytes"] / len(head["work"]["kv_bytes_shard"])
+    achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch/numpy draws; no dataset)",
+        "config": {"workload": DESCR[HEADLINE],
+                   "l2": "256 MB buffer written before every timed step (KV 302 MB > 129 MB L2 as well)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "partials": "fp32 per-shard outputs into the merge"},
+        "kv_gbs": s["kv_gbs"],
+        "tflops": s["tflops"],
+        "step_roofline_frac": s["step_roofline_frac"],
+        "decode_roofline_frac": s["decode_roofline_frac"],
+        "merge_hbm_frac": s["merge_hbm_frac"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_dense_" + HEADLINE),
+                     "kernel": "shard decode call (scheduler + decode + split combine), CUDA events per call",
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "e2e": head["e2e"],
+        "clocks": clocks,
+        "gpu_launches": head["launches"],
+        "wall_s": wall,
+        "configs": configs,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------- oracle (CPU) arm
+
+
+def oracle_sample_step(w, h, threads):
+    """The oracle's whole step (every shard, merge, W_UV) on workload w."""
+    import oracle
+    D = w.dcp_world
+    parts, lses, counts = [], [], []
+    for r in range(D):
+        o, l, c = oracle.dcp_decode(h["q_nope"], h["q_pe"], h["caches"][r], h["tables"][r], h["seq_lens"], h["qsl"],
+                                    D, r, w.scale, threads=threads)
+        parts.append(o), lses.append(l), counts.append(c)
+    merged, lse = oracle.lse_merge(np.stack(parts), np.stack(lses), np.stack(counts))
+    if h["w_uv"] is not None:
+        merged = oracle.wuv_project(merged, h["w_uv"])
+    return merged, lse
+
+
+def oracle_sample(batch):
+    from mla_decode_attention_04_gb300 import workloads as wl
+    w = wl.plain_decode(dcp_world=2, batch=batch, device="cpu")
+    h = dict(q_nope=wl.bf16_bits(w.q_nope), q_pe=wl.bf16_bits(w.q_pe), seq_lens=w.seq_lens.numpy(),
+             qsl=w.query_start_loc.numpy(), caches=[wl.bf16_bits(s.cache) for s in w.shards],
+             tables=[s.block_table.numpy() for s in w.shards], w_uv=None)
+    return w, h
+
+
+def cpu_baseline(args, batch=16):
+    import oracle
+    threads = oracle.default_threads()
+    w, h = oracle_sample(batch)
+    oracle_sample_step(w, h, threads)  # warm (loads the library)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_sample_step(w, h, threads)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 50:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": w.num_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{batch} of the 64 requests of the headline workload (context 4096, H=16, D=2: both shards "
+                      f"+ merge), fp64 C oracle, {reps} repetitions"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    import oracle
+    threads = oracle.default_threads()
+    w, h = oracle_sample(8)
+    for _ in range(args.warmup):
+        oracle_sample_step(w, h, threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample_step(w, h, threads)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.median(times) * 1e3
+    value = w.num_tokens / (ms * 1e-3)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": DESCR[HEADLINE], "sample": "8 of the 64 requests per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "8 of the 64 requests of the headline workload per step (both shards + merge), "
+                                   "fp64 C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--configs", default="all", help="all | headline | comma list of workload names")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * mla_dcp.h -- C ABI of the GB300 (sm_103a) absorbed-MLA decode attention
+ * library under decode context parallelism (DCP).
+ *
+ * Operations and their sources (page title, then section):
+ *   - "vllm.v1.attention.backends.mla.flashattn_mla", FlashAttnMLAImpl.
+ *     _forward_decode: the absorbed MLA decode.  The query is split into
+ *     q_nope (kv_lora_rank = 512) and q_pe (qk_rope_head_dim = 64); one cache
+ *     row is kv_c (first 512) followed by k_pe (64); the kernel is called
+ *     with q=q_pe, k=k_pe, v=kv_c, q_v=q_nope, causal, a paged block_table,
+ *     per-request seq_lens, cu_seqlens_q = query_start_loc, softmax_scale,
+ *     and returns the softmax LSE laid out [tokens, heads] for DCP.
+ *   - "[Attention] add DCP support for FLASH_ATTN_MLA backend", review
+ *     thread: tokens are interleaved over the DCP ranks (token p on rank
+ *     p mod D) and every query row has its own seqlen_k on each rank (the
+ *     "DCP Rank 0/1" mask tables).
+ *   - "[Attention][DCP] Support DCP with query length > 1 (MTP) with FA3",
+ *     Purpose: q_len > 1 and mixed prefill/decode batches; the kernel only
+ *     needs the cp world size and rank.
+ *   - "[Attention] DCP sparse MLA output-merge optimizations", summary: the
+ *     LSE-weighted merge of the per-rank results, the W_UV projection that
+ *     commutes with it, per-row valid counts, sparse MLA.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" point to device memory of the current CUDA
+ *     device; the caller owns every buffer.  The library allocates nothing:
+ *     scratch comes from the caller's workspace.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  No call synchronises the host or reads device memory from the
+ *     host, so every call is asynchronous and returns before the GPU is done.
+ *   - bf16 is IEEE bfloat16 stored in 16 bits; lse is float32 natural-log
+ *     sum-exp of the scaled scores (softmax_scale included).
+ *   - Return value: MLA_OK, or an error code with a message retrievable by
+ *     mla_last_error() (thread-local).  Argument errors are detected on the
+ *     host before anything is launched.  Data-dependent conditions the host
+ *     cannot see without a sync (a page id out of range, q_len > seq_len)
+ *     are checked by the kernels, which record the first failure in the
+ *     workspace status word and skip the offending access; read it with
+ *     mla_workspace_status().
+ *   - Unsupported features (FP8 cache, other head dims), as in the backend's
+ *     constructor gates, return MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_DCP_H
+#define MLA_DCP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_KV_LORA_RANK 512
+#define MLA_ROPE_DIM 64
+#define MLA_KV_ROW (MLA_KV_LORA_RANK + MLA_ROPE_DIM)
+#define MLA_V_HEAD_DIM 128
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* shape, pointer, alignment, rank >= world ... */
+  MLA_ERR_UNSUPPORTED = 2,   /* FP8 cache, page size or head dims not served */
+  MLA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
+  MLA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required */
+  MLA_ERR_DEVICE_CHECK = 5   /* (mla_workspace_status) a kernel check fired */
+} mla_status;
+
+typedef enum { MLA_DTYPE_BF16 = 0, MLA_DTYPE_F32 = 1, MLA_DTYPE_FP8_E4M3 = 2 } mla_dtype;
+
+/* Message of the last failing call on this thread ("" if none). */
+const char *mla_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * mla_dcp_decode -- dense absorbed-MLA paged decode attention of DCP shard
+ * `dcp_rank` of `dcp_world` ("flashattn_mla" _forward_decode with the DCP
+ * mask of the FLASH_ATTN_MLA DCP review thread and the MTP page's cp world
+ * size / rank).
+ *
+ * For request b (0 <= b < num_requests) with global length L = seq_lens[b]
+ * and query tokens t in [query_start_loc[b], query_start_loc[b+1]) (q_len of
+ * them), query token i sits at global position P = L - q_len + i.  This
+ * shard holds the tokens p with p mod D == r at local slots j = p div D,
+ * local slot j of request b being row (j mod page_size) of page
+ * block_table[b * block_table_stride + j / page_size] of kv_cache.  Row
+ * (t, h) sees local slot j iff j*D + r <= P, i.e. the first
+ * n = floor((P - r)/D) + 1 slots (0 if P < r).  With
+ *   s_j = scale * (q_nope[t,h,:] . kv_c_j + q_pe[t,h,:] . k_pe_j)
+ * it writes lse[t,h] = log(sum_j exp(s_j)) and
+ * out[t,h,:] = sum_j exp(s_j - lse) kv_c_j; a row that sees no key gets
+ * lse = -inf and out = 0.  row_counts[t] = n.
+ *
+ *  q_nope   device bf16, row (t,h) at q_nope + (t*H + h)*q_nope_row_stride
+ *           elements, 512 contiguous elements; stride >= 512, a multiple of 8.
+ *  q_pe     device bf16, same with q_pe_row_stride (>= 64, multiple of 8).
+ *           (q_nope = q, q_pe = q + 512 with both strides 576 serves a fused
+ *           [T, H, 576] query.)
+ *  kv_cache device bf16 [num_blocks, page_size, 576], contiguous, 16-byte
+ *           aligned: this shard's cache slice.
+ *  page_size  8, 16, 32, or a multiple of 64.
+ *  block_table device int32 [num_requests, block_table_stride]: shard-local
+ *           page ids; only the first ceil(local_len/page_size) entries of a
+ *           row are read.
+ *  seq_lens device int32 [num_requests]: GLOBAL lengths, new tokens
+ *           included (q_len <= seq_len).
+ *  query_start_loc device int32 [num_requests + 1], nondecreasing, [0] = 0,
+ *           [num_requests] = num_tokens.
+ *  max_query_len  upper bound of the q_lens; 0 is treated as 1 (the
+ *           backend's capture-time clamp).
+ *  max_seq_len    upper bound of seq_lens (sizes the split plan).
+ *  out      device [num_tokens, num_heads, 512] of out_dtype (BF16 or F32).
+ *  lse      device float32 [num_tokens, num_heads].
+ *  row_counts device int32 [num_tokens], or NULL.
+ *  num_splits  0 = automatic split-KV plan, else an upper bound on the KV
+ *           chunks per request (fix it for CUDA-graph capture).
+ *  workspace   device scratch of at least mla_dcp_decode_workspace_size()
+ *           bytes, 256-byte aligned; contents need not be initialised.
+ *  Errors: INVALID_ARG (NULL/misaligned pointers, sizes < 0, dcp_rank not in
+ *  [0, dcp_world), num_heads not in [1, 128]), UNSUPPORTED (page size),
+ *  WORKSPACE, CUDA.  num_tokens == 0 is a successful no-op.
+ * ---------------------------------------------------------------------- */
+size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                     int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
+                                     int32_t num_splits);
+
+int mla_dcp_decode(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe, int64_t q_pe_row_stride,
+                   const void *kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                   const int32_t *block_table, int32_t block_table_stride, const int32_t *seq_lens,
+                   const int32_t *query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                   int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
+                   void *out, int32_t out_dtype, float *lse, int32_t *row_counts, int32_t num_splits,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * mla_sparse_dcp_decode -- the same attention over per-token top-k key lists
+ * ("[Attention] DCP sparse MLA output-merge optimizations": sparse MLA with
+ * per-row valid counts), restricted to DCP shard r of D.
+ *
+ * Query token t (of request b, global position P) uses the entries
+ * topk_indices[t * topk + e] for e < topk_valid[t]; an entry is a global
+ * token position of request b and is used iff 0 <= idx <= P (-1 pads).
+ * Shard r keeps the used entries with idx mod D == r (local slot idx div D,
+ * read through block_table as above).  Every kept entry is one key: with the
+ * same s_j as the dense call, lse/out are the softmax over the kept keys of
+ * that token (all heads share the list); local_counts[t] = number kept;
+ * no key kept gives lse = -inf, out = 0.
+ *
+ *  topk_indices device int32 [num_tokens, topk], topk in [1, 65536].
+ *  topk_valid   device int32 [num_tokens].
+ *  local_counts device int32 [num_tokens] (required: it is the merge's
+ *               per-row valid count).
+ *  Other arguments as in mla_dcp_decode.  workspace >=
+ *  mla_sparse_dcp_decode_workspace_size() bytes.
+ * ---------------------------------------------------------------------- */
+size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk,
+                                            int32_t dcp_world);
+
+int mla_sparse_dcp_decode(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe, int64_t q_pe_row_stride,
+                          const void *kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                          const int32_t *block_table, int32_t block_table_stride, const int32_t *seq_lens,
+                          const int32_t *query_start_loc, int32_t num_requests, int32_t num_tokens,
+                          int32_t num_heads, const int32_t *topk_indices, int32_t topk, const int32_t *topk_valid,
+                          int32_t dcp_world, int32_t dcp_rank, float scale, void *out, int32_t out_dtype,
+                          float *lse, int32_t *local_counts, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * dcp_lse_merge -- LSE-weighted merge of the D shard results, optionally
+ * fused with the per-head W_UV up-projection ("[Attention] DCP sparse MLA
+ * output-merge optimizations", summary: _dcp_lse_merge /
+ * _dcp_merge_and_v_up_proj; the projection commutes with the merge).
+ *
+ * For token t, head h, over the shards r that take part (valid_counts[r*T+t]
+ * > 0 when valid_counts is given, else lses[(r*T+t)*H+h] > -inf):
+ *   LSE = log(sum_r exp(lse_r)),  o = sum_r exp(lse_r - LSE) * partial_r
+ *   out[t,h,:] = o            (w_uv == NULL, width 512)
+ *   out[t,h,:] = o . W_UV[h]  (w_uv != NULL, width 128)
+ * A row no shard takes part in gets out = 0 and LSE = -inf; the partials and
+ * lses of shards that do not take part are not read (they may hold
+ * anything, NaN included).
+ *
+ *  partials  device [dcp_world, num_tokens, num_heads, 512] of
+ *            partial_dtype (BF16 or F32), 16-byte aligned.
+ *  lses      device float32 [dcp_world, num_tokens, num_heads].
+ *  valid_counts device int32 [dcp_world, num_tokens] or NULL.
+ *  w_uv      device bf16 [num_heads, 512, 128] or NULL, 16-byte aligned.
+ *  out       device [num_tokens, num_heads, 128 or 512] of out_dtype (BF16
+ *            or F32).
+ *  lse_out   device float32 [num_tokens, num_heads] or NULL.
+ *  Errors: INVALID_ARG, CUDA.  num_tokens == 0 is a successful no-op.
+ * ---------------------------------------------------------------------- */
+int dcp_lse_merge(const void *partials, int32_t partial_dtype, const float *lses, const int32_t *valid_counts,
+                  const void *w_uv, int32_t dcp_world, int32_t num_tokens, int32_t num_heads, void *out,
+                  int32_t out_dtype, float *lse_out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * mla_workspace_status -- synchronises `stream`, then reads the status word
+ * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
+ * with *detail set to the first failing check's code: 1 = a page id (or its
+ * block-table column) out of range, 2 = q_len > seq_len or a bad
+ * query_start_loc, 3 = a pipeline wait gave up, 4 = the split plan did not
+ * fit the workspace.  This is the one call that blocks the host.
+ * ---------------------------------------------------------------------- */
+int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
+
+/* ------------------------------------------------------------------------
+ * mla_kernel_launch_count -- number of kernels this library has launched in
+ * this process so far (all threads; memsets excluded).  Lets a caller state
+ * how many of the library's kernels ran inside a timed region.
+ * ---------------------------------------------------------------------- */
+int64_t mla_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DCP_H */

@@ -1,0 +1,329 @@
+// api.cu -- the C ABI (include/mla_dcp.h): argument checks, planning, launches.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <cmath>
+#include <string>
+
+#include "common.cuh"
+#include "decode_kernels.h"
+#include "plan.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<int64_t> g_launches{0};
+
+void count_launch(int n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return MLA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
+
+bool page_size_supported(int32_t ps) { return ps == 8 || ps == 16 || ps == 32 || (ps >= 64 && ps % 64 == 0); }
+
+// Checks shared by the dense and sparse decode calls.
+int check_decode_common(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                        const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                        const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                        const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                        int32_t dcp_world, int32_t dcp_rank, float scale, void* out, int32_t out_dtype, float* lse,
+                        void* workspace) {
+  if (kv_cache_dtype != MLA_DTYPE_BF16)
+    return fail(MLA_ERR_UNSUPPORTED, "kv_cache_dtype %d: only a bf16 latent cache is served (FP8 not supported)",
+                kv_cache_dtype);
+  if (num_tokens < 0 || num_requests < 1 || num_heads < 1 || num_heads > mla::kMaxHeads)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: num_requests=%d num_tokens=%d num_heads=%d (heads in [1,%d])",
+                num_requests, num_tokens, num_heads, mla::kMaxHeads);
+  if (dcp_world < 1 || dcp_world > 64 || dcp_rank < 0 || dcp_rank >= dcp_world)
+    return fail(MLA_ERR_INVALID_ARG, "dcp_rank %d not in [0, dcp_world=%d) or dcp_world not in [1, 64]", dcp_rank,
+                dcp_world);
+  if (num_blocks < 1 || kv_cache == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "empty KV cache (num_blocks=%lld)", (long long)num_blocks);
+  if (!page_size_supported(page_size))
+    return fail(MLA_ERR_UNSUPPORTED, "page_size %d: supported are 8, 16, 32 and multiples of 64", page_size);
+  if (block_table_stride < 1) return fail(MLA_ERR_INVALID_ARG, "block_table_stride %d < 1", block_table_stride);
+  if (!q_nope || !q_pe || !block_table || !seq_lens || !query_start_loc || !out || !lse)
+    return fail(MLA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (q_nope_row_stride < mla::kNope || q_nope_row_stride % 8 || q_pe_row_stride < mla::kRope ||
+      q_pe_row_stride % 8)
+    return fail(MLA_ERR_INVALID_ARG, "query row strides %lld/%lld: need >= 512/64 and multiples of 8",
+                (long long)q_nope_row_stride, (long long)q_pe_row_stride);
+  if (!aligned(q_nope, 16) || !aligned(q_pe, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(block_table, 4))
+    return fail(MLA_ERR_INVALID_ARG, "misaligned pointer (q/cache/out need 16-byte alignment)");
+  if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_F32)
+    return fail(MLA_ERR_INVALID_ARG, "out_dtype %d: BF16 or F32", out_dtype);
+  if (!std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale is not finite");
+  if (workspace == nullptr || !aligned(workspace, 256))
+    return fail(MLA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                     int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
+                                     int32_t num_splits) {
+  if (dcp_world < 1) dcp_world = 1;
+  return mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, num_splits,
+                               current_sm_count())
+      .total;
+}
+
+int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                   const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                   const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                   int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
+                   void* out, int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
+                               kv_cache_dtype, block_table, block_table_stride, seq_lens, query_start_loc,
+                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                               workspace);
+  if (rc != MLA_OK) return rc;
+  if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
+    return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
+  if (num_tokens == 0) return ok();
+  const mla::DecodePlan plan = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len,
+                                                     dcp_world, num_splits, current_sm_count());
+  if (workspace_bytes < plan.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
+
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+
+  mla::SchedArgs sa{};
+  sa.seq_lens = seq_lens;
+  sa.query_start_loc = query_start_loc;
+  sa.num_requests = num_requests;
+  sa.num_tokens = num_tokens;
+  sa.num_heads = num_heads;
+  sa.dcp_world = dcp_world;
+  sa.dcp_rank = dcp_rank;
+  sa.rows_per_group = plan.rows_per_group;
+  sa.max_splits = plan.max_splits;
+  sa.target_tiles = plan.target_tiles;
+  sa.max_tiles = plan.max_tiles;
+  sa.max_partial_rows = (int32_t)plan.max_partial_rows;
+  sa.hdr = hdr;
+  sa.req = reinterpret_cast<mla::ReqInfo*>(ws + plan.off_req);
+  sa.tiles = reinterpret_cast<mla::Tile*>(ws + plan.off_tiles);
+  sa.tok2req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
+  sa.row_counts = row_counts;
+  mla::schedule_kernel<<<1, 1024, 0, st>>>(sa);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "schedule_kernel launch");
+  count_launch();
+
+  mla::DecodeArgs da{};
+  da.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  da.q_nope_stride = q_nope_row_stride;
+  da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  da.q_pe_stride = q_pe_row_stride;
+  da.kv = static_cast<const __nv_bfloat16*>(kv_cache);
+  da.num_blocks = num_blocks;
+  da.page_size = page_size;
+  da.block_table = block_table;
+  da.bt_stride = block_table_stride;
+  da.num_heads = num_heads;
+  da.dcp_world = dcp_world;
+  da.dcp_rank = dcp_rank;
+  da.scale = scale;
+  da.out = out;
+  da.out_f32 = out_dtype == MLA_DTYPE_F32;
+  da.lse = lse;
+  da.hdr = hdr;
+  da.req = sa.req;
+  da.tiles = sa.tiles;
+  da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
+  da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
+  da.num_tokens = num_tokens;
+  if ((e = mla::launch_decode_simt(da, plan.rows_per_group, false, plan.max_tiles, st)) != cudaSuccess)
+    return cuda_fail(e, "decode launch");
+  count_launch();
+
+  if (plan.max_splits > 1) {
+    mla::CombineArgs ca{};
+    ca.req = sa.req;
+    ca.tok2req = sa.tok2req;
+    ca.part_lse = da.part_lse;
+    ca.part_o = da.part_o;
+    ca.num_tokens = num_tokens;
+    ca.num_heads = num_heads;
+    ca.out = out;
+    ca.out_f32 = da.out_f32;
+    ca.lse = lse;
+    const int64_t rows = (int64_t)num_tokens * num_heads;
+    mla::combine_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(ca);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "combine launch");
+    count_launch();
+  }
+  return ok();
+}
+
+size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t dcp_world) {
+  (void)dcp_world;
+  return mla::make_sparse_plan(num_tokens, num_heads, topk).total;
+}
+
+int mla_sparse_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                          const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                          const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens,
+                          int32_t num_heads, const int32_t* topk_indices, int32_t topk, const int32_t* topk_valid,
+                          int32_t dcp_world, int32_t dcp_rank, float scale, void* out, int32_t out_dtype,
+                          float* lse, int32_t* local_counts, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
+                               kv_cache_dtype, block_table, block_table_stride, seq_lens, query_start_loc,
+                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                               workspace);
+  if (rc != MLA_OK) return rc;
+  if (!topk_indices || !topk_valid || !local_counts)
+    return fail(MLA_ERR_INVALID_ARG, "topk_indices, topk_valid and local_counts are required");
+  if (topk < 1 || topk > 65536) return fail(MLA_ERR_INVALID_ARG, "topk %d not in [1, 65536]", topk);
+  if (num_tokens == 0) return ok();
+  const mla::SparsePlan plan = mla::make_sparse_plan(num_tokens, num_heads, topk);
+  if (workspace_bytes < plan.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+
+  mla::SparseListArgs la{};
+  la.topk = topk_indices;
+  la.topk_valid = topk_valid;
+  la.seq_lens = seq_lens;
+  la.query_start_loc = query_start_loc;
+  la.num_requests = num_requests;
+  la.num_tokens = num_tokens;
+  la.topk_k = topk;
+  la.dcp_world = dcp_world;
+  la.dcp_rank = dcp_rank;
+  la.lists = reinterpret_cast<int32_t*>(ws + plan.off_lists);
+  la.local_counts = local_counts;
+  la.tok_req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
+  la.hdr = hdr;
+  if ((e = mla::launch_sparse_lists(la, st)) != cudaSuccess) return cuda_fail(e, "sparse list launch");
+  count_launch();
+
+  mla::DecodeArgs da{};
+  da.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  da.q_nope_stride = q_nope_row_stride;
+  da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  da.q_pe_stride = q_pe_row_stride;
+  da.kv = static_cast<const __nv_bfloat16*>(kv_cache);
+  da.num_blocks = num_blocks;
+  da.page_size = page_size;
+  da.block_table = block_table;
+  da.bt_stride = block_table_stride;
+  da.num_heads = num_heads;
+  da.dcp_world = dcp_world;
+  da.dcp_rank = dcp_rank;
+  da.scale = scale;
+  da.out = out;
+  da.out_f32 = out_dtype == MLA_DTYPE_F32;
+  da.lse = lse;
+  da.hdr = hdr;
+  da.lists = la.lists;
+  da.list_count = local_counts;
+  da.tok_req = la.tok_req;
+  da.list_stride = topk;
+  da.num_tokens = num_tokens;
+  da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
+  const int grid = num_tokens * da.groups_per_token;
+  if ((e = mla::launch_decode_simt(da, plan.rows_per_group, true, grid, st)) != cudaSuccess)
+    return cuda_fail(e, "sparse decode launch");
+  count_launch();
+  return ok();
+}
+
+int dcp_lse_merge(const void* partials, int32_t partial_dtype, const float* lses, const int32_t* valid_counts,
+                  const void* w_uv, int32_t dcp_world, int32_t num_tokens, int32_t num_heads, void* out,
+                  int32_t out_dtype, float* lse_out, void* stream) {
+  if (dcp_world < 1 || dcp_world > 64) return fail(MLA_ERR_INVALID_ARG, "dcp_world %d not in [1, 64]", dcp_world);
+  if (num_tokens < 0 || num_heads < 1 || num_heads > mla::kMaxHeads)
+    return fail(MLA_ERR_INVALID_ARG, "bad sizes: num_tokens=%d num_heads=%d", num_tokens, num_heads);
+  if (!partials || !lses || !out) return fail(MLA_ERR_INVALID_ARG, "partials, lses and out are required");
+  if (partial_dtype != MLA_DTYPE_BF16 && partial_dtype != MLA_DTYPE_F32)
+    return fail(MLA_ERR_INVALID_ARG, "partial_dtype %d: BF16 or F32", partial_dtype);
+  if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_F32)
+    return fail(MLA_ERR_INVALID_ARG, "out_dtype %d: BF16 or F32", out_dtype);
+  if (!aligned(partials, 16) || !aligned(out, 16) || !aligned(lses, 4) || (w_uv && !aligned(w_uv, 16)))
+    return fail(MLA_ERR_INVALID_ARG, "misaligned pointer (partials/out/w_uv need 16-byte alignment)");
+  if (num_tokens == 0) return ok();
+  mla::MergeArgs ma{};
+  ma.partials = partials;
+  ma.partial_f32 = partial_dtype == MLA_DTYPE_F32;
+  ma.lses = lses;
+  ma.valid_counts = valid_counts;
+  ma.w_uv = static_cast<const __nv_bfloat16*>(w_uv);
+  ma.dcp_world = dcp_world;
+  ma.num_tokens = num_tokens;
+  ma.num_heads = num_heads;
+  ma.out = out;
+  ma.out_f32 = out_dtype == MLA_DTYPE_F32;
+  ma.lse_out = lse_out;
+  cudaError_t e = mla::launch_merge(ma, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  count_launch();
+  return ok();
+}
+
+int64_t mla_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mla_workspace_status(const void* workspace, void* stream, int32_t* detail) {
+  if (!workspace) return fail(MLA_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int32_t h[2] = {0, 0};
+  e = cudaMemcpy(h, workspace, sizeof h, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (detail) *detail = h[1];
+  if (h[0] != 0) return fail(MLA_ERR_DEVICE_CHECK, "device check %d fired", h[1]);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// decode_kernels.h -- launchers of the decode, sparse-list and merge kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "decode_args.h"
+
+namespace mla {
+
+// CUDA-core decode over the tile list (dense) or over (token, head group)
+// pairs (sparse); grid = tile capacity (dense) or T * groups (sparse).
+cudaError_t launch_decode_simt(const DecodeArgs& a, int rows_per_group, bool sparse, int grid, cudaStream_t stream);
+
+struct SparseListArgs {
+  const int32_t* topk;        // [T, K]
+  const int32_t* topk_valid;  // [T]
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_requests, num_tokens, topk_k, dcp_world, dcp_rank;
+  int32_t* lists;         // [T, K] out: shard-local slots
+  int32_t* local_counts;  // [T] out
+  int32_t* tok_req;       // [T] out
+  WorkspaceHeader* hdr;
+};
+cudaError_t launch_sparse_lists(const SparseListArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+  const void* partials;  // [D, T, H, 512]
+  int32_t partial_f32;
+  const float* lses;             // [D, T, H]
+  const int32_t* valid_counts;   // [D, T] or NULL
+  const __nv_bfloat16* w_uv;     // [H, 512, 128] or NULL
+  int32_t dcp_world, num_tokens, num_heads;
+  void* out;
+  int32_t out_f32;
+  float* lse_out;  // or NULL
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+}  // namespace mla

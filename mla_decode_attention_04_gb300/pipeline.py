@@ -1,0 +1,74 @@
+"""One DCP decode step on one GPU: the D shard decodes, then the merge.
+
+On one device the D DCP shards are D disjoint slices of the cache in the same
+HBM, so the step is D calls of the shard decode (dense or sparse) writing into
+one [D, T, H, 512] partial buffer, and one call of the LSE merge (optionally
+fused with W_UV).  Everything here is argument marshalling around the C ABI;
+all buffers are allocated once by ``DcpStep`` so that a step allocates
+nothing and can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (KV_LORA_RANK, V_HEAD_DIM, decode_workspace_size, dcp_lse_merge, mla_dcp_decode, mla_sparse_dcp_decode,
+               sparse_workspace_size)
+
+
+class DcpStep:
+    """Preallocated buffers + the launch sequence of one decode step.
+
+    ``shards``: list of (kv_cache slice, block_table) per DCP rank.
+    ``partial_dtype``: dtype of the per-shard outputs handed to the merge
+    (float32 by default: the merge then adds no bf16 rounding of its inputs).
+    """
+
+    def __init__(self, q_nope, q_pe, shards, seq_lens, query_start_loc, max_query_len, max_seq_len, scale, w_uv=None,
+                 topk=None, topk_valid=None, partial_dtype=torch.float32, out_dtype=torch.bfloat16, num_splits=0,
+                 use_counts=True):
+        self.q_nope, self.q_pe, self.shards = q_nope, q_pe, shards
+        self.seq_lens, self.qsl = seq_lens, query_start_loc
+        self.max_query_len, self.max_seq_len, self.scale = int(max_query_len), int(max_seq_len), float(scale)
+        self.w_uv, self.topk, self.topk_valid = w_uv, topk, topk_valid
+        self.num_splits = num_splits
+        self.use_counts = use_counts
+        D = len(shards)
+        T, H = q_nope.shape[0], q_nope.shape[1]
+        dev = q_nope.device
+        self.D, self.T, self.H = D, T, H
+        self.partials = torch.empty((D, T, H, KV_LORA_RANK), dtype=partial_dtype, device=dev)
+        self.lses = torch.empty((D, T, H), dtype=torch.float32, device=dev)
+        self.counts = torch.empty((D, T), dtype=torch.int32, device=dev)
+        width = V_HEAD_DIM if w_uv is not None else KV_LORA_RANK
+        self.out = torch.empty((T, H, width), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        B = seq_lens.shape[0]
+        if topk is not None:
+            need = sparse_workspace_size(T, H, topk.shape[1], D)
+        else:
+            need = decode_workspace_size(B, T, H, max_query_len, max_seq_len, D, num_splits)
+        self.workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None):
+        for r, (cache, bt) in enumerate(self.shards):
+            if self.topk is not None:
+                mla_sparse_dcp_decode(self.q_nope, self.q_pe, cache, bt, self.seq_lens, self.qsl, self.topk,
+                                      self.topk_valid, self.D, r, self.scale, out=self.partials[r], lse=self.lses[r],
+                                      local_counts=self.counts[r], workspace=self.workspace, stream=stream)
+            else:
+                mla_dcp_decode(self.q_nope, self.q_pe, cache, bt, self.seq_lens, self.qsl, self.max_query_len,
+                               self.max_seq_len, self.D, r, self.scale, out=self.partials[r], lse=self.lses[r],
+                               row_counts=self.counts[r], num_splits=self.num_splits, workspace=self.workspace,
+                               stream=stream)
+        dcp_lse_merge(self.partials, self.lses, self.counts if self.use_counts else None, self.w_uv, out=self.out,
+                      lse_out=self.lse, stream=stream)
+        return self.out, self.lse
+
+
+def step_for_workload(w, partial_dtype=torch.float32, num_splits=0, sparse=None):
+    """DcpStep for a ``workloads.Workload`` already on the GPU."""
+    sparse = (w.topk is not None) if sparse is None else sparse
+    shards = [(s.cache, s.block_table) for s in w.shards]
+    return DcpStep(w.q_nope, w.q_pe, shards, w.seq_lens, w.query_start_loc, w.max_query_len, w.max_seq_len, w.scale,
+                   w_uv=w.w_uv, topk=w.topk if sparse else None, topk_valid=w.topk_valid if sparse else None,
+                   partial_dtype=partial_dtype, num_splits=num_splits)
