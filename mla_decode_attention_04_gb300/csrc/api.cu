@@ -141,13 +141,12 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   sa.dcp_world = dcp_world;
   sa.dcp_rank = dcp_rank;
   sa.rows_per_group = plan.rows_per_group;
-  sa.max_splits = plan.max_splits;
-  sa.target_tiles = plan.target_tiles;
-  sa.max_tiles = plan.max_tiles;
+  sa.grid = plan.grid;
+  sa.max_pairs = plan.max_pairs;
   sa.max_partial_rows = (int32_t)plan.max_partial_rows;
   sa.hdr = hdr;
   sa.req = reinterpret_cast<mla::ReqInfo*>(ws + plan.off_req);
-  sa.tiles = reinterpret_cast<mla::Tile*>(ws + plan.off_tiles);
+  sa.pairs = reinterpret_cast<mla::PairInfo*>(ws + plan.off_pairs);
   sa.tok2req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
   sa.row_counts = row_counts;
   mla::schedule_kernel<<<1, 1024, 0, st>>>(sa);
@@ -173,17 +172,20 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   da.lse = lse;
   da.hdr = hdr;
   da.req = sa.req;
-  da.tiles = sa.tiles;
+  da.pairs = sa.pairs;
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
   da.num_tokens = num_tokens;
-  if ((e = mla::launch_decode_simt(da, plan.rows_per_group, false, plan.max_tiles, st)) != cudaSuccess)
+  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, false, plan.grid, plan.grid, st)) != cudaSuccess)
     return cuda_fail(e, "decode launch");
   count_launch();
 
-  if (plan.max_splits > 1) {
+  {
     mla::CombineArgs ca{};
+    ca.hdr = hdr;
     ca.req = sa.req;
+    ca.pairs = sa.pairs;
+    ca.rows_per_group = plan.rows_per_group;
     ca.tok2req = sa.tok2req;
     ca.part_lse = da.part_lse;
     ca.part_o = da.part_o;
@@ -273,7 +275,7 @@ int mla_sparse_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const v
   da.num_tokens = num_tokens;
   da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
   const int grid = num_tokens * da.groups_per_token;
-  if ((e = mla::launch_decode_simt(da, plan.rows_per_group, true, grid, st)) != cudaSuccess)
+  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, true, grid, current_sm_count(), st)) != cudaSuccess)
     return cuda_fail(e, "sparse decode launch");
   count_launch();
   return ok();

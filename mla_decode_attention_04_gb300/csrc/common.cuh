@@ -27,37 +27,48 @@ enum DeviceCheck : int32_t {
 
 // Workspace header, at offset 0 of every decode workspace.
 struct WorkspaceHeader {
-  int32_t status;      // 0 or MLA_ERR_DEVICE_CHECK
-  int32_t detail;      // DeviceCheck code of the first failure
-  int32_t num_tiles;   // tiles written by the scheduler
-  int32_t pad[61];     // header is 256 bytes
+  int32_t status;       // 0 or MLA_ERR_DEVICE_CHECK
+  int32_t detail;       // DeviceCheck code of the first failure
+  int32_t num_pairs;    // (request, row group) pairs written by the scheduler
+  int32_t pad0;
+  int64_t total_items;  // key tiles over all pairs (0: nothing to run)
+  int32_t pad[58];      // header is 256 bytes
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header size");
 
-// One unit of decode work: rows [row0, row0 + nrows) of request b against its
-// local keys [key0, key1) (the KV chunk of split `split` of `nsplit`).
-struct Tile {
-  int32_t b;
-  int32_t row0;     // first row (i * H + h) of the request handled
-  int32_t key0;     // first local key of the chunk
-  int32_t key1;     // one past the last local key of the chunk
-  int32_t split;    // index of this chunk among the request's chunks
-  int32_t nsplit;   // chunks of this request (1 => write final output)
-  int32_t pbase;    // first partial slot of the request (nsplit > 1)
-  int32_t group;    // row-group index (row0 / rows_per_group)
-};
-
 // Per-request facts derived on the device by the scheduler.
 struct ReqInfo {
-  int32_t q0;       // query_start_loc[b]
+  int32_t q0;         // query_start_loc[b]
   int32_t q_len;
-  int32_t seq_len;  // global
-  int32_t local_len;
-  int32_t nsplit;
-  int32_t pbase;    // first partial slot (slot = pbase + split * rows + row)
-  int32_t rows;     // q_len * H
-  int32_t chunk;    // keys per split (multiple of kKeyTile)
+  int32_t seq_len;    // global
+  int32_t local_len;  // keys this shard holds
+  int32_t rows;       // q_len * H (token-major: row = i * H + h)
+  int32_t pair_base;  // first (request, row group) pair of the request
+  int32_t pad[2];
 };
+
+// One (request, row group): rows [row0, row0 + nrows) of request b and the
+// nt 64-key tiles of its local keys, which are the work items
+// [item0, item0 + nt) of the flattened list that the decode grid divides into
+// equal contiguous ranges.  A pair crossing range boundaries is computed in
+// nsplit chunks whose partial results sit at slots pbase + split * NR + row
+// and are merged by the combine kernel.
+struct PairInfo {
+  int64_t item0;
+  int32_t b;
+  int32_t row0;
+  int32_t nrows;
+  int32_t nt;
+  int32_t nsplit;
+  int32_t pbase;
+};
+static_assert(sizeof(PairInfo) == 32, "pair size");
+
+// CTA that owns work item i when W items are divided over G CTAs as
+// [floor(c W / G), floor((c + 1) W / G)).
+__host__ __device__ __forceinline__ int64_t item_owner(int64_t i, int64_t W, int64_t G) {
+  return ((i + 1) * G + W - 1) / W - 1;
+}
 
 __device__ __forceinline__ void record_check(WorkspaceHeader* hdr, int32_t code) {
   if (atomicCAS(&hdr->status, 0, (int32_t)MLA_ERR_DEVICE_CHECK) == 0) hdr->detail = code;

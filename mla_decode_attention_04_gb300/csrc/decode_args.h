@@ -23,7 +23,7 @@ struct DecodeArgs {
   WorkspaceHeader* hdr;
   // dense
   const ReqInfo* req;
-  const Tile* tiles;
+  const PairInfo* pairs;
   float* part_lse;
   float* part_o;
   // sparse

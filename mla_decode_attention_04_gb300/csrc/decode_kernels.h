@@ -7,9 +7,12 @@
 
 namespace mla {
 
-// CUDA-core decode over the tile list (dense) or over (token, head group)
-// pairs (sparse); grid = tile capacity (dense) or T * groups (sparse).
-cudaError_t launch_decode_simt(const DecodeArgs& a, int rows_per_group, bool sparse, int grid, cudaStream_t stream);
+// Tensor-core decode: min(max_units, num_sms) persistent CTAs over the
+// scheduler's balanced key-tile ranges (dense; max_units must then equal the
+// grid the scheduler planned for) or over the T * groups (token, head group)
+// units (sparse).
+cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool sparse, int max_units, int num_sms,
+                             cudaStream_t stream);
 
 struct SparseListArgs {
   const int32_t* topk;        // [T, K]
@@ -36,5 +39,7 @@ struct MergeArgs {
   float* lse_out;  // or NULL
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+// W_UV-fused merge on tensor cores (one CTA per head and 32 tokens).
+cudaError_t launch_merge_wuv_tc(const MergeArgs& a, cudaStream_t stream);
 
 }  // namespace mla

@@ -1,0 +1,545 @@
+// decode_tc.cu -- tensor-core (tcgen05 / TMEM) absorbed-MLA decode, dense and sparse.
+//
+// Math per (token, head) row, as in "vllm.v1.attention.backends.mla.
+// flashattn_mla" (_forward_decode: scores q_nope.kv_c + q_pe.k_pe, values
+// kv_c, softmax scale, LSE) with the per-row DCP key limit of the "[Attention]
+// add DCP support for FLASH_ATTN_MLA backend" mask tables, or with the
+// per-token key lists of sparse MLA.
+//
+// One CTA per SM walks work units (request or token, row group, KV chunk).
+// A unit's NR rows (NR = 16 or 32 (token, head) pairs) share every key, so
+// per 64-key tile:
+//   S  [128 lanes x 64]  = Q (TMEM, rows padded to 128 lanes) . KV^T   (K = 576)
+//   O^T[512 x NR]       += KV_c^T (smem, MN-major) . P^T (smem)        (K = 64)
+// The first product keeps the 64 keys on the MMA's N side, the second puts
+// the 512 latent dims on M and the few rows on N, so neither wastes the
+// tensor core on padding for the value product and O^T only needs 4*NR TMEM
+// columns next to Q (288) and S (64).
+//
+// Warp roles: producer (TMA tile loads through the block table; for sparse,
+// 4 warps of 16-byte cp.async row gathers), one MMA-issuing warp, and four
+// softmax warps (one per TMEM lane quarter) that also rescale O^T, zero the
+// value rows of keys past the chunk end, and write the outputs.  A 3-stage
+// shared-memory ring of 64-key tiles (72 KB each) keeps ~144 KB of KV loads
+// in flight per SM.  The online softmax rescales O^T lazily: the running
+// reference max only moves when a tile's max exceeds it by more than 2^8.
+#include "common.cuh"
+#include "decode_args.h"
+#include "decode_kernels.h"
+#include "tc_ptx.cuh"
+#include "tma_host.h"
+
+namespace mla {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kStages = 3;
+constexpr int kChunk = 64 * 128;        // one 64-key x 64-dim bf16 tile, SW128
+constexpr int kStageBytes = 9 * kChunk;  // 576 dims
+constexpr int kColQ = 0;                 // TMEM columns: Q [0, 288)
+constexpr int kColS = 288;               //               S [288, 352)
+constexpr int kColO = 352;               //               O^T [352, 352 + 4 NR)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct TcShared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t s_full, s_free, p_ready, unit_done, q_ready;
+  uint32_t tmem_base;
+  int32_t any_rescale[2];
+  float m_ref[32], l_sum[32], alpha[32], inv_l[32];
+};
+
+template <bool SPARSE>
+struct Roles {
+  static constexpr int kProducerWarps = SPARSE ? 4 : 1;
+  static constexpr int kMmaWarp = kProducerWarps;
+  static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
+  static constexpr int kThreads = (kProducerWarps + 5) * 32;
+};
+
+// Work unit description, identical for every role.
+struct Unit {
+  int b, row0, nrows, key0, key1, n_kt;
+  int q0, q_len, seq_len, local_len;
+  int split, nsplit, pbase;
+  int token;  // sparse: the token
+};
+
+// The sequence of units of one CTA.  Dense: the CTA's equal share
+// [c W / G, (c + 1) W / G) of the scheduler's flattened key-tile list, cut at
+// (request, row group) boundaries.  Sparse: (token, head group) units dealt
+// round-robin.  Every role walks the same sequence.
+template <int NR, bool SPARSE>
+struct UnitIter {
+  int64_t i, hi, W, G;
+  int num_pairs;
+  int u, units;
+
+  __device__ void init(const DecodeArgs& a) {
+    if constexpr (SPARSE) {
+      u = blockIdx.x;
+      units = a.num_tokens * a.groups_per_token;
+    } else {
+      W = a.hdr->total_items;
+      G = gridDim.x;
+      num_pairs = a.hdr->num_pairs;
+      i = (int64_t)blockIdx.x * W / G;
+      hi = ((int64_t)blockIdx.x + 1) * W / G;
+    }
+  }
+
+  __device__ bool next(const DecodeArgs& a, Unit& w) {
+    if constexpr (SPARSE) {
+      for (; u < units; u += gridDim.x) {
+        const int t = u / a.groups_per_token, g = u % a.groups_per_token;
+        w.token = t;
+        w.b = a.tok_req[t];
+        w.row0 = g * NR;
+        w.nrows = min(NR, a.num_heads - w.row0);
+        w.key0 = 0;
+        w.key1 = a.list_count[t];
+        w.split = 0;
+        w.nsplit = 1;
+        w.pbase = 0;
+        w.q0 = t;
+        w.q_len = 1;
+        w.seq_len = 0;
+        w.local_len = w.key1;
+        w.n_kt = (w.key1 + kKeyTile - 1) / kKeyTile;
+        u += gridDim.x;
+        if (w.b >= 0) return true;
+        u -= gridDim.x;
+      }
+      return false;
+    } else {
+      if (i >= hi) return false;
+      int lo = 0, up = num_pairs - 1;  // last pair with item0 <= i
+      while (lo < up) {
+        const int mid = (lo + up + 1) >> 1;
+        if (a.pairs[mid].item0 <= i) lo = mid; else up = mid - 1;
+      }
+      const PairInfo pi = a.pairs[lo];
+      const ReqInfo ri = a.req[pi.b];
+      const int64_t end = min(hi, pi.item0 + pi.nt);
+      w.token = -1;
+      w.b = pi.b;
+      w.row0 = pi.row0;
+      w.nrows = pi.nrows;
+      w.key0 = (int)(i - pi.item0) * kKeyTile;
+      w.key1 = min((int)(end - pi.item0) * kKeyTile, ri.local_len);
+      w.n_kt = (int)(end - i);
+      w.nsplit = pi.nsplit;
+      w.split = pi.nsplit > 1 ? (int)(item_owner(i, W, G) - item_owner(pi.item0, W, G)) : 0;
+      w.pbase = pi.pbase;
+      w.q0 = ri.q0;
+      w.q_len = ri.q_len;
+      w.seq_len = ri.seq_len;
+      w.local_len = ri.local_len;
+      i = end;
+      return true;
+    }
+  }
+};
+
+// cache slot (page * page_size + offset) of shard-local key j of request b, or -1
+__device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
+  const int pidx = j / a.page_size;
+  if (pidx >= a.bt_stride) return -1;
+  const int page = a.block_table[(int64_t)b * a.bt_stride + pidx];
+  if (page < 0 || page >= a.num_blocks) return -1;
+  return (int64_t)page * a.page_size + j % a.page_size;
+}
+
+template <int NR, bool SPARSE>
+__global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeArgs a) {
+  using R = Roles<SPARSE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* kv = base;                                  // [kStages][9][kChunk]
+  uint8_t* pT = base + kStages * kStageBytes;          // [NR][128 B] SW128 K-major
+  TcShared& sh = *reinterpret_cast<TcShared*>(pT + 4096);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == R::kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.full[s], SPARSE ? 32 * R::kProducerWarps : 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_free, 1);
+    mbar_init(&sh.p_ready, 1);
+    mbar_init(&sh.unit_done, 1);
+    mbar_init(&sh.q_ready, 1);
+    sh.any_rescale[0] = sh.any_rescale[1] = 0;
+    fence_mbar_init();
+  }
+  if (!SPARSE && threadIdx.x == 32 * R::kMmaWarp) prefetch_tmap(&kv_map);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  bool ok = true;
+
+  if (warp < R::kProducerWarps) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0;
+    if constexpr (!SPARSE) {
+      if (lane == 0) {
+        const uint64_t pol = policy_evict_first();
+        const int ps = a.page_size;
+        UnitIter<NR, SPARSE> it;
+        it.init(a);
+        Unit w;
+        while (ok && it.next(a, w)) {
+          for (int kt = 0; kt < w.n_kt && ok; ++kt) {
+            const int k = w.key0 + kt * kKeyTile;
+            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
+            uint8_t* dst = kv + stage * kStageBytes;
+            if (ps >= kKeyTile) {
+              const int64_t slot = slot_of(a, w.b, k);
+              if (slot < 0) {
+                record_check(a.hdr, kCheckPageOutOfRange);
+                mbar_arrive(&sh.full[stage]);
+              } else {
+                const int page = (int)(slot / ps), off = (int)(slot % ps);
+                mbar_arrive_expect_tx(&sh.full[stage], kStageBytes);
+                for (int c = 0; c < 9; ++c) tma_load_3d(dst + c * kChunk, &kv_map, c * 64, off, page, &sh.full[stage], pol);
+              }
+            } else {
+              const int nsub = kKeyTile / ps;
+              int pages[kKeyTile / 8];
+              int nvalid = 0;
+              for (int i = 0; i < nsub; ++i) {
+                const int j = k + i * ps;
+                pages[i] = -1;
+                if (j < w.local_len) {
+                  const int64_t slot = slot_of(a, w.b, j);
+                  if (slot < 0) record_check(a.hdr, kCheckPageOutOfRange);
+                  else { pages[i] = (int)(slot / ps); ++nvalid; }
+                }
+              }
+              mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nvalid * ps * 128 * 9));
+              for (int i = 0; i < nsub; ++i)
+                if (pages[i] >= 0)
+                  for (int c = 0; c < 9; ++c)
+                    tma_load_3d(dst + c * kChunk + i * ps * 128, &kv_map, c * 64, 0, pages[i], &sh.full[stage], pol);
+            }
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+        }
+      }
+    } else {
+      // sparse: 4 warps gather 64 rows x 72 16-byte pieces per tile with cp.async
+      const int pt = threadIdx.x;  // 0..127
+      UnitIter<NR, SPARSE> it;
+      it.init(a);
+      Unit w;
+      while (ok && it.next(a, w)) {
+        const int32_t* list = a.lists + (int64_t)w.token * a.list_stride;
+        for (int kt = 0; kt < w.n_kt && ok; ++kt) {
+          const int k0 = kt * kKeyTile;
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
+          uint8_t* dst = kv + stage * kStageBytes;
+          // thread pt handles key (pt / 2) and pieces [36 * (pt & 1), +36)
+          const int key = pt >> 1;
+          const int j = k0 + key;
+          int64_t slot = -1;
+          if (j < w.key1) {
+            slot = slot_of(a, w.b, list[j]);
+            if (slot < 0) record_check(a.hdr, kCheckPageOutOfRange);
+          }
+          const char* src = reinterpret_cast<const char*>(a.kv) + (slot < 0 ? 0 : slot) * (kRow * 2);
+          const uint32_t nbytes = slot < 0 ? 0u : 16u;
+          for (int q = 0; q < 36; ++q) {
+            const int piece = 36 * (pt & 1) + q;  // 0..71
+            const int cc = piece >> 3, within = piece & 7;
+            const uint32_t d = smem_u32(dst + cc * kChunk + key * 128 + ((within ^ (key & 7)) << 4));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src + piece * 16), "r"(nbytes)
+                         : "memory");
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[stage]))
+                       : "memory");
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  } else if (warp == R::kMmaWarp) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, j = 0, q_ph = 0;
+      const uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
+      const uint32_t id_pv = idesc_bf16_f32(128, NR, 1, 0);
+      const uint32_t pT_addr = smem_u32(pT);
+      UnitIter<NR, SPARSE> it;
+      it.init(a);
+      Unit w;
+      while (ok && it.next(a, w)) {
+        if (w.n_kt == 0) continue;
+        if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
+        q_ph ^= 1;
+        tc_fence_after();
+        for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
+          if (!mbar_wait(&sh.full[stage], phase) || !mbar_wait(&sh.s_free, (j & 1) ^ 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(kv + stage * kStageBytes);
+#pragma unroll 1
+          for (int c = 0; c < 9; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8,
+                     smem_desc_sw128(st + c * kChunk + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+          mma_commit(&sh.s_full);
+          if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + kColO + m * NR, smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024),
+                     smem_desc_sw128(pT_addr + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
+          mma_commit(&sh.empty[stage]);
+          if (kt == w.n_kt - 1) mma_commit(&sh.unit_done);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int sw = warp - R::kSoftmaxWarp0;   // 0..3
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int st_tid = sw * 32 + lane;        // 0..127 within the softmax group
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int row = lane * 4 + quarter;       // row owned by this thread (if < NR)
+    const bool row_thread = lane < NR / 4;
+    const float scale_log2 = a.scale * kLog2e;
+    const int H = a.num_heads;
+    uint32_t j = 0, u_ph = 0;
+    int stage = 0;
+    UnitIter<NR, SPARSE> it;
+    it.init(a);
+    Unit w;
+    while (ok && it.next(a, w)) {
+      // global (token, head) row index of unit row n
+      auto grow = [&](int n) -> int64_t {
+        if constexpr (SPARSE) return (int64_t)w.token * H + w.row0 + n;
+        else return (int64_t)w.q0 * H + w.row0 + n;
+      };
+      const bool partial = !SPARSE && w.nsplit > 1;
+      int kend = w.key0;  // keys [key0, kend) visible to this thread's row
+      if (row_thread && row < w.nrows) {
+        if constexpr (SPARSE) {
+          kend = w.key1;
+        } else {
+          const int i = (w.row0 + row) / H;
+          const int P = w.seq_len - w.q_len + i;
+          kend = min(visible_keys(P, a.dcp_world, a.dcp_rank), w.key1);
+        }
+      }
+      float m_ref = -INFINITY, l_sum = 0.f;
+
+      if (w.n_kt > 0) {
+        // Q rows -> TMEM lanes (quarter, lane): columns [0, 288) hold 576 bf16
+        const bool have = row_thread && row < w.nrows;
+        const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow(row) * a.q_nope_stride) : nullptr;
+        const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow(row) * a.q_pe_stride) : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 9; ++c) {
+          uint32_t r[32];
+          if (have) {
+            const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const uint4 x = src[v];
+              r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) r[v] = 0u;
+          }
+          tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) mbar_arrive(&sh.q_ready);
+      }
+
+      for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
+        if (!mbar_wait(&sh.s_full, j & 1)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s_lo[32], s_hi[32];
+        tmem_ld<32>(tmem + lane_base + kColS, s_lo);
+        tmem_ld<32>(tmem + lane_base + kColS + 32, s_hi);
+        tmem_wait_ld();
+        uint32_t s[64];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = s_lo[c];
+          s[32 + c] = s_hi[c];
+        }
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) {
+          mbar_arrive(&sh.s_free);
+          sh.any_rescale[(j + 1) & 1] = 0;
+        }
+        const int kbase = w.key0 + kt * kKeyTile;
+        if (row_thread) {
+          const int valid = max(0, min(kend - kbase, kKeyTile));
+          float tmax = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float v = c < valid ? __uint_as_float(s[c]) * scale_log2 : -INFINITY;
+            s[c] = __float_as_uint(v);
+            tmax = fmaxf(tmax, v);
+          }
+          float alpha = 1.f;
+          if (tmax > m_ref + kRescaleThreshold) {  // also the first finite max (m_ref = -inf)
+            alpha = exp2f(m_ref - tmax);           // 0 when m_ref = -inf
+            if (m_ref > -INFINITY) sh.any_rescale[j & 1] = 1;
+            l_sum *= alpha;
+            m_ref = tmax;
+          }
+          sh.alpha[row] = alpha;
+          float sum = 0.f;
+          uint32_t packed[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[c]) - m_ref) : 0.f;
+            const float p1 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[c + 1]) - m_ref) : 0.f;
+            sum += p0 + p1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            packed[c / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          l_sum += sum;
+          uint8_t* prow = pT + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        }
+        // value rows of keys past the chunk end: zero them (P is 0 there, and
+        // 0 * (garbage) must not reach the accumulator)
+        const int tile_valid = min(w.key1 - kbase, kKeyTile);
+        if (tile_valid < kKeyTile) {
+          uint8_t* st = kv + stage * kStageBytes;
+          const int nz = (kKeyTile - tile_valid) * 64;  // 16-byte pieces over 8 value chunks
+          for (int i = st_tid; i < nz; i += 128) {
+            const int key = tile_valid + (i >> 6), piece = i & 63;
+            *reinterpret_cast<uint4*>(st + (piece >> 3) * kChunk + key * 128 + ((piece & 7) << 4)) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        named_bar_sync(1, 128);
+        if (sh.any_rescale[j & 1]) {
+          // PV of the previous tile completed before S of this one (in-order tcgen05)
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+            uint32_t o[NR];
+            tmem_ld<NR>(tmem + lane_base + kColO + m * NR, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < NR; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * sh.alpha[n]);
+            tmem_st<NR>(tmem + lane_base + kColO + m * NR, o);
+          }
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) mbar_arrive(&sh.p_ready);
+        if (++stage == kStages) stage = 0;
+      }
+      if (!ok) break;
+
+      // ---- epilogue of the unit
+      if (w.n_kt > 0) {
+        if (!mbar_wait(&sh.unit_done, u_ph)) { ok = false; break; }
+        u_ph ^= 1;
+        tc_fence_after();
+      }
+      if (row_thread) {
+        const bool live = l_sum > 0.f && m_ref > -INFINITY;
+        sh.inv_l[row] = live ? 1.f / l_sum : 0.f;
+        if (row < w.nrows) {
+          const float lse = live ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
+          if (partial) a.part_lse[(int64_t)w.pbase + (int64_t)w.split * NR + row] = lse;
+          else a.lse[grow(row)] = lse;
+        }
+      }
+      named_bar_sync(1, 128);
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        uint32_t o[NR];
+        if (w.n_kt > 0) {
+          tmem_ld<NR>(tmem + lane_base + kColO + m * NR, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int n = 0; n < NR; ++n) o[n] = 0u;
+        }
+        const int dim = m * 128 + quarter * 32 + lane;
+#pragma unroll
+        for (int n = 0; n < NR; ++n) {
+          if (n >= w.nrows) break;
+          const float v = __uint_as_float(o[n]) * sh.inv_l[n];
+          if (partial) {
+            const int64_t slot = (int64_t)w.pbase + (int64_t)w.split * NR + n;
+            a.part_o[slot * kNope + dim] = v;
+          } else if (a.out_f32) {
+            static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
+          } else {
+            static_cast<__nv_bfloat16*>(a.out)[grow(n) * kNope + dim] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, 128);
+    }
+  }
+
+  if (!ok) record_check(a.hdr, kCheckWaitTimeout);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == R::kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+template <int NR, bool SPARSE>
+cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cudaStream_t stream) {
+  const size_t smem = 1024 + kStages * kStageBytes + 4096 + sizeof(TcShared);
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<NR, SPARSE><<<grid, Roles<SPARSE>::kThreads, smem, stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool sparse, int max_units, int num_sms,
+                             cudaStream_t stream) {
+  if (max_units <= 0) return cudaSuccess;
+  CUtensorMap map;
+  if (!make_kv_tensor_map(&map, a.kv, a.num_blocks, a.page_size)) return cudaErrorInvalidValue;
+  const int grid = max_units < num_sms ? max_units : num_sms;
+  if (sparse)
+    return rows_per_group == 16 ? launch_tc<16, true>(a, map, grid, stream) : launch_tc<32, true>(a, map, grid, stream);
+  return rows_per_group == 16 ? launch_tc<16, false>(a, map, grid, stream) : launch_tc<32, false>(a, map, grid, stream);
+}
+
+}  // namespace mla

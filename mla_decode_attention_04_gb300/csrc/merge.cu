@@ -94,55 +94,6 @@ __global__ void __launch_bounds__(256) merge_rows_kernel(MergeArgs a) {
   if (a.lse_out && lane == 0) a.lse_out[row] = lse;
 }
 
-// W_UV fused, CUDA cores: one CTA per (head, block of 16 tokens), 128 threads
-// (one per output column).  The merged rows are kept in fp32 in smem.
-constexpr int kTokBlock = 16;
-
-__global__ void __launch_bounds__(128) merge_wuv_simt_kernel(MergeArgs a) {
-  __shared__ float o_s[kTokBlock][kNope];
-  const int h = blockIdx.y;
-  const int t0 = blockIdx.x * kTokBlock;
-  const int T = a.num_tokens, H = a.num_heads;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int k = warp; k < kTokBlock; k += 4) {
-    const int t = t0 + k;
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    if (t < T) {
-      float w[kMaxD];
-      float lse;
-      if (merge_weights(a, t, h, w, &lse)) {
-        for (int r = 0; r < a.dcp_world; ++r)
-          if (w[r] != 0.f) accumulate_row(a, ((int64_t)r * T + t) * H + h, w[r], acc);
-      }
-      if (a.lse_out && lane == 0) a.lse_out[(int64_t)t * H + h] = lse;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) o_s[k][128 * i + 4 * lane + c] = acc[4 * i + c];
-  }
-  __syncthreads();
-  const int v = threadIdx.x;
-  float y[kTokBlock];
-#pragma unroll
-  for (int k = 0; k < kTokBlock; ++k) y[k] = 0.f;
-  const __nv_bfloat16* W = a.w_uv + (int64_t)h * kNope * kVHead + v;
-  for (int d = 0; d < kNope; ++d) {
-    const float wv = __bfloat162float(W[(int64_t)d * kVHead]);
-#pragma unroll
-    for (int k = 0; k < kTokBlock; ++k) y[k] = fmaf(o_s[k][d], wv, y[k]);
-  }
-  for (int k = 0; k < kTokBlock; ++k) {
-    const int t = t0 + k;
-    if (t >= T) break;
-    const int64_t idx = ((int64_t)t * H + h) * kVHead + v;
-    if (a.out_f32) static_cast<float*>(a.out)[idx] = y[k];
-    else static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(y[k]);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
@@ -151,11 +102,9 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     const int64_t rows = (int64_t)a.num_tokens * a.num_heads;
     const int grid = (int)((rows + 7) / 8);
     merge_rows_kernel<<<grid, 256, 0, stream>>>(a);
-  } else {
-    dim3 grid((a.num_tokens + kTokBlock - 1) / kTokBlock, a.num_heads);
-    merge_wuv_simt_kernel<<<grid, 128, 0, stream>>>(a);
+    return cudaGetLastError();
   }
-  return cudaGetLastError();
+  return launch_merge_wuv_tc(a, stream);
 }
 
 }  // namespace mla

@@ -12,20 +12,25 @@ struct SchedArgs {
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
   int32_t num_requests, num_tokens, num_heads, dcp_world, dcp_rank;
-  int32_t rows_per_group, max_splits, target_tiles, max_tiles, max_partial_rows;
+  int32_t rows_per_group;
+  int32_t grid;              // CTAs of the decode launch that the items are balanced over
+  int32_t max_pairs;
+  int32_t max_partial_rows;
   WorkspaceHeader* hdr;
   ReqInfo* req;
-  Tile* tiles;
+  PairInfo* pairs;
   int32_t* tok2req;
   int32_t* row_counts;  // may be NULL
 };
 
 struct CombineArgs {
+  const WorkspaceHeader* hdr;
   const ReqInfo* req;
+  const PairInfo* pairs;
   const int32_t* tok2req;
   const float* part_lse;
   const float* part_o;
-  int32_t num_tokens, num_heads;
+  int32_t num_tokens, num_heads, rows_per_group;
   void* out;
   int32_t out_f32;
   float* lse;
@@ -33,12 +38,11 @@ struct CombineArgs {
 
 // Where everything lives inside a dense-decode workspace (byte offsets).
 struct DecodePlan {
-  int32_t rows_per_group;   // rows (token, head) per tile: 16 or 32
-  int32_t max_splits;       // KV chunks per request at most
-  int32_t target_tiles;     // scheduler aims at this many tiles
-  int32_t max_tiles;        // capacity of the tile list
-  int64_t max_partial_rows; // capacity of the split partials
-  size_t off_req, off_tok, off_tiles, off_plse, off_po, total;
+  int32_t rows_per_group;    // rows (token, head) per work unit: 16 or 32
+  int32_t grid;              // decode CTAs
+  int32_t max_pairs;         // capacity of the (request, row group) list
+  int64_t max_partial_rows;  // capacity of the split partials
+  size_t off_req, off_tok, off_pairs, off_plse, off_po, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -46,32 +50,35 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_query_len, int32_t max_seq_len,
                                    int32_t D, int32_t num_splits, int32_t num_sms) {
   DecodePlan p{};
-  if (max_query_len < 1) max_query_len = 1;
+  if (max_query_len < 1) max_query_len = 1;  // the backend's capture-time clamp
+  if (D < 1) D = 1;
   p.rows_per_group = (int64_t)max_query_len * H <= 16 ? 16 : 32;
   const int64_t NR = p.rows_per_group;
-  p.target_tiles = 2 * (num_sms > 0 ? num_sms : 148);
-  const int64_t max_local = (max_seq_len + D - 1) / (D > 0 ? D : 1);
+  const int64_t max_local = (max_seq_len + D - 1) / D;
   const int64_t max_key_tiles = (max_local + kKeyTile - 1) / kKeyTile;
-  const int64_t groups_lb = ((int64_t)T * H + NR - 1) / NR;
-  int64_t ms;
+  const int64_t groups_ub = ((int64_t)T * H + NR - 1) / NR + B;  // >= sum_b ceil(q_len_b H / NR)
+  int64_t items_ub = groups_ub * max_key_tiles;
+  int64_t g = num_sms > 0 ? num_sms : 148;
+  // num_splits > 0 caps the grid at num_splits CTAs per row group; with
+  // balanced ranges a row group of average size is then cut into about
+  // num_splits KV chunks
   if (num_splits > 0) {
-    ms = num_splits;
-  } else {
-    ms = (p.target_tiles + (groups_lb > 0 ? groups_lb : 1) - 1) / (groups_lb > 0 ? groups_lb : 1);
-    if (ms > 64) ms = 64;
+    const int64_t groups_lb = ((int64_t)T * H + NR - 1) / NR;
+    const int64_t cap = (int64_t)num_splits * (groups_lb > 0 ? groups_lb : 1);
+    if (g > cap) g = cap;
   }
-  if (ms > max_key_tiles) ms = max_key_tiles;
-  if (ms < 1) ms = 1;
-  p.max_splits = (int32_t)ms;
-  p.max_tiles = (int32_t)((groups_lb + B) * ms);
-  p.max_partial_rows = ms > 1 ? ms * (int64_t)T * H : 0;
+  if (g > items_ub) g = items_ub;
+  if (g < 1) g = 1;
+  p.grid = (int32_t)g;
+  p.max_pairs = (int32_t)(groups_ub > 0 ? groups_ub : 1);
+  p.max_partial_rows = (groups_ub + g) * NR;
   size_t off = sizeof(WorkspaceHeader);
   p.off_req = off;
   off = align_up(off + sizeof(ReqInfo) * (size_t)(B > 0 ? B : 1), 256);
   p.off_tok = off;
   off = align_up(off + sizeof(int32_t) * (size_t)(T > 0 ? T : 1), 256);
-  p.off_tiles = off;
-  off = align_up(off + sizeof(Tile) * (size_t)(p.max_tiles > 0 ? p.max_tiles : 1), 256);
+  p.off_pairs = off;
+  off = align_up(off + sizeof(PairInfo) * (size_t)p.max_pairs, 256);
   p.off_plse = off;
   off = align_up(off + sizeof(float) * (size_t)p.max_partial_rows, 256);
   p.off_po = off;
@@ -80,7 +87,7 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   return p;
 }
 
-// Sparse decode workspace: header, then the per-token shard-local key lists.
+// Sparse decode workspace: header, token -> request map, per-token lists.
 struct SparsePlan {
   int32_t rows_per_group;
   size_t off_tok, off_lists, total;

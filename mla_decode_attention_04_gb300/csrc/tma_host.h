@@ -1,0 +1,41 @@
+// tma_host.h -- host-side creation of TMA tensor maps (driver entry point
+// obtained through the runtime, so the library links no driver stub).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+namespace mla {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Tensor map over a paged latent cache [num_blocks][page_size][576] bf16 with a
+// box of 64 columns (128 bytes, 128-byte swizzle) x min(page_size, 64) rows x 1
+// page.  Returns false on failure.
+inline bool make_kv_tensor_map(CUtensorMap* map, const void* kv, int64_t num_blocks, int32_t page_size) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {576, (cuuint64_t)page_size, (cuuint64_t)num_blocks};
+  const cuuint64_t strides[2] = {576 * 2, (cuuint64_t)page_size * 576 * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)(page_size < 64 ? page_size : 64), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mla
