@@ -304,6 +304,22 @@ def profile_traffic(kernel_tag):
         return None
 
 
+def replica_max_ms(step_ms, device):
+    """Slowest rank's step time (every rank runs an independent replica of the
+    workload; the job is done when the slowest one is)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return step_ms
+    t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank, world, step_ms):
+    """Query tokens of all ranks per second of the slowest rank's step."""
+    return tokens_per_rank * world / (step_ms * 1e-3)
+
+
 def run_ours(args):
     import mla_decode_attention_04_gb300 as mla
     from mla_decode_attention_04_gb300 import build as mla_build
@@ -330,14 +346,9 @@ def run_ours(args):
         wall = time.perf_counter() - t0
     clocks = clk.summary()
     s = summarize(head, pk)
-    step_ms = s["ms_per_step"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = replica_max_ms(s["ms_per_step"], "cuda")
     tokens = head["work"]["tokens"]
-    value = tokens * world / (step_ms * 1e-3)
+    value = whole_job_value(tokens, world, step_ms)
 
     configs = {}
     if args.configs != "headline" and rank == 0:
