@@ -45,12 +45,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+constexpr int kPBytes = 32 * 128;  // one P^T buffer: up to 32 rows x 64 keys bf16
+
 struct TcShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t s_full, s_free, p_ready, unit_done, q_ready;
+  uint64_t s_full, s_free, p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
+  int32_t wait_ok;  // result of the softmax group's last mbarrier wait
   float m_ref[32], l_sum[32], alpha[32], inv_l[32];
 };
 
@@ -162,8 +165,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* kv = base;                                  // [kStages][9][kChunk]
-  uint8_t* pT = base + kStages * kStageBytes;          // [NR][128 B] SW128 K-major
-  TcShared& sh = *reinterpret_cast<TcShared*>(pT + 4096);
+  uint8_t* pT = base + kStages * kStageBytes;          // 2 x [NR][128 B] SW128 K-major
+  TcShared& sh = *reinterpret_cast<TcShared*>(pT + 2 * kPBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -179,6 +182,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.s_free, 1);
     mbar_init(&sh.p_ready, 1);
+    mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.unit_done, 1);
     mbar_init(&sh.q_ready, 1);
     sh.any_rescale[0] = sh.any_rescale[1] = 0;
@@ -287,33 +291,47 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       UnitIter<NR, SPARSE> it;
       it.init(a);
       Unit w;
+      // S(j) = Q . KV(j)^T into the single S buffer; the softmax warps copy S
+      // to registers and release it (s_free) before working on it, so QK^T of
+      // tile j+1 is issued ahead of PV of tile j and overlaps the softmax.
+      auto issue_qk = [&](uint32_t jj, int stg, uint32_t ph) -> bool {
+        if (!mbar_wait(&sh.full[stg], ph) || !mbar_wait(&sh.s_free, (jj & 1) ^ 1)) return false;
+        tc_fence_after();
+        const uint32_t st = smem_u32(kv + stg * kStageBytes);
+#pragma unroll 1
+        for (int c = 0; c < 9; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8,
+                   smem_desc_sw128(st + c * kChunk + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+        mma_commit(&sh.s_full);
+        return true;
+      };
       while (ok && it.next(a, w)) {
         if (w.n_kt == 0) continue;
         if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
         q_ph ^= 1;
         tc_fence_after();
+        if (!issue_qk(j, stage, phase)) { ok = false; break; }
         for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-          if (!mbar_wait(&sh.full[stage], phase) || !mbar_wait(&sh.s_free, (j & 1) ^ 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = smem_u32(kv + stage * kStageBytes);
-#pragma unroll 1
-          for (int c = 0; c < 9; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8,
-                     smem_desc_sw128(st + c * kChunk + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
-          mma_commit(&sh.s_full);
+          const int nstage = stage + 1 == kStages ? 0 : stage + 1;
+          const uint32_t nphase = stage + 1 == kStages ? phase ^ 1 : phase;
+          if (kt + 1 < w.n_kt && !issue_qk(j + 1, nstage, nphase)) { ok = false; break; }
           if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
           tc_fence_after();
+          const uint32_t st = smem_u32(kv + stage * kStageBytes);
+          const uint32_t pb = pT_addr + (j & 1) * kPBytes;
 #pragma unroll 1
           for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tmem + kColO + m * NR, smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024),
-                     smem_desc_sw128(pT_addr + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
+                     smem_desc_sw128(pb + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
           mma_commit(&sh.empty[stage]);
+          mma_commit(&sh.pv_done);
           if (kt == w.n_kt - 1) mma_commit(&sh.unit_done);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          stage = nstage;
+          phase = nphase;
         }
       }
     }
@@ -329,6 +347,17 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     const int H = a.num_heads;
     uint32_t j = 0, u_ph = 0;
     int stage = 0;
+    // One thread waits; the named barrier hands its verdict to the group, so
+    // the 128 threads always take the same branch (no thread is left at a
+    // barrier the others skipped).  Consecutive calls are separated by at
+    // least one more group barrier, so the flag is not overwritten early.
+    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (st_tid == 0) sh.wait_ok = mbar_wait(bar, parity) ? 1 : 0;
+      named_bar_sync(1, 128);
+      const bool r = sh.wait_ok != 0;
+      tc_fence_after();
+      return r;
+    };
     UnitIter<NR, SPARSE> it;
     it.init(a);
     Unit w;
@@ -379,8 +408,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-        if (!mbar_wait(&sh.s_full, j & 1)) { ok = false; break; }
-        tc_fence_after();
+        if (!group_wait(&sh.s_full, j & 1)) { ok = false; break; }
         uint32_t s_lo[32], s_hi[32];
         tmem_ld<32>(tmem + lane_base + kColS, s_lo);
         tmem_ld<32>(tmem + lane_base + kColS + 32, s_hi);
@@ -426,7 +454,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             packed[c / 2] = *reinterpret_cast<uint32_t*>(&h2);
           }
           l_sum += sum;
-          uint8_t* prow = pT + (row >> 3) * 1024 + (row & 7) * 128;
+          // P^T buffer j & 1: PV(j - 2) read it and completed before this tile
+          // (tile j - 1 waited for PV(j - 2) before releasing its P)
+          uint8_t* prow = pT + (j & 1) * kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
@@ -444,9 +474,15 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
                 make_uint4(0, 0, 0, 0);
           }
         }
-        named_bar_sync(1, 128);
+        // PV of the previous tile must be complete before O^T is rescaled and
+        // before this tile's P is released (waited every tile, in order); the
+        // barrier inside group_wait also publishes any_rescale
+        if (j > 0) {
+          if (!group_wait(&sh.pv_done, (j - 1) & 1)) { ok = false; break; }
+        } else {
+          named_bar_sync(1, 128);
+        }
         if (sh.any_rescale[j & 1]) {
-          // PV of the previous tile completed before S of this one (in-order tcgen05)
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
             uint32_t o[NR];
@@ -468,9 +504,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 
       // ---- epilogue of the unit
       if (w.n_kt > 0) {
-        if (!mbar_wait(&sh.unit_done, u_ph)) { ok = false; break; }
+        if (!group_wait(&sh.unit_done, u_ph)) { ok = false; break; }
         u_ph ^= 1;
-        tc_fence_after();
       }
       if (row_thread) {
         const bool live = l_sum > 0.f && m_ref > -INFINITY;
@@ -521,7 +556,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 
 template <int NR, bool SPARSE>
 cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cudaStream_t stream) {
-  const size_t smem = 1024 + kStages * kStageBytes + 4096 + sizeof(TcShared);
+  const size_t smem = 1024 + kStages * kStageBytes + 2 * kPBytes + sizeof(TcShared);
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
