@@ -14,7 +14,11 @@
 // The first product keeps the 64 keys on the MMA's N side, the second puts
 // the 512 latent dims on M and the few rows on N, so neither wastes the
 // tensor core on padding for the value product and O^T only needs 4*NR TMEM
-// columns next to Q (288) and S (64).
+// columns next to Q (288) and S (64).  P enters the value product as two
+// bf16 terms (hi + lo, both accumulated into O^T), so the probabilities keep
+// fp32-level precision; the extra MMA re-reads only the small P operand.
+// The MMA warp issues QK^T of tile j+1 before PV of tile j, so the score
+// product overlaps the softmax.
 //
 // Warp roles: producer (TMA tile loads through the block table; for sparse,
 // 4 warps of 16-byte cp.async row gathers), one MMA-issuing warp, and four
@@ -45,7 +49,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-constexpr int kPBytes = 32 * 128;  // one P^T buffer: up to 32 rows x 64 keys bf16
+// P^T (up to 32 rows x 64 keys, bf16, SW128 K-major) lives in the k_pe chunk
+// of the tile's own stage, free once QK^T of the tile is done: P as bf16
+// hi at offset 0 and lo = bf16(P - hi) at offset kPBytes.
+constexpr int kPBytes = 32 * 128;
+constexpr int kPChunk = 8;  // the k_pe chunk of a stage
 
 struct TcShared {
   uint64_t full[kStages];
@@ -88,11 +96,16 @@ struct UnitIter {
       u = blockIdx.x;
       units = a.num_tokens * a.groups_per_token;
     } else {
+      // the scheduler balanced the W items over min(grid, W) non-empty ranges
       W = a.hdr->total_items;
-      G = gridDim.x;
+      G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
       num_pairs = a.hdr->num_pairs;
-      i = (int64_t)blockIdx.x * W / G;
-      hi = ((int64_t)blockIdx.x + 1) * W / G;
+      if ((int64_t)blockIdx.x < G) {
+        i = (int64_t)blockIdx.x * W / G;
+        hi = ((int64_t)blockIdx.x + 1) * W / G;
+      } else {
+        i = hi = 0;
+      }
     }
   }
 
@@ -165,8 +178,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* kv = base;                                  // [kStages][9][kChunk]
-  uint8_t* pT = base + kStages * kStageBytes;          // 2 x [NR][128 B] SW128 K-major
-  TcShared& sh = *reinterpret_cast<TcShared*>(pT + 2 * kPBytes);
+  TcShared& sh = *reinterpret_cast<TcShared*>(base + kStages * kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -287,7 +299,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       uint32_t phase = 0, j = 0, q_ph = 0;
       const uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_pv = idesc_bf16_f32(128, NR, 1, 0);
-      const uint32_t pT_addr = smem_u32(pT);
       UnitIter<NR, SPARSE> it;
       it.init(a);
       Unit w;
@@ -320,13 +331,15 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(kv + stage * kStageBytes);
-          const uint32_t pb = pT_addr + (j & 1) * kPBytes;
+          const uint32_t pb = st + kPChunk * kChunk;  // P hi; P lo at + kPBytes
 #pragma unroll 1
           for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + kColO + m * NR, smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024),
-                     smem_desc_sw128(pb + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t va = smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024);
+              mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
+              mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kPBytes + kk * 32, 16, 1024), id_pv, 1);
+            }
           mma_commit(&sh.empty[stage]);
           mma_commit(&sh.pv_done);
           if (kt == w.n_kt - 1) mma_commit(&sh.unit_done);
@@ -443,24 +456,31 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             m_ref = tmax;
           }
           sh.alpha[row] = alpha;
+          // P^T row in the k_pe chunk of this tile's stage (QK^T of the tile,
+          // its only reader, is complete): bf16 hi, and lo = bf16(P - hi) so
+          // that hi + lo carries P to ~2^-17 through the bf16 MMA
+          uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + (row >> 3) * 1024 + (row & 7) * 128;
           float sum = 0.f;
-          uint32_t packed[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[c]) - m_ref) : 0.f;
-            const float p1 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[c + 1]) - m_ref) : 0.f;
-            sum += p0 + p1;
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            packed[c / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = 8 * c + 2 * e;
+              const float p0 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[k]) - m_ref) : 0.f;
+              const float p1 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[k + 1]) - m_ref) : 0.f;
+              sum += p0 + p1;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+              const float2 hf = __bfloat1622float2(h2);
+              const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+              hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            const int off = (c ^ (row & 7)) << 4;
+            *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(prow + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
           l_sum += sum;
-          // P^T buffer j & 1: PV(j - 2) read it and completed before this tile
-          // (tile j - 1 waited for PV(j - 2) before releasing its P)
-          uint8_t* prow = pT + (j & 1) * kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         }
         // value rows of keys past the chunk end: zero them (P is 0 there, and
         // 0 * (garbage) must not reach the accumulator)
@@ -556,7 +576,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 
 template <int NR, bool SPARSE>
 cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cudaStream_t stream) {
-  const size_t smem = 1024 + kStages * kStageBytes + 2 * kPBytes + sizeof(TcShared);
+  const size_t smem = 1024 + kStages * kStageBytes + sizeof(TcShared);
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

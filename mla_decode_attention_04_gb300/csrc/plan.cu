@@ -128,7 +128,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     item_carry += item_tot;
   }
   __syncthreads();
-  const long long W = item_carry, G = a.grid;
+  // balance over min(grid, W) ranges so that no range is empty: then every
+  // range boundary inside a pair starts a real chunk and the chunk index of
+  // a unit is its owner minus the owner of the pair's first item
+  const long long W = item_carry, G = (long long)a.grid < W ? (long long)a.grid : (W > 0 ? W : 1);
 
   // pass 2: chunks per pair (how many CTA ranges cut it) and partial slots
   long long part_carry = 0;

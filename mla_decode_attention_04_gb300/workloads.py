@@ -147,7 +147,8 @@ def custom(seq_lens, q_lens, num_heads, dcp_world, page_size=64, seed=0, q_std=1
     for r in range(D):
         shard_tokens.append([np.arange(r, L, D, dtype=np.int64) for L in seq_lens])
     pages_per_req = [[-(-len(tok) // ps) for tok in shard_tokens[r]] for r in range(D)]
-    num_pages = [sum(p) + spare_pages for p in pages_per_req]
+    # every shard owns at least one page (a cache allocation is never empty)
+    num_pages = [max(1, sum(p) + spare_pages) for p in pages_per_req]
     page_base = np.zeros(D, dtype=np.int64)
     page_base[1:] = np.cumsum(num_pages)[:-1]
     total_pages = max(1, int(sum(num_pages)))
