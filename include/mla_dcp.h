@@ -201,6 +201,44 @@ int dcp_lse_merge(const void *partials, int32_t partial_dtype, const float *lses
 int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
 
 /* ------------------------------------------------------------------------
+ * mla_dcp_decode_static_scratch -- mla_dcp_decode for callers that cannot
+ * allocate device memory.  No counterpart on the pages; it exists for users
+ * of this library, not for the method.
+ *
+ * Some callers cannot call cudaMalloc (or anything that allocates) when they
+ * run a decode step: code working inside a device-memory budget fixed at
+ * start-up, engines whose only allocator is their own pre-reserved pool, or
+ * latency-critical paths where allocation is forbidden.  They cannot provide
+ * the workspace mla_dcp_decode asks for.  This variant takes the same
+ * arguments minus the workspace and uses a fixed array of
+ * MLA_STATIC_SCRATCH_BYTES in the library's device memory instead.
+ *
+ *  - The array exists on every GPU that loads the library and stays
+ *    allocated until the process exits.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture on the device.
+ *  - Problems whose scratch (mla_dcp_decode_workspace_size) exceeds the
+ *    array are refused with MLA_ERR_WORKSPACE before anything runs.
+ *  - Every call shares the one array: calls that may overlap on the GPU
+ *    (unordered streams) race on it.  Calls on one stream are fine.  The
+ *    array keeps the last call's contents; what must start at zero (the
+ *    status word) is cleared by each call.
+ *  - mla_workspace_status() cannot reach this array; device checks of this
+ *    variant are not reported.
+ *  - It allocates nothing and calls no allocating routine.
+ * ---------------------------------------------------------------------- */
+#define MLA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int mla_dcp_decode_static_scratch(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe,
+                                  int64_t q_pe_row_stride, const void *kv_cache, int64_t num_blocks, int32_t page_size,
+                                  int32_t kv_cache_dtype, const int32_t *block_table, int32_t block_table_stride,
+                                  const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_requests,
+                                  int32_t num_tokens, int32_t num_heads, int32_t max_query_len, int32_t max_seq_len,
+                                  int32_t dcp_world, int32_t dcp_rank, float scale, void *out, int32_t out_dtype,
+                                  float *lse, int32_t *row_counts, int32_t num_splits, void *stream);
+
+/* ------------------------------------------------------------------------
  * mla_kernel_launch_count -- number of kernels this library has launched in
  * this process so far (all threads; memsets excluded).  Lets a caller state
  * how many of the library's kernels ran inside a timed region.

@@ -31,7 +31,13 @@ MLA_DTYPE_BF16, MLA_DTYPE_F32, MLA_DTYPE_FP8_E4M3 = 0, 1, 2
 EXPORTS = [
     "mla_last_error", "mla_dcp_decode_workspace_size", "mla_dcp_decode", "mla_sparse_dcp_decode_workspace_size",
     "mla_sparse_dcp_decode", "dcp_lse_merge", "mla_workspace_status", "mla_kernel_launch_count",
+    "mla_dcp_decode_static_scratch",
 ]
+
+# Size of the library's fixed device scratch array used by
+# mla_dcp_decode_static_scratch (the entry point for callers that cannot
+# allocate device memory); see include/mla_dcp.h.
+MLA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class MlaError(RuntimeError):
@@ -63,6 +69,9 @@ def _bind(lib):
     lib.mla_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_kernel_launch_count.restype = i64
     lib.mla_kernel_launch_count.argtypes = []
+    lib.mla_dcp_decode_static_scratch.restype = ctypes.c_int
+    lib.mla_dcp_decode_static_scratch.argtypes = [vp, i64, vp, i64, vp, i64, i32, i32, vp, i32, vp, vp, i32, i32, i32,
+                                                  i32, i32, i32, i32, f32, vp, i32, vp, vp, i32, vp]
     return lib
 
 

@@ -93,6 +93,11 @@ int check_decode_common(const void* q_nope, int64_t q_nope_row_stride, const voi
 
 }  // namespace
 
+namespace mla {
+// Lets other translation units of the library report through mla_last_error.
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
