@@ -59,7 +59,7 @@ def peaks():
 # ------------------------------------------------------------ algorithmic work
 
 
-def work_of(w):
+def work_of(w, partial_bytes=4):
     """Algorithmic KV bytes, FLOPs and merge bytes of one step of workload w."""
     L = w.seq_lens.cpu().numpy().astype(np.int64)
     qsl = w.query_start_loc.cpu().numpy().astype(np.int64)
@@ -91,7 +91,7 @@ def work_of(w):
         flops = int(used.sum()) * H * FLOPS_PER_KEY_ROW
     T = w.num_tokens
     out_w = 128 if w.w_uv is not None else 512
-    merge_bytes = D * T * H * (512 * 4 + 4) + D * T * 4 + T * H * (out_w * 2 + 4)
+    merge_bytes = D * T * H * (512 * partial_bytes + 4) + D * T * 4 + T * H * (out_w * 2 + 4)
     if w.w_uv is not None:
         merge_bytes += H * 512 * 128 * 2
     q_bytes = T * H * 576 * 2
@@ -171,7 +171,7 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
 
     w = wl.NAMED[name](device="cuda")
     step = pipeline.step_for_workload(w)
-    work = work_of(w)
+    work = work_of(w, step.partials.element_size())
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if l2_flush else None
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -382,7 +382,8 @@ def run_ours(args):
         "config": {"workload": DESCR[HEADLINE],
                    "l2": "256 MB buffer written before every timed step (KV 302 MB > 129 MB L2 as well)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "partials": "fp32 per-shard outputs into the merge"},
+                   "partials": f"{str(head['step'].partials.dtype).replace('torch.', '')} per-shard outputs "
+                               "into the merge (fp32 where W_UV follows)"},
         "kv_gbs": s["kv_gbs"],
         "tflops": s["tflops"],
         "step_roofline_frac": s["step_roofline_frac"],

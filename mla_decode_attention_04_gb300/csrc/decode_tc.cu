@@ -14,9 +14,9 @@
 // The first product keeps the 64 keys on the MMA's N side, the second puts
 // the 512 latent dims on M and the few rows on N, so neither wastes the
 // tensor core on padding for the value product and O^T only needs 4*NR TMEM
-// columns next to Q (288) and S (64).  P enters the value product as two
-// bf16 terms (hi + lo, both accumulated into O^T), so the probabilities keep
-// fp32-level precision; the extra MMA re-reads only the small P operand.
+// columns next to Q (288) and S (64).  For fp32 outputs P enters the value
+// product as two bf16 terms (hi + lo, both accumulated into O^T), so the
+// probabilities keep fp32-level precision; for bf16 outputs one bf16 term.
 // The MMA warp issues QK^T of tile j+1 before PV of tile j, so the score
 // product overlaps the softmax.
 //
@@ -181,6 +181,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   TcShared& sh = *reinterpret_cast<TcShared*>(base + kStages * kStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // fp32 outputs get P as bf16 hi + lo (fp32-level probabilities); bf16
+  // outputs get bf16 P, already finer than the output rounding
+  const bool p_split = a.out_f32 != 0;
 
   if (warp == R::kMmaWarp) {
     tmem_alloc(&sh.tmem_base, 512);
@@ -338,7 +341,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t va = smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024);
               mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
-              mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kPBytes + kk * 32, 16, 1024), id_pv, 1);
+              if (p_split)
+                mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kPBytes + kk * 32, 16, 1024), id_pv, 1);
             }
           mma_commit(&sh.empty[stage]);
           mma_commit(&sh.pv_done);
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             }
             const int off = (c ^ (row & 7)) << 4;
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(prow + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            if (p_split) *reinterpret_cast<uint4*>(prow + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
           l_sum += sum;
         }

@@ -19,12 +19,14 @@ class DcpStep:
     """Preallocated buffers + the launch sequence of one decode step.
 
     ``shards``: list of (kv_cache slice, block_table) per DCP rank.
-    ``partial_dtype``: dtype of the per-shard outputs handed to the merge
-    (float32 by default: the merge then adds no bf16 rounding of its inputs).
+    ``partial_dtype``: dtype of the per-shard outputs handed to the merge.
+    ``None`` picks float32 when the merge projects through W_UV (whose
+    unit-scale weights amplify input rounding by about sqrt(512)) and bfloat16
+    otherwise (the 512-wide merge keeps bf16 partials well inside tolerance).
     """
 
     def __init__(self, q_nope, q_pe, shards, seq_lens, query_start_loc, max_query_len, max_seq_len, scale, w_uv=None,
-                 topk=None, topk_valid=None, partial_dtype=torch.float32, out_dtype=torch.bfloat16, num_splits=0,
+                 topk=None, topk_valid=None, partial_dtype=None, out_dtype=torch.bfloat16, num_splits=0,
                  use_counts=True):
         self.q_nope, self.q_pe, self.shards = q_nope, q_pe, shards
         self.seq_lens, self.qsl = seq_lens, query_start_loc
@@ -36,6 +38,8 @@ class DcpStep:
         T, H = q_nope.shape[0], q_nope.shape[1]
         dev = q_nope.device
         self.D, self.T, self.H = D, T, H
+        if partial_dtype is None:
+            partial_dtype = torch.float32 if w_uv is not None else torch.bfloat16
         self.partials = torch.empty((D, T, H, KV_LORA_RANK), dtype=partial_dtype, device=dev)
         self.lses = torch.empty((D, T, H), dtype=torch.float32, device=dev)
         self.counts = torch.empty((D, T), dtype=torch.int32, device=dev)
@@ -65,7 +69,7 @@ class DcpStep:
         return self.out, self.lse
 
 
-def step_for_workload(w, partial_dtype=torch.float32, num_splits=0, sparse=None):
+def step_for_workload(w, partial_dtype=None, num_splits=0, sparse=None):
     """DcpStep for a ``workloads.Workload`` already on the GPU."""
     sparse = (w.topk is not None) if sparse is None else sparse
     shards = [(s.cache, s.block_table) for s in w.shards]
