@@ -215,48 +215,60 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     if constexpr (!SPARSE) {
-      if (lane == 0) {
-        const uint64_t pol = policy_evict_first();
-        const int ps = a.page_size;
-        UnitIter<NR, SPARSE> it;
-        it.init(a);
-        Unit w;
-        while (ok && it.next(a, w)) {
-          for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-            const int k = w.key0 + kt * kKeyTile;
-            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
-            uint8_t* dst = kv + stage * kStageBytes;
-            if (ps >= kKeyTile) {
-              const int64_t slot = slot_of(a, w.b, k);
-              if (slot < 0) {
-                record_check(a.hdr, kCheckPageOutOfRange);
-                mbar_arrive(&sh.full[stage]);
+      // The whole warp walks the units; lane l holds the page id of block-
+      // table column (cache_col + l), refilled 32 columns at a time, so the
+      // block-table reads of 32 pages cost one memory latency.  Lane 0 waits
+      // for free stages and issues the TMA loads.
+      const uint64_t pol = policy_evict_first();
+      const int ps = a.page_size;
+      const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
+      UnitIter<NR, SPARSE> it;
+      it.init(a);
+      Unit w;
+      int cache_b = -1, cache_col = 0, my_page = -1;
+      while (ok && it.next(a, w)) {
+        for (int kt = 0; kt < w.n_kt && ok; ++kt) {
+          const int k = w.key0 + kt * kKeyTile;
+          int pages[kKeyTile / 8];
+          int nvalid = 0;
+#pragma unroll 1
+          for (int i = 0; i < nsub; ++i) {
+            const int j = k + i * ps;  // first key of this page's part of the tile
+            const int col = j / ps;
+            if (w.b != cache_b || col < cache_col || col >= cache_col + 32) {
+              cache_b = w.b;
+              cache_col = col;
+              const int c2 = col + lane;
+              const int last_col = (w.local_len - 1) / ps;
+              my_page = (c2 <= last_col && c2 < a.bt_stride) ? a.block_table[(int64_t)w.b * a.bt_stride + c2] : -1;
+            }
+            const int page = __shfl_sync(0xffffffffu, my_page, col - cache_col);
+            pages[i] = -1;
+            if (j < w.local_len) {
+              if (page < 0 || page >= a.num_blocks || col >= a.bt_stride) {
+                if (lane == 0) record_check(a.hdr, kCheckPageOutOfRange);
               } else {
-                const int page = (int)(slot / ps), off = (int)(slot % ps);
-                mbar_arrive_expect_tx(&sh.full[stage], kStageBytes);
-                for (int c = 0; c < 9; ++c) tma_load_3d(dst + c * kChunk, &kv_map, c * 64, off, page, &sh.full[stage], pol);
+                pages[i] = page;
+                ++nvalid;
               }
+            }
+          }
+          if (lane == 0) {
+            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) {
+              ok = false;
             } else {
-              const int nsub = kKeyTile / ps;
-              int pages[kKeyTile / 8];
-              int nvalid = 0;
-              for (int i = 0; i < nsub; ++i) {
-                const int j = k + i * ps;
-                pages[i] = -1;
-                if (j < w.local_len) {
-                  const int64_t slot = slot_of(a, w.b, j);
-                  if (slot < 0) record_check(a.hdr, kCheckPageOutOfRange);
-                  else { pages[i] = (int)(slot / ps); ++nvalid; }
-                }
-              }
-              mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nvalid * ps * 128 * 9));
+              uint8_t* dst = kv + stage * kStageBytes;
+              const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
+              mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)nvalid * rows * 128u * 9u);
+              const int off = ps >= kKeyTile ? k % ps : 0;
               for (int i = 0; i < nsub; ++i)
                 if (pages[i] >= 0)
                   for (int c = 0; c < 9; ++c)
-                    tma_load_3d(dst + c * kChunk + i * ps * 128, &kv_map, c * 64, 0, pages[i], &sh.full[stage], pol);
+                    tma_load_3d(dst + c * kChunk + i * ps * 128, &kv_map, c * 64, off, pages[i], &sh.full[stage], pol);
             }
-            if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
     } else {
@@ -308,16 +320,25 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       // S(j) = Q . KV(j)^T into the single S buffer; the softmax warps copy S
       // to registers and release it (s_free) before working on it, so QK^T of
       // tile j+1 is issued ahead of PV of tile j and overlaps the softmax.
+      // Descriptors are linear in the start address (its field is addr >> 4
+      // and every address here is below 256 KB), so each operand is a base
+      // descriptor plus a constant offset in 16-byte units: the issue loops
+      // below are fully unrolled with no descriptor arithmetic per MMA.
+      const uint32_t kv0 = smem_u32(kv);
+      const uint64_t d_kv = smem_desc_sw128(kv0, 16, 1024);                 // K-major KV rows (QK^T B)
+      const uint64_t d_v = smem_desc_sw128(kv0, 8192, 1024);                // MN-major kv_c (PV A)
+      const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T (PV B)
+      constexpr uint64_t kStageUnits = kStageBytes >> 4;
       auto issue_qk = [&](uint32_t jj, int stg, uint32_t ph) -> bool {
         if (!mbar_wait(&sh.full[stg], ph) || !mbar_wait(&sh.s_free, (jj & 1) ^ 1)) return false;
         tc_fence_after();
-        const uint32_t st = smem_u32(kv + stg * kStageBytes);
-#pragma unroll 1
+        const uint64_t b0 = d_kv + (uint64_t)stg * kStageUnits;
+#pragma unroll
         for (int c = 0; c < 9; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8,
-                   smem_desc_sw128(st + c * kChunk + kk * 32, 16, 1024), id_qk, (c | kk) != 0);
+            mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8, b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk,
+                   (c | kk) != 0);
         mma_commit(&sh.s_full);
         return true;
       };
@@ -333,16 +354,16 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           if (kt + 1 < w.n_kt && !issue_qk(j + 1, nstage, nphase)) { ok = false; break; }
           if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = smem_u32(kv + stage * kStageBytes);
-          const uint32_t pb = st + kPChunk * kChunk;  // P hi; P lo at + kPBytes
-#pragma unroll 1
+          const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
+          const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
+          const uint32_t first = kt == 0 ? 0u : 1u;
+#pragma unroll
           for (int m = 0; m < 4; ++m)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t va = smem_desc_sw128(st + 2 * m * kChunk + kk * 2048, 8192, 1024);
-              mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kk * 32, 16, 1024), id_pv, (kt | kk) != 0);
-              if (p_split)
-                mma_ss(tmem + kColO + m * NR, va, smem_desc_sw128(pb + kPBytes + kk * 32, 16, 1024), id_pv, 1);
+              const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
+              mma_ss(tmem + kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
+              if (p_split) mma_ss(tmem + kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
             }
           mma_commit(&sh.empty[stage]);
           mma_commit(&sh.pv_done);
@@ -402,21 +423,28 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         const bool have = row_thread && row < w.nrows;
         const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow(row) * a.q_nope_stride) : nullptr;
         const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow(row) * a.q_pe_stride) : nullptr;
+        // three 64-dim chunks per batch: all their loads are in flight before
+        // the first store, so a unit pays three load latencies, not nine
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
-          uint32_t r[32];
-          if (have) {
+        for (int cb = 0; cb < 9; cb += 3) {
+          uint4 x[24];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const int c = cb + q;
             const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const uint4 x = src[v];
-              r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-            }
-          } else {
-#pragma unroll
-            for (int v = 0; v < 32; ++v) r[v] = 0u;
+            for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
           }
-          tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
+              r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
+            }
+            tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
