@@ -62,8 +62,17 @@ struct TcShared {
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
-  float m_ref[32], l_sum[32], alpha[32], inv_l[32];
+  float alpha[32], inv_l[32];
+  float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
+  float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
 };
+
+// 2^x with the hardware ex2 instruction (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <bool SPARSE>
 struct Roles {
@@ -379,8 +388,19 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int st_tid = sw * 32 + lane;        // 0..127 within the softmax group
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int row = lane * 4 + quarter;       // row owned by this thread (if < NR)
-    const bool row_thread = lane < NR / 4;
+    // Every unit row is replicated over TPR TMEM lanes (the M = 128 rows of
+    // QK^T cost the same whether padded or not), so each softmax thread owns
+    // KPT of the 64 keys of one row.  Lane l of quarter q holds row l % NR and
+    // key slice q * (32 / NR) + l / NR: the slice is uniform over a warp (or
+    // over each half-warp for NR = 16), so each thread reads just its own
+    // columns of S.  The row max is reduced through shared memory; each thread
+    // keeps a partial row sum until the unit's epilogue.
+    constexpr int TPR = 128 / NR;          // lanes per row: 8 or 4
+    constexpr int KPT = kKeyTile / TPR;    // keys per thread: 8 or 16
+    constexpr int RPW = 32 / NR;           // replicas of a row inside one warp: 2 or 1
+    const int row = lane % NR;             // unit row of this lane
+    const int kslice = quarter * RPW + lane / NR;  // keys [kslice * KPT, + KPT) of the tile
+    const bool row_lead = kslice == 0;     // writes the row's shared values
     const float scale_log2 = a.scale * kLog2e;
     const int H = a.num_heads;
     uint32_t j = 0, u_ph = 0;
@@ -407,7 +427,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       };
       const bool partial = !SPARSE && w.nsplit > 1;
       int kend = w.key0;  // keys [key0, kend) visible to this thread's row
-      if (row_thread && row < w.nrows) {
+      if (row < w.nrows) {
         if constexpr (SPARSE) {
           kend = w.key1;
         } else {
@@ -419,8 +439,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       float m_ref = -INFINITY, l_sum = 0.f;
 
       if (w.n_kt > 0) {
-        // Q rows -> TMEM lanes (quarter, lane): columns [0, 288) hold 576 bf16
-        const bool have = row_thread && row < w.nrows;
+        // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
+        // (the TPR lanes of a row read the same addresses: one request per warp)
+        const bool have = row < w.nrows;
         const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow(row) * a.q_nope_stride) : nullptr;
         const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow(row) * a.q_pe_stride) : nullptr;
         // three 64-dim chunks per batch: all their loads are in flight before
@@ -454,65 +475,73 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
         if (!group_wait(&sh.s_full, j & 1)) { ok = false; break; }
-        uint32_t s_lo[32], s_hi[32];
-        tmem_ld<32>(tmem + lane_base + kColS, s_lo);
-        tmem_ld<32>(tmem + lane_base + kColS + 32, s_hi);
-        tmem_wait_ld();
-        uint32_t s[64];
+        // this thread's KPT columns of its lane's row of S
+        float s[KPT];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s[c] = s_lo[c];
-          s[32 + c] = s_hi[c];
+        for (int r = 0; r < RPW; ++r) {
+          uint32_t v[KPT];
+          tmem_ld<KPT>(tmem + lane_base + kColS + (quarter * RPW + r) * KPT, v);
+          tmem_wait_ld();
+          if (lane / NR == r) {
+#pragma unroll
+            for (int e = 0; e < KPT; ++e) s[e] = __uint_as_float(v[e]);
+          }
         }
+        const int kbase = w.key0 + kt * kKeyTile;
+        const int valid = max(0, min(kend - kbase, kKeyTile));
+        float pmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          const float v = kslice * KPT + e < valid ? s[e] * scale_log2 : -INFINITY;
+          s[e] = v;
+          pmax = fmaxf(pmax, v);
+        }
+        sh.red[j & 1][kslice][row] = pmax;
         tc_fence_before();
         named_bar_sync(1, 128);
         if (st_tid == 0) {
           mbar_arrive(&sh.s_free);
           sh.any_rescale[(j + 1) & 1] = 0;
         }
-        const int kbase = w.key0 + kt * kKeyTile;
-        if (row_thread) {
-          const int valid = max(0, min(kend - kbase, kKeyTile));
+        {
           float tmax = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float v = c < valid ? __uint_as_float(s[c]) * scale_log2 : -INFINITY;
-            s[c] = __float_as_uint(v);
-            tmax = fmaxf(tmax, v);
-          }
+          for (int k = 0; k < TPR; ++k) tmax = fmaxf(tmax, sh.red[j & 1][k][row]);
           float alpha = 1.f;
           if (tmax > m_ref + kRescaleThreshold) {  // also the first finite max (m_ref = -inf)
-            alpha = exp2f(m_ref - tmax);           // 0 when m_ref = -inf
-            if (m_ref > -INFINITY) sh.any_rescale[j & 1] = 1;
+            alpha = fast_exp2(m_ref - tmax);       // 0 when m_ref = -inf
+            if (m_ref > -INFINITY && row_lead) sh.any_rescale[j & 1] = 1;
             l_sum *= alpha;
             m_ref = tmax;
           }
-          sh.alpha[row] = alpha;
-          // P^T row in the k_pe chunk of this tile's stage (QK^T of the tile,
-          // its only reader, is complete): bf16 hi, and lo = bf16(P - hi) so
-          // that hi + lo carries P to ~2^-17 through the bf16 MMA
+          if (row_lead) sh.alpha[row] = alpha;
+          // P^T in the k_pe chunk of this tile's stage (QK^T of the tile, its
+          // only reader, is complete).  For fp32 outputs P goes in as bf16 hi
+          // and lo = bf16(P - hi), so hi + lo carries P to ~2^-17.
           uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + (row >> 3) * 1024 + (row & 7) * 128;
           float sum = 0.f;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c8 = 0; c8 < KPT / 8; ++c8) {
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int k = 8 * c + 2 * e;
-              const float p0 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[k]) - m_ref) : 0.f;
-              const float p1 = m_ref > -INFINITY ? exp2f(__uint_as_float(s[k + 1]) - m_ref) : 0.f;
+              const float p0 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e] - m_ref) : 0.f;
+              const float p1 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e + 1] - m_ref) : 0.f;
               sum += p0 + p1;
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-              const float2 hf = __bfloat1622float2(h2);
-              const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
               hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-              lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+              if (p_split) {
+                const float2 hf = __bfloat1622float2(h2);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+              }
             }
-            const int off = (c ^ (row & 7)) << 4;
+            const int piece = kslice * (KPT / 8) + c8;  // 16-byte piece (8 keys) of the row
+            const int off = (piece ^ (row & 7)) << 4;
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             if (p_split) *reinterpret_cast<uint4*>(prow + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
-          l_sum += sum;
+          l_sum += sum;  // this thread's part of the row sum (same alpha for every part)
         }
         // value rows of keys past the chunk end: zero them (P is 0 there, and
         // 0 * (garbage) must not reach the accumulator)
@@ -559,11 +588,16 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         if (!group_wait(&sh.unit_done, u_ph)) { ok = false; break; }
         u_ph ^= 1;
       }
-      if (row_thread) {
-        const bool live = l_sum > 0.f && m_ref > -INFINITY;
-        sh.inv_l[row] = live ? 1.f / l_sum : 0.f;
+      sh.lpart[kslice][row] = l_sum;
+      named_bar_sync(1, 128);
+      if (row_lead) {
+        float lt = 0.f;
+#pragma unroll
+        for (int k = 0; k < TPR; ++k) lt += sh.lpart[k][row];
+        const bool live = lt > 0.f && m_ref > -INFINITY;
+        sh.inv_l[row] = live ? 1.f / lt : 0.f;
         if (row < w.nrows) {
-          const float lse = live ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
+          const float lse = live ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
           if (partial) a.part_lse[(int64_t)w.pbase + (int64_t)w.split * NR + row] = lse;
           else a.lse[grow(row)] = lse;
         }
