@@ -43,8 +43,14 @@ constexpr int kStages = 3;
 constexpr int kChunk = 64 * 128;        // one 64-key x 64-dim bf16 tile, SW128
 constexpr int kStageBytes = 9 * kChunk;  // 576 dims
 constexpr int kColQ = 0;                 // TMEM columns: Q [0, 288)
-constexpr int kColS = 288;               //               S [288, 352)
-constexpr int kColO = 352;               //               O^T [352, 352 + 4 NR)
+constexpr int kColS = 288;               //               S buffers [288, 288 + 64 SBUF)
+// S is double-buffered when TMEM has room (NR = 16: 288 + 2*64 + 4*16 = 480
+// columns), so QK^T of tile j+1 runs while the softmax reads S of tile j.
+template <int NR> struct TmemPlan {
+  static constexpr int kSBufs = NR == 16 ? 2 : 1;
+  static constexpr int kColO = kColS + kSBufs * 64;  // O^T [kColO, kColO + 4 NR)
+  static_assert(kColO + 4 * NR <= 512, "TMEM budget");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -58,7 +64,7 @@ constexpr int kPChunk = 8;  // the k_pe chunk of a stage
 struct TcShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t s_full, s_free, p_ready, pv_done, unit_done, q_ready;
+  uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
@@ -193,6 +199,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   // fp32 outputs get P as bf16 hi + lo (fp32-level probabilities); bf16
   // outputs get bf16 P, already finer than the output rounding
   const bool p_split = a.out_f32 != 0;
+  constexpr int SB = TmemPlan<NR>::kSBufs;
 
   if (warp == R::kMmaWarp) {
     tmem_alloc(&sh.tmem_base, 512);
@@ -203,8 +210,10 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       mbar_init(&sh.full[s], SPARSE ? 32 * R::kProducerWarps : 1);
       mbar_init(&sh.empty[s], 1);
     }
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.s_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.s_free[b], 1);
+    }
     mbar_init(&sh.p_ready, 1);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.unit_done, 1);
@@ -339,16 +348,18 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T (PV B)
       constexpr uint64_t kStageUnits = kStageBytes >> 4;
       auto issue_qk = [&](uint32_t jj, int stg, uint32_t ph) -> bool {
-        if (!mbar_wait(&sh.full[stg], ph) || !mbar_wait(&sh.s_free, (jj & 1) ^ 1)) return false;
+        // S buffer jj % SB was last read by the softmax for tile jj - SB
+        const int sb = jj % SB;
+        if (!mbar_wait(&sh.full[stg], ph) || !mbar_wait(&sh.s_free[sb], ((jj / SB) & 1) ^ 1)) return false;
         tc_fence_after();
         const uint64_t b0 = d_kv + (uint64_t)stg * kStageUnits;
 #pragma unroll
         for (int c = 0; c < 9; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColS, tmem + kColQ + (c * 4 + kk) * 8, b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk,
+            mma_ts(tmem + kColS + sb * 64, tmem + kColQ + (c * 4 + kk) * 8, b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk,
                    (c | kk) != 0);
-        mma_commit(&sh.s_full);
+        mma_commit(&sh.s_full[sb]);
         return true;
       };
       while (ok && it.next(a, w)) {
@@ -371,8 +382,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-              mma_ss(tmem + kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
-              if (p_split) mma_ss(tmem + kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+              mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
+              if (p_split) mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
             }
           mma_commit(&sh.empty[stage]);
           mma_commit(&sh.pv_done);
@@ -474,13 +485,13 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-        if (!group_wait(&sh.s_full, j & 1)) { ok = false; break; }
+        if (!group_wait(&sh.s_full[j % SB], (j / SB) & 1)) { ok = false; break; }
         // this thread's KPT columns of its lane's row of S
         float s[KPT];
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
           uint32_t v[KPT];
-          tmem_ld<KPT>(tmem + lane_base + kColS + (quarter * RPW + r) * KPT, v);
+          tmem_ld<KPT>(tmem + lane_base + kColS + (j % SB) * 64 + (quarter * RPW + r) * KPT, v);
           tmem_wait_ld();
           if (lane / NR == r) {
 #pragma unroll
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         tc_fence_before();
         named_bar_sync(1, 128);
         if (st_tid == 0) {
-          mbar_arrive(&sh.s_free);
+          mbar_arrive(&sh.s_free[j % SB]);
           sh.any_rescale[(j + 1) & 1] = 0;
         }
         {
@@ -567,11 +578,11 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
             uint32_t o[NR];
-            tmem_ld<NR>(tmem + lane_base + kColO + m * NR, o);
+            tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
             tmem_wait_ld();
 #pragma unroll
             for (int n = 0; n < NR; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * sh.alpha[n]);
-            tmem_st<NR>(tmem + lane_base + kColO + m * NR, o);
+            tmem_st<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
           }
           tmem_wait_st();
         }
@@ -607,7 +618,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       for (int m = 0; m < 4; ++m) {
         uint32_t o[NR];
         if (w.n_kt > 0) {
-          tmem_ld<NR>(tmem + lane_base + kColO + m * NR, o);
+          tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
