@@ -347,11 +347,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint64_t d_v = smem_desc_sw128(kv0, 8192, 1024);                // MN-major kv_c (PV A)
       const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T (PV B)
       constexpr uint64_t kStageUnits = kStageBytes >> 4;
-      auto issue_qk = [&](uint32_t jj, int stg, uint32_t ph) -> bool {
-        // S buffer jj % SB was last read by the softmax for tile jj - SB
+      auto issue_qk = [&](uint32_t jj, int stg) {
         const int sb = jj % SB;
-        if (!mbar_wait(&sh.full[stg], ph) || !mbar_wait(&sh.s_free[sb], ((jj / SB) & 1) ^ 1)) return false;
-        tc_fence_after();
         const uint64_t b0 = d_kv + (uint64_t)stg * kStageUnits;
 #pragma unroll
         for (int c = 0; c < 9; ++c)
@@ -360,36 +357,61 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             mma_ts(tmem + kColS + sb * 64, tmem + kColQ + (c * 4 + kk) * 8, b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk,
                    (c | kk) != 0);
         mma_commit(&sh.s_full[sb]);
-        return true;
+      };
+      auto issue_pv = [&](int stg, bool first_of_unit) {
+        const uint64_t v0 = d_v + (uint64_t)stg * kStageUnits;
+        const uint64_t p0 = d_p + (uint64_t)stg * kStageUnits;  // P hi; P lo at + kPBytes
+        const uint32_t first = first_of_unit ? 0u : 1u;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
+            mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
+            if (p_split) mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+          }
+        mma_commit(&sh.empty[stg]);
+        mma_commit(&sh.pv_done);
       };
       while (ok && it.next(a, w)) {
         if (w.n_kt == 0) continue;
         if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
         q_ph ^= 1;
         tc_fence_after();
-        if (!issue_qk(j, stage, phase)) { ok = false; break; }
-        for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-          const int nstage = stage + 1 == kStages ? 0 : stage + 1;
-          const uint32_t nphase = stage + 1 == kStages ? phase ^ 1 : phase;
-          if (kt + 1 < w.n_kt && !issue_qk(j + 1, nstage, nphase)) { ok = false; break; }
-          if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
-          const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
-          const uint32_t first = kt == 0 ? 0u : 1u;
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-              mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
-              if (p_split) mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
-            }
-          mma_commit(&sh.empty[stage]);
-          mma_commit(&sh.pv_done);
-          if (kt == w.n_kt - 1) mma_commit(&sh.unit_done);
-          stage = nstage;
-          phase = nphase;
+        // Issue QK^T of tile jq and PV of tile j (j < jq) in whichever order
+        // their inputs arrive: PV(j) as soon as P(j) is ready (this frees the
+        // ring stage for the next load), QK^T(jq) as soon as its tile has
+        // landed and its S buffer has been read.  Both in tile order.
+        const uint32_t j0 = j, jend = j + w.n_kt;
+        uint32_t jq = j;
+        int qstage = stage;
+        uint32_t qphase = phase;
+        uint64_t t_last = global_ns();
+        while (j < jend) {
+          bool did = false;
+          if (j < jq && mbar_test_wait(&sh.p_ready, j & 1)) {
+            tc_fence_after();
+            issue_pv(stage, j == j0);
+            if (j + 1 == jend) mma_commit(&sh.unit_done);
+            ++j;
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+            did = true;
+          } else if (jq < jend && mbar_test_wait(&sh.full[qstage], qphase) &&
+                     mbar_test_wait(&sh.s_free[jq % SB], ((jq / SB) & 1) ^ 1)) {
+            tc_fence_after();
+            issue_qk(jq, qstage);
+            ++jq;
+            if (++qstage == kStages) { qstage = 0; qphase ^= 1; }
+            did = true;
+          }
+          if (did) {
+            t_last = global_ns();
+          } else if (global_ns() - t_last > 2000000000ull) {
+            ok = false;
+            break;
+          } else {
+            __nanosleep(32);  // leave issue slots to the softmax warp sharing this SM sub-partition
+          }
         }
       }
     }
