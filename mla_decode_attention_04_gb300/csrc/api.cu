@@ -134,9 +134,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
 
-  cudaError_t e = cudaMemsetAsync(hdr, 0, 16, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
-
+  cudaError_t e;
   mla::SchedArgs sa{};
   sa.seq_lens = seq_lens;
   sa.query_start_loc = query_start_loc;
@@ -153,7 +151,11 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   sa.req = reinterpret_cast<mla::ReqInfo*>(ws + plan.off_req);
   sa.pairs = reinterpret_cast<mla::PairInfo*>(ws + plan.off_pairs);
   sa.tok2req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
+  sa.pair_done = reinterpret_cast<int32_t*>(ws + plan.off_cnt);
   sa.row_counts = row_counts;
+  sa.out = out;
+  sa.out_f32 = out_dtype == MLA_DTYPE_F32;
+  sa.lse = lse;
   mla::schedule_kernel<<<1, 1024, 0, st>>>(sa);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "schedule_kernel launch");
   count_launch();
@@ -178,6 +180,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   da.hdr = hdr;
   da.req = sa.req;
   da.pairs = sa.pairs;
+  da.pair_done = sa.pair_done;
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
   da.num_tokens = num_tokens;
@@ -185,25 +188,6 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
     return cuda_fail(e, "decode launch");
   count_launch();
 
-  {
-    mla::CombineArgs ca{};
-    ca.hdr = hdr;
-    ca.req = sa.req;
-    ca.pairs = sa.pairs;
-    ca.rows_per_group = plan.rows_per_group;
-    ca.tok2req = sa.tok2req;
-    ca.part_lse = da.part_lse;
-    ca.part_o = da.part_o;
-    ca.num_tokens = num_tokens;
-    ca.num_heads = num_heads;
-    ca.out = out;
-    ca.out_f32 = da.out_f32;
-    ca.lse = lse;
-    const int64_t rows = (int64_t)num_tokens * num_heads;
-    mla::combine_kernel<<<(int)((rows + 7) / 8), 256, 0, st>>>(ca);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "combine launch");
-    count_launch();
-  }
   return ok();
 }
 

@@ -24,6 +24,7 @@ struct DecodeArgs {
   // dense
   const ReqInfo* req;
   const PairInfo* pairs;
+  int32_t* pair_done;  // finished KV chunks per pair (the last finisher merges)
   float* part_lse;
   float* part_o;
   // sparse

@@ -68,6 +68,7 @@ struct TcShared {
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
+  int32_t is_last;  // this CTA finished the last KV chunk of its pair
   float alpha[32], inv_l[32];
   float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
   float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
@@ -93,6 +94,7 @@ struct Unit {
   int b, row0, nrows, key0, key1, n_kt;
   int q0, q_len, seq_len, local_len;
   int split, nsplit, pbase;
+  int pair;   // dense: index of the (request, row group) pair
   int token;  // sparse: the token
 };
 
@@ -129,6 +131,7 @@ struct UnitIter {
       for (; u < units; u += gridDim.x) {
         const int t = u / a.groups_per_token, g = u % a.groups_per_token;
         w.token = t;
+        w.pair = -1;
         w.b = a.tok_req[t];
         w.row0 = g * NR;
         w.nrows = min(NR, a.num_heads - w.row0);
@@ -158,6 +161,7 @@ struct UnitIter {
       const ReqInfo ri = a.req[pi.b];
       const int64_t end = min(hi, pi.item0 + pi.nt);
       w.token = -1;
+      w.pair = lo;
       w.b = pi.b;
       w.row0 = pi.row0;
       w.nrows = pi.nrows;
@@ -662,6 +666,48 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
       tc_fence_before();
+      if (partial) {
+        // The CTA that finishes a pair's last KV chunk merges the chunks by
+        // LSE (threadfence-reduction pattern: publish, count, re-fence, read).
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[w.pair], 1) == w.nsplit - 1;
+        named_bar_sync(1, 128);
+        if (sh.is_last) {
+          __threadfence();
+          const int d0 = st_tid * 4;  // 4 of the 512 latent dims per thread
+          for (int n = 0; n < w.nrows; ++n) {
+            const float* pl = a.part_lse + w.pbase + n;
+            float m = -INFINITY;
+            for (int sp = 0; sp < w.nsplit; ++sp) m = fmaxf(m, __ldcg(pl + sp * NR));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float lse = -INFINITY;
+            if (m > -INFINITY) {
+              float z = 0.f;
+              for (int sp = 0; sp < w.nsplit; ++sp) z += fast_exp2((__ldcg(pl + sp * NR) - m) * kLog2e);
+              lse = m + __logf(z);
+              for (int sp = 0; sp < w.nsplit; ++sp) {
+                const float wgt = fast_exp2((__ldcg(pl + sp * NR) - lse) * kLog2e);
+                const int64_t slot = (int64_t)w.pbase + (int64_t)sp * NR + n;
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0));
+                acc.x += wgt * v.x;
+                acc.y += wgt * v.y;
+                acc.z += wgt * v.z;
+                acc.w += wgt * v.w;
+              }
+            }
+            const int64_t g = grow(n);
+            if (a.out_f32) {
+              *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc;
+            } else {
+              const __nv_bfloat162 x = __floats2bfloat162_rn(acc.x, acc.y), y = __floats2bfloat162_rn(acc.z, acc.w);
+              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+            }
+            if (st_tid == 0) a.lse[g] = lse;
+          }
+        }
+      }
       named_bar_sync(1, 128);
     }
   }

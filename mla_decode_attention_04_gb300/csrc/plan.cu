@@ -1,4 +1,4 @@
-// plan.cu -- balanced split-KV scheduler and split combine of the dense decode.
+// plan.cu -- balanced split-KV scheduler of the dense decode.
 //
 // The scheduler runs on the device (one CTA) so that turning seq_lens /
 // query_start_loc into work needs no host synchronisation: the review of
@@ -13,7 +13,9 @@
 // G decode CTAs divide into equal contiguous ranges, so every CTA streams the
 // same number of KV tiles whatever the length mix; a pair cut by range
 // boundaries is computed in several KV chunks whose results are merged by
-// LSE afterwards (the same merge as the DCP merge, over chunks).
+// LSE (the same merge as the DCP merge, over chunks) by the decode CTA that
+// finishes the pair's last chunk.  Rows of requests without local keys get
+// their final result (out 0, lse -inf) here.
 #include "common.cuh"
 #include "plan.h"
 
@@ -75,7 +77,11 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
   __shared__ int s_overflow;
   WorkspaceHeader* hdr = a.hdr;
   const int H = a.num_heads, NR = a.rows_per_group;
-  if (threadIdx.x == 0) s_overflow = 0;
+  if (threadIdx.x == 0) {
+    s_overflow = 0;
+    hdr->status = 0;  // this call's checks start clean (no kernel of it has run yet)
+    hdr->detail = 0;
+  }
   for (int t = threadIdx.x; t < a.num_tokens; t += blockDim.x) a.tok2req[t] = -1;
   __syncthreads();
 
@@ -113,6 +119,21 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
           pi.nsplit = 1;
           pi.pbase = 0;
           a.pairs[pair_off + g] = pi;
+          a.pair_done[pair_off + g] = 0;
+        }
+      }
+      if (p.nt == 0 && p.q_len > 0) {
+        // no local key: the rows' final result (no decode unit covers them)
+        for (int r = 0; r < ri.rows; ++r) {
+          const int64_t grow = (int64_t)p.q0 * H + r;
+          a.lse[grow] = -INFINITY;
+          if (a.out_f32) {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + grow * kNope);
+            for (int k = 0; k < kNope / 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + grow * kNope);
+            for (int k = 0; k < kNope / 8; ++k) o[k] = make_uint4(0, 0, 0, 0);
+          }
         }
       }
       for (int i = 0; i < p.q_len; ++i) {
@@ -175,68 +196,6 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     hdr->num_pairs = s_overflow ? 0 : (int)pair_carry;
     hdr->total_items = s_overflow ? 0 : W;
   }
-}
-
-// Per (token, head) row: merge the KV-chunk partials of a split pair, or
-// write the empty-row result (out 0, lse -inf) of a pair without keys.
-// One warp per row.
-__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int H = a.num_heads, NR = a.rows_per_group;
-  if (warp >= a.num_tokens * H) return;
-  if (a.hdr->num_pairs == 0) return;  // scheduler overflow: nothing was planned
-  const int t = warp / H, h = warp % H;
-  const int b = a.tok2req[t];
-  if (b < 0) return;
-  const ReqInfo ri = a.req[b];
-  const int rr = (t - ri.q0) * H + h;  // row within the request
-  const int g = rr / NR;
-  const PairInfo pi = a.pairs[ri.pair_base + g];
-  if (pi.nt > 0 && pi.nsplit <= 1) return;  // the decode wrote this row
-  const int n = rr - g * NR;
-  float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  float lse = -INFINITY;
-  if (pi.nt > 0) {
-    float m = -INFINITY;
-    for (int s = 0; s < pi.nsplit; ++s) m = fmaxf(m, a.part_lse[pi.pbase + s * NR + n]);
-    if (m > -INFINITY) {
-      float z = 0.f;
-      for (int s = 0; s < pi.nsplit; ++s) z += __expf(a.part_lse[pi.pbase + s * NR + n] - m);
-      lse = m + __logf(z);
-      for (int s = 0; s < pi.nsplit; ++s) {
-        const int slot = pi.pbase + s * NR + n;
-        const float w = __expf(a.part_lse[slot] - lse);
-        if (w == 0.f) continue;
-        const float4* p = reinterpret_cast<const float4*>(a.part_o + (size_t)slot * kNope);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 v = p[k * 32 + lane];
-          acc[4 * k + 0] += w * v.x;
-          acc[4 * k + 1] += w * v.y;
-          acc[4 * k + 2] += w * v.z;
-          acc[4 * k + 3] += w * v.w;
-        }
-      }
-    }
-  }
-  const size_t orow = ((size_t)t * H + h) * kNope;
-  if (a.out_f32) {
-    float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) o[k * 32 + lane] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-  } else {
-    uint2* o = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      __nv_bfloat162 x = __floats2bfloat162_rn(acc[4 * k], acc[4 * k + 1]);
-      __nv_bfloat162 y = __floats2bfloat162_rn(acc[4 * k + 2], acc[4 * k + 3]);
-      o[k * 32 + lane] = make_uint2(*reinterpret_cast<uint32_t*>(&x), *reinterpret_cast<uint32_t*>(&y));
-    }
-  }
-  if (lane == 0) a.lse[(size_t)t * H + h] = lse;
 }
 
 }  // namespace mla

@@ -19,18 +19,10 @@ struct SchedArgs {
   WorkspaceHeader* hdr;
   ReqInfo* req;
   PairInfo* pairs;
+  int32_t* pair_done;   // per-pair finished-chunk counters, zeroed here
   int32_t* tok2req;
   int32_t* row_counts;  // may be NULL
-};
-
-struct CombineArgs {
-  const WorkspaceHeader* hdr;
-  const ReqInfo* req;
-  const PairInfo* pairs;
-  const int32_t* tok2req;
-  const float* part_lse;
-  const float* part_o;
-  int32_t num_tokens, num_heads, rows_per_group;
+  // rows of pairs without keys get their final result here (out 0, lse -inf)
   void* out;
   int32_t out_f32;
   float* lse;
@@ -42,7 +34,7 @@ struct DecodePlan {
   int32_t grid;              // decode CTAs
   int32_t max_pairs;         // capacity of the (request, row group) list
   int64_t max_partial_rows;  // capacity of the split partials
-  size_t off_req, off_tok, off_pairs, off_plse, off_po, total;
+  size_t off_req, off_tok, off_pairs, off_cnt, off_plse, off_po, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -79,6 +71,8 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   off = align_up(off + sizeof(int32_t) * (size_t)(T > 0 ? T : 1), 256);
   p.off_pairs = off;
   off = align_up(off + sizeof(PairInfo) * (size_t)p.max_pairs, 256);
+  p.off_cnt = off;  // per-pair count of finished KV chunks
+  off = align_up(off + sizeof(int32_t) * (size_t)p.max_pairs, 256);
   p.off_plse = off;
   off = align_up(off + sizeof(float) * (size_t)p.max_partial_rows, 256);
   p.off_po = off;
@@ -104,6 +98,5 @@ inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk) {
 }
 
 __global__ void schedule_kernel(SchedArgs a);
-__global__ void combine_kernel(CombineArgs a);
 
 }  // namespace mla
