@@ -675,36 +675,86 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         named_bar_sync(1, 128);
         if (sh.is_last) {
           __threadfence();
-          const int d0 = st_tid * 4;  // 4 of the 512 latent dims per thread
-          for (int n = 0; n < w.nrows; ++n) {
-            const float* pl = a.part_lse + w.pbase + n;
-            float m = -INFINITY;
-            for (int sp = 0; sp < w.nsplit; ++sp) m = fmaxf(m, __ldcg(pl + sp * NR));
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            float lse = -INFINITY;
-            if (m > -INFINITY) {
-              float z = 0.f;
-              for (int sp = 0; sp < w.nsplit; ++sp) z += fast_exp2((__ldcg(pl + sp * NR) - m) * kLog2e);
-              lse = m + __logf(z);
-              for (int sp = 0; sp < w.nsplit; ++sp) {
-                const float wgt = fast_exp2((__ldcg(pl + sp * NR) - lse) * kLog2e);
-                const int64_t slot = (int64_t)w.pbase + (int64_t)sp * NR + n;
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0));
-                acc.x += wgt * v.x;
-                acc.y += wgt * v.y;
-                acc.z += wgt * v.z;
-                acc.w += wgt * v.w;
+          // (1) each row's LSE over the chunks: warp sw owns rows sw, sw+4, ...,
+          // its lanes stride over the chunks (all loads of a pass in flight)
+          float mx[NR / 4], z[NR / 4];
+#pragma unroll
+          for (int i = 0; i < NR / 4; ++i) mx[i] = -INFINITY, z[i] = 0.f;
+          for (int sp0 = 0; sp0 < w.nsplit; sp0 += 32) {
+            const int sp = sp0 + lane;
+            float v[NR / 4];
+#pragma unroll
+            for (int i = 0; i < NR / 4; ++i) {
+              const int n = sw + 4 * i;
+              v[i] = (n < w.nrows && sp < w.nsplit) ? __ldcg(a.part_lse + w.pbase + (int64_t)sp * NR + n) : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < NR / 4; ++i) {
+              if (v[i] > mx[i]) {
+                z[i] = z[i] * fast_exp2((mx[i] - v[i]) * kLog2e) + 1.f;
+                mx[i] = v[i];
+              } else if (v[i] > -INFINITY) {
+                z[i] += fast_exp2((v[i] - mx[i]) * kLog2e);
               }
             }
-            const int64_t g = grow(n);
-            if (a.out_f32) {
-              *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc;
-            } else {
-              const __nv_bfloat162 x = __floats2bfloat162_rn(acc.x, acc.y), y = __floats2bfloat162_rn(acc.z, acc.w);
-              *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
-                  make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+          }
+#pragma unroll
+          for (int i = 0; i < NR / 4; ++i) {
+            float gm = mx[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+            float zz = mx[i] > -INFINITY ? z[i] * fast_exp2((mx[i] - gm) * kLog2e) : 0.f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+            const int n = sw + 4 * i;
+            if (lane == 0 && n < w.nrows) {
+              const float lse = gm > -INFINITY ? gm + __logf(zz) : -INFINITY;
+              sh.alpha[n] = lse;
+              a.lse[grow(n)] = lse;
             }
-            if (st_tid == 0) a.lse[g] = lse;
+          }
+          named_bar_sync(1, 128);
+          // (2) weighted sum of the chunks: thread st_tid owns latent dims
+          // [4 st_tid, 4 st_tid + 4) of 8 rows at a time
+          const int d0 = st_tid * 4;
+#pragma unroll 1
+          for (int n0 = 0; n0 < w.nrows; n0 += 8) {
+            float4 acc[8];
+            float lrow[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+              lrow[k] = n0 + k < w.nrows ? sh.alpha[n0 + k] : -INFINITY;
+            }
+#pragma unroll 2
+            for (int sp = 0; sp < w.nsplit; ++sp) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (lrow[k] > -INFINITY) {
+                  const int64_t slot = (int64_t)w.pbase + (int64_t)sp * NR + n0 + k;
+                  const float lv = __ldcg(a.part_lse + slot);
+                  const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0));
+                  const float wgt = fast_exp2((lv - lrow[k]) * kLog2e);
+                  acc[k].x += wgt * v.x;
+                  acc[k].y += wgt * v.y;
+                  acc[k].z += wgt * v.z;
+                  acc[k].w += wgt * v.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (n0 + k >= w.nrows) break;
+              const int64_t g = grow(n0 + k);
+              if (a.out_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
+              } else {
+                const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+                const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+              }
+            }
           }
         }
       }
