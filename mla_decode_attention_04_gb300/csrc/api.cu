@@ -152,6 +152,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   sa.pairs = reinterpret_cast<mla::PairInfo*>(ws + plan.off_pairs);
   sa.tok2req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
   sa.pair_done = reinterpret_cast<int32_t*>(ws + plan.off_cnt);
+  sa.cta_pair0 = reinterpret_cast<int32_t*>(ws + plan.off_cta);
   sa.row_counts = row_counts;
   sa.out = out;
   sa.out_f32 = out_dtype == MLA_DTYPE_F32;
@@ -181,6 +182,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   da.req = sa.req;
   da.pairs = sa.pairs;
   da.pair_done = sa.pair_done;
+  da.cta_pair0 = sa.cta_pair0;
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
   da.num_tokens = num_tokens;

@@ -52,8 +52,10 @@ struct ReqInfo {
 // [item0, item0 + nt) of the flattened list that the decode grid divides into
 // equal contiguous ranges.  A pair crossing range boundaries is computed in
 // nsplit chunks whose partial results sit at slots pbase + split * NR + row
-// and are merged by the combine kernel.
-struct PairInfo {
+// and are merged by the decode CTA that finishes the pair's last chunk.  The
+// request's facts are repeated here so that a decode CTA reads one record per
+// unit.
+struct __align__(16) PairInfo {
   int64_t item0;
   int32_t b;
   int32_t row0;
@@ -61,8 +63,12 @@ struct PairInfo {
   int32_t nt;
   int32_t nsplit;
   int32_t pbase;
+  int32_t q0;         // the request's query_start_loc
+  int32_t q_len;
+  int32_t seq_len;    // global
+  int32_t local_len;  // keys this shard holds
 };
-static_assert(sizeof(PairInfo) == 32, "pair size");
+static_assert(sizeof(PairInfo) == 48, "pair size");
 
 // CTA that owns work item i when W items are divided over G CTAs as
 // [floor(c W / G), floor((c + 1) W / G)).

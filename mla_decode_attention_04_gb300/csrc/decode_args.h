@@ -25,6 +25,7 @@ struct DecodeArgs {
   const ReqInfo* req;
   const PairInfo* pairs;
   int32_t* pair_done;  // finished KV chunks per pair (the last finisher merges)
+  const int32_t* cta_pair0;  // pair holding the first item of each CTA's range
   float* part_lse;
   float* part_o;
   // sparse

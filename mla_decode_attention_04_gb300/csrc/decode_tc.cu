@@ -100,12 +100,15 @@ struct Unit {
 
 // The sequence of units of one CTA.  Dense: the CTA's equal share
 // [c W / G, (c + 1) W / G) of the scheduler's flattened key-tile list, cut at
-// (request, row group) boundaries.  Sparse: (token, head group) units dealt
-// round-robin.  Every role walks the same sequence.
+// (request, row group) boundaries; the scheduler names the pair holding the
+// range's first item, later units are the following pairs, and the record of
+// the next pair is loaded one unit ahead.  Sparse: (token, head group) units
+// dealt round-robin.  Every role walks the same sequence.
 template <int NR, bool SPARSE>
 struct UnitIter {
   int64_t i, hi, W, G;
-  int num_pairs;
+  int p;         // dense: pair of the next unit
+  PairInfo nxt;  // dense: its record (loaded ahead)
   int u, units;
 
   __device__ void init(const DecodeArgs& a) {
@@ -116,10 +119,11 @@ struct UnitIter {
       // the scheduler balanced the W items over min(grid, W) non-empty ranges
       W = a.hdr->total_items;
       G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
-      num_pairs = a.hdr->num_pairs;
-      if ((int64_t)blockIdx.x < G) {
+      if ((int64_t)blockIdx.x < G && W > 0) {
         i = (int64_t)blockIdx.x * W / G;
         hi = ((int64_t)blockIdx.x + 1) * W / G;
+        p = a.cta_pair0[blockIdx.x];
+        nxt = a.pairs[p];
       } else {
         i = hi = 0;
       }
@@ -152,30 +156,26 @@ struct UnitIter {
       return false;
     } else {
       if (i >= hi) return false;
-      int lo = 0, up = num_pairs - 1;  // last pair with item0 <= i
-      while (lo < up) {
-        const int mid = (lo + up + 1) >> 1;
-        if (a.pairs[mid].item0 <= i) lo = mid; else up = mid - 1;
-      }
-      const PairInfo pi = a.pairs[lo];
-      const ReqInfo ri = a.req[pi.b];
+      while (nxt.nt == 0) nxt = a.pairs[++p];  // pairs without keys own no item
+      const PairInfo pi = nxt;
       const int64_t end = min(hi, pi.item0 + pi.nt);
       w.token = -1;
-      w.pair = lo;
+      w.pair = p;
       w.b = pi.b;
       w.row0 = pi.row0;
       w.nrows = pi.nrows;
       w.key0 = (int)(i - pi.item0) * kKeyTile;
-      w.key1 = min((int)(end - pi.item0) * kKeyTile, ri.local_len);
+      w.key1 = min((int)(end - pi.item0) * kKeyTile, pi.local_len);
       w.n_kt = (int)(end - i);
       w.nsplit = pi.nsplit;
       w.split = pi.nsplit > 1 ? (int)(item_owner(i, W, G) - item_owner(pi.item0, W, G)) : 0;
       w.pbase = pi.pbase;
-      w.q0 = ri.q0;
-      w.q_len = ri.q_len;
-      w.seq_len = ri.seq_len;
-      w.local_len = ri.local_len;
+      w.q0 = pi.q0;
+      w.q_len = pi.q_len;
+      w.seq_len = pi.seq_len;
+      w.local_len = pi.local_len;
       i = end;
+      if (i < hi) nxt = a.pairs[++p];
       return true;
     }
   }
@@ -453,15 +453,56 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       tc_fence_after();
       return r;
     };
+    // global (token, head) row index of row n of unit u
+    auto grow_of = [&](const Unit& u, int n) -> int64_t {
+      if constexpr (SPARSE) return (int64_t)u.token * H + u.row0 + n;
+      else return (int64_t)u.q0 * H + u.row0 + n;
+    };
+    // Q rows of unit u into TMEM, then q_ready.  Called once every QK^T
+    // issued so far is complete (the softmax has read all their S).
+    auto load_q = [&](const Unit& u) {
+      // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
+      // (the TPR lanes of a row read the same addresses: one request per warp)
+      const bool have = row < u.nrows;
+      const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow_of(u, row) * a.q_nope_stride) : nullptr;
+      const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow_of(u, row) * a.q_pe_stride) : nullptr;
+      // three 64-dim chunks per batch: all their loads are in flight before
+      // the first store, so a unit pays three load latencies, not nine
+#pragma unroll 1
+      for (int cb = 0; cb < 9; cb += 3) {
+        uint4 x[24];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int c = cb + q;
+          const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          uint32_t r[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
+            r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
+          }
+          tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (st_tid == 0) mbar_arrive(&sh.q_ready);
+    };
     UnitIter<NR, SPARSE> it;
     it.init(a);
-    Unit w;
-    while (ok && it.next(a, w)) {
-      // global (token, head) row index of unit row n
-      auto grow = [&](int n) -> int64_t {
-        if constexpr (SPARSE) return (int64_t)w.token * H + w.row0 + n;
-        else return (int64_t)w.q0 * H + w.row0 + n;
-      };
+    Unit w, wn;
+    bool more = it.next(a, wn);
+    if (more && wn.n_kt > 0) load_q(wn);
+    while (ok && more) {
+      w = wn;
+      more = it.next(a, wn);
+      auto grow = [&](int n) -> int64_t { return grow_of(w, n); };
       const bool partial = !SPARSE && w.nsplit > 1;
       int kend = w.key0;  // keys [key0, kend) visible to this thread's row
       if (row < w.nrows) {
@@ -474,41 +515,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
       float m_ref = -INFINITY, l_sum = 0.f;
-
-      if (w.n_kt > 0) {
-        // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
-        // (the TPR lanes of a row read the same addresses: one request per warp)
-        const bool have = row < w.nrows;
-        const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow(row) * a.q_nope_stride) : nullptr;
-        const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow(row) * a.q_pe_stride) : nullptr;
-        // three 64-dim chunks per batch: all their loads are in flight before
-        // the first store, so a unit pays three load latencies, not nine
-#pragma unroll 1
-        for (int cb = 0; cb < 9; cb += 3) {
-          uint4 x[24];
-#pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            const int c = cb + q;
-            const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            uint32_t r[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
-              r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
-            }
-            tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_sync(1, 128);
-        if (st_tid == 0) mbar_arrive(&sh.q_ready);
-      }
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
         if (!group_wait(&sh.s_full[j % SB], (j / SB) & 1)) { ok = false; break; }
@@ -619,6 +625,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         if (++stage == kStages) stage = 0;
       }
       if (!ok) break;
+      // the next unit's Q goes in now, so that its first QK^T overlaps this
+      // unit's epilogue
+      if (more && wn.n_kt > 0) load_q(wn);
 
       // ---- epilogue of the unit
       if (w.n_kt > 0) {

@@ -118,6 +118,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
           pi.nt = p.nt;
           pi.nsplit = 1;
           pi.pbase = 0;
+          pi.q0 = ri.q0;
+          pi.q_len = ri.q_len;
+          pi.seq_len = ri.seq_len;
+          pi.local_len = ri.local_len;
           a.pairs[pair_off + g] = pi;
           a.pair_done[pair_off + g] = 0;
         }
@@ -167,7 +171,13 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
       for (int g = 0; g < groups; ++g) {
         PairInfo& pi = a.pairs[pb + g];
         int ns = 1;
-        if (pi.nt > 0 && W > 0) ns = (int)(item_owner(pi.item0 + pi.nt - 1, W, G) - item_owner(pi.item0, W, G) + 1);
+        if (pi.nt > 0 && W > 0) {
+          ns = (int)(item_owner(pi.item0 + pi.nt - 1, W, G) - item_owner(pi.item0, W, G) + 1);
+          // CTA c's range starts at item floor(c W / G): the CTAs whose range
+          // starts inside [item0, item0 + nt) begin with this pair
+          const long long c_lo = (pi.item0 * G + W - 1) / W, c_hi = ((pi.item0 + pi.nt) * G + W - 1) / W;
+          for (long long c = c_lo; c < c_hi; ++c) a.cta_pair0[c] = pb + g;
+        }
         pi.nsplit = ns;
         if (ns > 1) parts += (long long)ns * NR;
       }

@@ -20,6 +20,7 @@ struct SchedArgs {
   ReqInfo* req;
   PairInfo* pairs;
   int32_t* pair_done;   // per-pair finished-chunk counters, zeroed here
+  int32_t* cta_pair0;   // [grid] pair holding the first item of each decode CTA's range
   int32_t* tok2req;
   int32_t* row_counts;  // may be NULL
   // rows of pairs without keys get their final result here (out 0, lse -inf)
@@ -34,7 +35,7 @@ struct DecodePlan {
   int32_t grid;              // decode CTAs
   int32_t max_pairs;         // capacity of the (request, row group) list
   int64_t max_partial_rows;  // capacity of the split partials
-  size_t off_req, off_tok, off_pairs, off_cnt, off_plse, off_po, total;
+  size_t off_req, off_tok, off_pairs, off_cnt, off_cta, off_plse, off_po, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -73,6 +74,8 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   off = align_up(off + sizeof(PairInfo) * (size_t)p.max_pairs, 256);
   p.off_cnt = off;  // per-pair count of finished KV chunks
   off = align_up(off + sizeof(int32_t) * (size_t)p.max_pairs, 256);
+  p.off_cta = off;  // first pair of each decode CTA's item range
+  off = align_up(off + sizeof(int32_t) * (size_t)p.grid, 256);
   p.off_plse = off;
   off = align_up(off + sizeof(float) * (size_t)p.max_partial_rows, 256);
   p.off_po = off;
