@@ -190,6 +190,106 @@ __device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
   return (int64_t)page * a.page_size + j % a.page_size;
 }
 
+// Merge of a split pair's chunks by LSE, run by the 128 softmax threads of the
+// CTA that finished the pair's last chunk (dense units only).
+template <int NR>
+__device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Unit& u, TcShared& sh, int st_tid) {
+  const int lane = st_tid & 31, sw = st_tid >> 5;
+  __threadfence();
+  // (1) each row's LSE over the chunks: warp sw owns rows sw, sw+4, ...,
+  // its lanes stride over the chunks (all loads of a pass in flight)
+  float mx[NR / 4], z[NR / 4];
+#pragma unroll
+  for (int i = 0; i < NR / 4; ++i) mx[i] = -INFINITY, z[i] = 0.f;
+  for (int sp0 = 0; sp0 < u.nsplit; sp0 += 32) {
+    const int sp = sp0 + lane;
+    float v[NR / 4];
+#pragma unroll
+    for (int i = 0; i < NR / 4; ++i) {
+      const int n = sw + 4 * i;
+      v[i] = (n < u.nrows && sp < u.nsplit) ? __ldcg(a.part_lse + u.pbase + (int64_t)sp * NR + n) : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < NR / 4; ++i) {
+      if (v[i] > mx[i]) {
+        z[i] = z[i] * fast_exp2((mx[i] - v[i]) * kLog2e) + 1.f;
+        mx[i] = v[i];
+      } else if (v[i] > -INFINITY) {
+        z[i] += fast_exp2((v[i] - mx[i]) * kLog2e);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NR / 4; ++i) {
+    float gm = mx[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    float zz = mx[i] > -INFINITY ? z[i] * fast_exp2((mx[i] - gm) * kLog2e) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+    const int n = sw + 4 * i;
+    if (lane == 0 && n < u.nrows) {
+      const float lse = gm > -INFINITY ? gm + __logf(zz) : -INFINITY;
+      sh.alpha[n] = lse;
+      a.lse[((int64_t)u.q0 * a.num_heads + u.row0 + n)] = lse;
+    }
+  }
+  named_bar_sync(1, 128);
+  // (2) weighted sum of the chunks: thread st_tid owns latent dims
+  // [4 st_tid, 4 st_tid + 4) of 8 rows at a time, kPass chunks per pass
+  // (all 2 * 8 * kPass loads of a pass in flight)
+  constexpr int kPass = 2;
+  const int d0 = st_tid * 4;
+#pragma unroll 1
+  for (int n0 = 0; n0 < u.nrows; n0 += 8) {
+    float4 acc[8];
+    float lrow[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      lrow[k] = n0 + k < u.nrows ? sh.alpha[n0 + k] : -INFINITY;
+    }
+#pragma unroll 1
+    for (int sp0 = 0; sp0 < u.nsplit; sp0 += kPass) {
+      float lv[kPass][8];
+      float4 v[kPass][8];
+#pragma unroll
+      for (int q = 0; q < kPass; ++q)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const bool use = sp0 + q < u.nsplit && lrow[k] > -INFINITY;
+          const int64_t slot = (int64_t)u.pbase + (int64_t)(sp0 + q) * NR + n0 + k;
+          lv[q][k] = use ? __ldcg(a.part_lse + slot) : -INFINITY;
+          v[q][k] = use ? __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int q = 0; q < kPass; ++q)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float wgt = lv[q][k] > -INFINITY ? fast_exp2((lv[q][k] - lrow[k]) * kLog2e) : 0.f;
+          acc[k].x += wgt * v[q][k].x;
+          acc[k].y += wgt * v[q][k].y;
+          acc[k].z += wgt * v[q][k].z;
+          acc[k].w += wgt * v[q][k].w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (n0 + k >= u.nrows) break;
+      const int64_t g = ((int64_t)u.q0 * a.num_heads + u.row0 + n0 + k);
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
+      } else {
+        const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+        const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+      }
+    }
+  }
+}
+
 template <int NR, bool SPARSE>
 __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeArgs a) {
@@ -466,20 +566,23 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const bool have = row < u.nrows;
       const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow_of(u, row) * a.q_nope_stride) : nullptr;
       const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow_of(u, row) * a.q_pe_stride) : nullptr;
-      // three 64-dim chunks per batch: all their loads are in flight before
-      // the first store, so a unit pays three load latencies, not nine
+      // batches of 64-dim chunks (dense: five then four; sparse, with fewer
+      // registers per thread: three): all loads of a batch are in flight
+      // before its first store, so a unit pays two or three load latencies
+      constexpr int kQB = SPARSE ? 3 : 5;
 #pragma unroll 1
-      for (int cb = 0; cb < 9; cb += 3) {
-        uint4 x[24];
+      for (int cb = 0; cb < 9; cb += kQB) {
+        uint4 x[8 * kQB];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
+        for (int q = 0; q < kQB; ++q) {
           const int c = cb + q;
           const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
+          for (int v = 0; v < 8; ++v) x[8 * q + v] = have && c < 9 ? src[v] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
+        for (int q = 0; q < kQB; ++q) {
+          if (cb + q >= 9) break;
           uint32_t r[32];
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
@@ -494,9 +597,25 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       named_bar_sync(1, 128);
       if (st_tid == 0) mbar_arrive(&sh.q_ready);
     };
+    // A split pair's chunk is counted one tile after its epilogue (or at the
+    // end), so the fence and the atomic's round trip overlap the next unit's
+    // MMAs; the CTA whose count completes the pair merges its chunks by LSE
+    // (threadfence-reduction pattern: publish, count, re-fence, read) at its
+    // next epilogue, outside the tile loop.
+    auto count_chunk = [&](const Unit& u) -> bool {
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[u.pair], 1) == u.nsplit - 1;
+      named_bar_sync(1, 128);
+      return sh.is_last != 0;
+    };
     UnitIter<NR, SPARSE> it;
     it.init(a);
     Unit w, wn;
+    Unit pend;               // split chunk written but not yet counted
+    bool have_pend = false;
+    Unit mrg;                // pair whose chunks this CTA merges next
+    bool have_mrg = false;
     bool more = it.next(a, wn);
     if (more && wn.n_kt > 0) load_q(wn);
     while (ok && more) {
@@ -623,6 +742,13 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         named_bar_sync(1, 128);
         if (st_tid == 0) mbar_arrive(&sh.p_ready);
         if (++stage == kStages) stage = 0;
+        if (have_pend) {
+          if (count_chunk(pend)) {
+            mrg = pend;
+            have_mrg = true;
+          }
+          have_pend = false;
+        }
       }
       if (!ok) break;
       // the next unit's Q goes in now, so that its first QK^T overlaps this
@@ -676,99 +802,17 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
       tc_fence_before();
       if (partial) {
-        // The CTA that finishes a pair's last KV chunk merges the chunks by
-        // LSE (threadfence-reduction pattern: publish, count, re-fence, read).
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[w.pair], 1) == w.nsplit - 1;
-        named_bar_sync(1, 128);
-        if (sh.is_last) {
-          __threadfence();
-          // (1) each row's LSE over the chunks: warp sw owns rows sw, sw+4, ...,
-          // its lanes stride over the chunks (all loads of a pass in flight)
-          float mx[NR / 4], z[NR / 4];
-#pragma unroll
-          for (int i = 0; i < NR / 4; ++i) mx[i] = -INFINITY, z[i] = 0.f;
-          for (int sp0 = 0; sp0 < w.nsplit; sp0 += 32) {
-            const int sp = sp0 + lane;
-            float v[NR / 4];
-#pragma unroll
-            for (int i = 0; i < NR / 4; ++i) {
-              const int n = sw + 4 * i;
-              v[i] = (n < w.nrows && sp < w.nsplit) ? __ldcg(a.part_lse + w.pbase + (int64_t)sp * NR + n) : -INFINITY;
-            }
-#pragma unroll
-            for (int i = 0; i < NR / 4; ++i) {
-              if (v[i] > mx[i]) {
-                z[i] = z[i] * fast_exp2((mx[i] - v[i]) * kLog2e) + 1.f;
-                mx[i] = v[i];
-              } else if (v[i] > -INFINITY) {
-                z[i] += fast_exp2((v[i] - mx[i]) * kLog2e);
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < NR / 4; ++i) {
-            float gm = mx[i];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
-            float zz = mx[i] > -INFINITY ? z[i] * fast_exp2((mx[i] - gm) * kLog2e) : 0.f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
-            const int n = sw + 4 * i;
-            if (lane == 0 && n < w.nrows) {
-              const float lse = gm > -INFINITY ? gm + __logf(zz) : -INFINITY;
-              sh.alpha[n] = lse;
-              a.lse[grow(n)] = lse;
-            }
-          }
-          named_bar_sync(1, 128);
-          // (2) weighted sum of the chunks: thread st_tid owns latent dims
-          // [4 st_tid, 4 st_tid + 4) of 8 rows at a time
-          const int d0 = st_tid * 4;
-#pragma unroll 1
-          for (int n0 = 0; n0 < w.nrows; n0 += 8) {
-            float4 acc[8];
-            float lrow[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-              lrow[k] = n0 + k < w.nrows ? sh.alpha[n0 + k] : -INFINITY;
-            }
-#pragma unroll 2
-            for (int sp = 0; sp < w.nsplit; ++sp) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                if (lrow[k] > -INFINITY) {
-                  const int64_t slot = (int64_t)w.pbase + (int64_t)sp * NR + n0 + k;
-                  const float lv = __ldcg(a.part_lse + slot);
-                  const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0));
-                  const float wgt = fast_exp2((lv - lrow[k]) * kLog2e);
-                  acc[k].x += wgt * v.x;
-                  acc[k].y += wgt * v.y;
-                  acc[k].z += wgt * v.z;
-                  acc[k].w += wgt * v.w;
-                }
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if (n0 + k >= w.nrows) break;
-              const int64_t g = grow(n0 + k);
-              if (a.out_f32) {
-                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
-              } else {
-                const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-                const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
-                    make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
-              }
-            }
-          }
-        }
+        pend = w;
+        have_pend = true;
       }
       named_bar_sync(1, 128);
+      if (have_mrg) {
+        merge_split_chunks<NR>(a, mrg, sh, st_tid);
+        have_mrg = false;
+        named_bar_sync(1, 128);
+      }
     }
+    if (ok && have_pend && count_chunk(pend)) merge_split_chunks<NR>(a, pend, sh, st_tid);
   }
 
   if (!ok) record_check(a.hdr, kCheckWaitTimeout);
