@@ -516,6 +516,18 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(name, repeat):
+    """Run the step of one benchmark workload ``repeat`` times, untimed: the
+    command the ncu summaries under profiles/ are captured from."""
+    from mla_decode_attention_04_gb300 import pipeline, workloads as wl
+    w = wl.NAMED[name](device="cuda")
+    step = pipeline.step_for_workload(w)
+    for _ in range(repeat):
+        step.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "repeat": repeat}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -523,7 +535,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--configs", default="all", help="all | headline | comma list of workload names")
+    ap.add_argument("--profile-case", default=None, help="run one workload's step untimed (for ncu), print no bench line")
+    ap.add_argument("--repeat", type=int, default=3, help="steps of --profile-case")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.repeat)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

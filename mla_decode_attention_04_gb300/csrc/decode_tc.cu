@@ -84,9 +84,10 @@ __device__ __forceinline__ float fast_exp2(float x) {
 template <bool SPARSE>
 struct Roles {
   static constexpr int kProducerWarps = SPARSE ? 4 : 1;
-  static constexpr int kMmaWarp = kProducerWarps;
-  static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;
-  static constexpr int kThreads = (kProducerWarps + 5) * 32;
+  static constexpr int kMmaWarp = kProducerWarps;          // issues QK^T (and owns TMEM)
+  static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;  // four consecutive warps
+  static constexpr int kPvWarp = kProducerWarps + 5;        // issues PV
+  static constexpr int kThreads = (kProducerWarps + 6) * 32;
 };
 
 // Work unit description, identical for every role.
@@ -429,8 +430,11 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
-  } else if (warp == R::kMmaWarp) {
+  } else if (warp == R::kMmaWarp || warp == R::kPvWarp) {
     // --------------------------------------------------------------- MMA
+    // One thread cannot issue tcgen05.mma fast enough to keep the tensor
+    // pipe busy with these small shapes, so QK^T and PV have an issuing
+    // thread each (in different warps); each commits its own MMAs.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, j = 0, q_ph = 0;
@@ -439,9 +443,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       UnitIter<NR, SPARSE> it;
       it.init(a);
       Unit w;
-      // S(j) = Q . KV(j)^T into the single S buffer; the softmax warps copy S
-      // to registers and release it (s_free) before working on it, so QK^T of
-      // tile j+1 is issued ahead of PV of tile j and overlaps the softmax.
       // Descriptors are linear in the start address (its field is addr >> 4
       // and every address here is below 256 KB), so each operand is a base
       // descriptor plus a constant offset in 16-byte units: the issue loops
@@ -451,70 +452,57 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint64_t d_v = smem_desc_sw128(kv0, 8192, 1024);                // MN-major kv_c (PV A)
       const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T (PV B)
       constexpr uint64_t kStageUnits = kStageBytes >> 4;
-      auto issue_qk = [&](uint32_t jj, int stg) {
-        const int sb = jj % SB;
-        const uint64_t b0 = d_kv + (uint64_t)stg * kStageUnits;
-#pragma unroll
-        for (int c = 0; c < 9; ++c)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColS + sb * 64, tmem + kColQ + (c * 4 + kk) * 8, b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk,
-                   (c | kk) != 0);
-        mma_commit(&sh.s_full[sb]);
-      };
-      auto issue_pv = [&](int stg, bool first_of_unit) {
-        const uint64_t v0 = d_v + (uint64_t)stg * kStageUnits;
-        const uint64_t p0 = d_p + (uint64_t)stg * kStageUnits;  // P hi; P lo at + kPBytes
-        const uint32_t first = first_of_unit ? 0u : 1u;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-            mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
-            if (p_split) mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
-          }
-        mma_commit(&sh.empty[stg]);
-        mma_commit(&sh.pv_done);
-      };
-      while (ok && it.next(a, w)) {
-        if (w.n_kt == 0) continue;
-        if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
-        q_ph ^= 1;
-        tc_fence_after();
-        // Issue QK^T of tile jq and PV of tile j (j < jq) in whichever order
-        // their inputs arrive: PV(j) as soon as P(j) is ready (this frees the
-        // ring stage for the next load), QK^T(jq) as soon as its tile has
-        // landed and its S buffer has been read.  Both in tile order.
-        const uint32_t j0 = j, jend = j + w.n_kt;
-        uint32_t jq = j;
-        int qstage = stage;
-        uint32_t qphase = phase;
-        uint64_t t_last = global_ns();
-        while (j < jend) {
-          bool did = false;
-          if (j < jq && mbar_test_wait(&sh.p_ready, j & 1)) {
+      if (warp == R::kMmaWarp) {
+        // S(j) = Q . KV(j)^T into S buffer j % SB as soon as tile j has
+        // landed and the softmax has copied S(j - SB) out of that buffer.
+        while (ok && it.next(a, w)) {
+          if (w.n_kt == 0) continue;
+          if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
+          q_ph ^= 1;
+          tc_fence_after();
+          for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
+            const int sb = j % SB;
+            if (!mbar_wait(&sh.full[stage], phase) || !mbar_wait(&sh.s_free[sb], ((j / SB) & 1) ^ 1)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            issue_pv(stage, j == j0);
-            if (j + 1 == jend) mma_commit(&sh.unit_done);
-            ++j;
+            const uint64_t b0 = d_kv + (uint64_t)stage * kStageUnits;
+#pragma unroll
+            for (int c = 0; c < 9; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kColS + sb * 64, tmem + kColQ + (c * 4 + kk) * 8,
+                       b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk, (c | kk) != 0);
+            mma_commit(&sh.s_full[sb]);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
-            did = true;
-          } else if (jq < jend && mbar_test_wait(&sh.full[qstage], qphase) &&
-                     mbar_test_wait(&sh.s_free[jq % SB], ((jq / SB) & 1) ^ 1)) {
-            tc_fence_after();
-            issue_qk(jq, qstage);
-            ++jq;
-            if (++qstage == kStages) { qstage = 0; qphase ^= 1; }
-            did = true;
           }
-          if (did) {
-            t_last = global_ns();
-          } else if (global_ns() - t_last > 2000000000ull) {
-            ok = false;
-            break;
-          } else {
-            __nanosleep(32);  // leave issue slots to the softmax warp sharing this SM sub-partition
+        }
+      } else {
+        // O^T += V_c(j)^T . P(j)^T once the softmax has written P(j); its
+        // completion frees the ring stage (QK^T(j), the stage's other
+        // reader, completed before the softmax saw S(j)).
+        while (ok && it.next(a, w)) {
+          if (w.n_kt == 0) continue;
+          for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
+            if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
+            const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
+            const uint32_t first = kt == 0 ? 0u : 1u;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
+                mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
+                if (p_split)
+                  mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+              }
+            mma_commit(&sh.empty[stage]);
+            mma_commit(&sh.pv_done);
+            if (kt + 1 == w.n_kt) mma_commit(&sh.unit_done);
+            if (++stage == kStages) stage = 0;
           }
         }
       }
