@@ -191,6 +191,21 @@ __device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
   return (int64_t)page * a.page_size + j % a.page_size;
 }
 
+// The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T, with
+// the accumulate flags and the P split fixed at compile time so that the
+// issue sequence has no run-time branches.
+template <int NR, bool FIRST, bool SPLIT>
+__device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p0, uint32_t id_pv) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
+      mma_ss(o0 + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, (FIRST && kk == 0) ? 0u : 1u);
+      if (SPLIT) mma_ss(o0 + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+    }
+}
+
 // Merge of a split pair's chunks by LSE, run by the 128 softmax threads of the
 // CTA that finished the pair's last chunk (dense units only).
 template <int NR>
@@ -489,16 +504,14 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             tc_fence_after();
             const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
             const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
-            const uint32_t first = kt == 0 ? 0u : 1u;
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-                mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, kk == 0 ? first : 1u);
-                if (p_split)
-                  mma_ss(tmem + TmemPlan<NR>::kColO + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
-              }
+            const uint32_t o0 = tmem + TmemPlan<NR>::kColO;
+            if (p_split) {
+              if (kt == 0) issue_pv_tile<NR, true, true>(o0, v0, p0, id_pv);
+              else issue_pv_tile<NR, false, true>(o0, v0, p0, id_pv);
+            } else {
+              if (kt == 0) issue_pv_tile<NR, true, false>(o0, v0, p0, id_pv);
+              else issue_pv_tile<NR, false, false>(o0, v0, p0, id_pv);
+            }
             mma_commit(&sh.empty[stage]);
             mma_commit(&sh.pv_done);
             if (kt + 1 == w.n_kt) mma_commit(&sh.unit_done);
