@@ -145,6 +145,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   sa.dcp_rank = dcp_rank;
   sa.rows_per_group = plan.rows_per_group;
   sa.grid = plan.grid;
+  sa.unit_penalty = plan.unit_penalty;
   sa.max_pairs = plan.max_pairs;
   sa.max_partial_rows = (int32_t)plan.max_partial_rows;
   sa.hdr = hdr;

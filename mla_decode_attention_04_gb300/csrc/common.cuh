@@ -14,6 +14,10 @@ constexpr int kRope = MLA_ROPE_DIM;      // 64: width of k_pe and q_pe
 constexpr int kRow = MLA_KV_ROW;         // 576: one latent cache row
 constexpr int kVHead = MLA_V_HEAD_DIM;   // 128: W_UV output width per head
 constexpr int kKeyTile = 64;             // keys per pipeline tile of the decode kernels
+// A decode CTA that starts a (request, row group) unit pays for loading its Q
+// into TMEM and for the previous unit's epilogue, about as long as streaming
+// this many key tiles; the split scheduler charges it to every unit.
+constexpr int kUnitPenalty = 6;
 constexpr int kMaxHeads = 128;
 
 // Device status word codes (first failure wins).
@@ -50,7 +54,9 @@ struct ReqInfo {
 // One (request, row group): rows [row0, row0 + nrows) of request b and the
 // nt 64-key tiles of its local keys, which are the work items
 // [item0, item0 + nt) of the flattened list that the decode grid divides into
-// equal contiguous ranges.  A pair crossing range boundaries is computed in
+// equal contiguous ranges.  Each pair with keys is preceded in that list by
+// kUnitPenalty items without work (the cost of starting a unit), so a range
+// that starts units gets fewer key tiles.  A pair crossing range boundaries is computed in
 // nsplit chunks whose partial results sit at slots pbase + split * NR + row
 // and are merged by the decode CTA that finishes the pair's last chunk.  The
 // request's facts are repeated here so that a decode CTA reads one record per

@@ -159,6 +159,10 @@ struct UnitIter {
       if (i >= hi) return false;
       while (nxt.nt == 0) nxt = a.pairs[++p];  // pairs without keys own no item
       const PairInfo pi = nxt;
+      // the range may start among the items that only carry the pair's
+      // start-up cost; a range holding none of its key tiles has no unit
+      if (i < pi.item0) i = pi.item0;
+      if (i >= hi) return false;
       const int64_t end = min(hi, pi.item0 + pi.nt);
       w.token = -1;
       w.pair = p;

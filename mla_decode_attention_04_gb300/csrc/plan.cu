@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
     if (b < a.num_requests) p = plan_request(a, b);
     const long long pair_off = block_exclusive_scan(p.groups, warp_sums, &s_total) + pair_carry;
     const long long pair_tot = s_total;
-    const long long item_off = block_exclusive_scan((long long)p.groups * p.nt, warp_sums, &s_total) + item_carry;
+    const long long vlen = p.nt > 0 ? (long long)p.nt + a.unit_penalty : 0;  // list items of one pair
+    const long long item_off = block_exclusive_scan((long long)p.groups * vlen, warp_sums, &s_total) + item_carry;
     const long long item_tot = s_total;
     if (b < a.num_requests) {
       if (!p.ok) record_check(hdr, kCheckBadQueryLayout);
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         // provisional pair entries (split plan filled in pass 2)
         for (int g = 0; g < p.groups; ++g) {
           PairInfo pi{};
-          pi.item0 = item_off + (long long)g * p.nt;
+          pi.item0 = item_off + (long long)g * vlen + (p.nt > 0 ? a.unit_penalty : 0);
           pi.b = b;
           pi.row0 = g * NR;
           pi.nrows = min(NR, ri.rows - g * NR);
@@ -174,8 +175,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         if (pi.nt > 0 && W > 0) {
           ns = (int)(item_owner(pi.item0 + pi.nt - 1, W, G) - item_owner(pi.item0, W, G) + 1);
           // CTA c's range starts at item floor(c W / G): the CTAs whose range
-          // starts inside [item0, item0 + nt) begin with this pair
-          const long long c_lo = (pi.item0 * G + W - 1) / W, c_hi = ((pi.item0 + pi.nt) * G + W - 1) / W;
+          // starts inside the pair's list items [item0 - penalty, item0 + nt)
+          // begin with this pair
+          const long long v0 = pi.item0 - a.unit_penalty;
+          const long long c_lo = (v0 * G + W - 1) / W, c_hi = ((pi.item0 + pi.nt) * G + W - 1) / W;
           for (long long c = c_lo; c < c_hi; ++c) a.cta_pair0[c] = pb + g;
         }
         pi.nsplit = ns;

@@ -14,6 +14,7 @@ struct SchedArgs {
   int32_t num_requests, num_tokens, num_heads, dcp_world, dcp_rank;
   int32_t rows_per_group;
   int32_t grid;              // CTAs of the decode launch that the items are balanced over
+  int32_t unit_penalty;      // items of balancing cost charged to every pair with keys
   int32_t max_pairs;
   int32_t max_partial_rows;
   WorkspaceHeader* hdr;
@@ -33,6 +34,7 @@ struct SchedArgs {
 struct DecodePlan {
   int32_t rows_per_group;    // rows (token, head) per work unit: 16 or 32
   int32_t grid;              // decode CTAs
+  int32_t unit_penalty;      // balancing cost of a unit start, in 64-key tiles
   int32_t max_pairs;         // capacity of the (request, row group) list
   int64_t max_partial_rows;  // capacity of the split partials
   size_t off_req, off_tok, off_pairs, off_cnt, off_cta, off_plse, off_po, total;
@@ -46,6 +48,7 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   if (max_query_len < 1) max_query_len = 1;  // the backend's capture-time clamp
   if (D < 1) D = 1;
   p.rows_per_group = (int64_t)max_query_len * H <= 16 ? 16 : 32;
+  p.unit_penalty = kUnitPenalty;
   const int64_t NR = p.rows_per_group;
   const int64_t max_local = (max_seq_len + D - 1) / D;
   const int64_t max_key_tiles = (max_local + kKeyTile - 1) / kKeyTile;
