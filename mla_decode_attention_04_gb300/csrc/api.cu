@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "decode_kernels.h"
+#include "pdl_launch.h"
 #include "plan.h"
 
 namespace {
@@ -158,8 +159,8 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   sa.out = out;
   sa.out_f32 = out_dtype == MLA_DTYPE_F32;
   sa.lse = lse;
-  mla::schedule_kernel<<<1, 1024, 0, st>>>(sa);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "schedule_kernel launch");
+  if ((e = mla::launch_pdl(mla::schedule_kernel, dim3(1), dim3(1024), 0, st, sa)) != cudaSuccess)
+    return cuda_fail(e, "schedule_kernel launch");
   count_launch();
 
   mla::DecodeArgs da{};

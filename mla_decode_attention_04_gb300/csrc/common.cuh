@@ -98,6 +98,16 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int32_t P, int32_t D, i
   return P >= r ? (P - r) / D + 1 : 0;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// so that it may start while the previous kernel in the stream finishes;
+// it lets its own successor launch at once and waits, before its first
+// global access, until the predecessor has completed and its writes are
+// visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_dep_sync() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 

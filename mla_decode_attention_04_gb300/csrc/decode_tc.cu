@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "decode_args.h"
 #include "decode_kernels.h"
+#include "pdl_launch.h"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     fence_mbar_init();
   }
   if (!SPARSE && threadIdx.x == 32 * R::kMmaWarp) prefetch_tmap(&kv_map);
+  grid_dep_sync();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -833,8 +835,7 @@ cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cud
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<NR, SPARSE><<<grid, Roles<SPARSE>::kThreads, smem, stream>>>(map, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel<NR, SPARSE>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream, map, a);
 }
 
 }  // namespace

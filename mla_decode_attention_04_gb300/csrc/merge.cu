@@ -8,6 +8,7 @@
 // up-projection y = o . W_UV[h] commutes with the merge.
 #include "common.cuh"
 #include "decode_kernels.h"
+#include "pdl_launch.h"
 
 namespace mla {
 
@@ -64,6 +65,7 @@ __device__ __forceinline__ void accumulate_row(const MergeArgs& a, int64_t prow,
 
 // One warp per (token, head) row, 512-wide output.
 __global__ void __launch_bounds__(256) merge_rows_kernel(MergeArgs a) {
+  grid_dep_sync();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int T = a.num_tokens, H = a.num_heads;
@@ -101,8 +103,7 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
   if (a.w_uv == nullptr) {
     const int64_t rows = (int64_t)a.num_tokens * a.num_heads;
     const int grid = (int)((rows + 7) / 8);
-    merge_rows_kernel<<<grid, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(merge_rows_kernel, dim3(grid), dim3(256), 0, stream, a);
   }
   return launch_merge_wuv_tc(a, stream);
 }

@@ -13,6 +13,7 @@
 // beyond ~2^-17.  The accumulator is 32 TMEM columns.
 #include "common.cuh"
 #include "decode_kernels.h"
+#include "pdl_launch.h"
 #include "tc_ptx.cuh"
 #include "tma_host.h"
 
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) merge_wuv_tc_kernel(const __grid_con
     fence_mbar_init();
     prefetch_tmap(&w_map);
   }
+  grid_dep_sync();
   // merge weights: warp per token, lanes over shards
   for (int n = warp; n < kNT; n += kThreads / 32) {
     const int t = t0 + n;
@@ -210,8 +212,7 @@ cudaError_t launch_merge_wuv_tc(const MergeArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(merge_wuv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.num_tokens + kNT - 1) / kNT, a.num_heads);
-  merge_wuv_tc_kernel<<<grid, kThreads, smem, stream>>>(map, a);
-  return cudaGetLastError();
+  return launch_pdl(merge_wuv_tc_kernel, grid, dim3(kThreads), smem, stream, map, a);
 }
 
 }  // namespace mla

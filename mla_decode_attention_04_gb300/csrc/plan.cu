@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
   __shared__ long long warp_sums[32];
   __shared__ long long s_total;
   __shared__ int s_overflow;
+  grid_dep_sync();
   WorkspaceHeader* hdr = a.hdr;
   const int H = a.num_heads, NR = a.rows_per_group;
   if (threadIdx.x == 0) {

@@ -8,10 +8,12 @@
 // per-row valid count.  One warp per token; order is kept with a ballot.
 #include "common.cuh"
 #include "decode_kernels.h"
+#include "pdl_launch.h"
 
 namespace mla {
 
 __global__ void __launch_bounds__(256) sparse_lists_kernel(SparseListArgs a) {
+  grid_dep_sync();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= a.num_tokens) return;
@@ -54,8 +56,7 @@ cudaError_t launch_sparse_lists(const SparseListArgs& a, cudaStream_t stream) {
   if (a.num_tokens <= 0) return cudaSuccess;
   const int warps = 8;
   const int grid = (a.num_tokens + warps - 1) / warps;
-  sparse_lists_kernel<<<grid, warps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(sparse_lists_kernel, dim3(grid), dim3(warps * 32), 0, stream, a);
 }
 
 }  // namespace mla
