@@ -2,7 +2,7 @@
 """Benchmark: MLA DCP decode on one GB300 (replicas on N GPUs).
 
 One step = the whole hot path on one batch: the D shard decodes (split-KV
-schedule, paged gathers, QK^T + online softmax + PV, split combine) and the
+schedule, paged gathers, QK^T + online softmax + PV, split-chunk merge) and the
 LSE merge.  The headline workload is plain decode: 64 requests, q_len 1,
 16 heads, context 4096, DCP D=2 (the D shards are D slices of one HBM).  The
 other benchmark workloads (plain decode D=1, MTP, long context, sparse +
@@ -423,7 +423,7 @@ def run_ours(args):
         "merge_hbm_frac": s["merge_hbm_frac"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_dense_" + HEADLINE),
-                     "kernel": "shard decode call (scheduler + decode + split combine) as a CUDA graph, "
+                     "kernel": "shard decode call (scheduler + decode with its split-chunk merge) as a CUDA graph, "
                                "CUDA events around each replay on the launching stream",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
         "e2e": head["e2e"],

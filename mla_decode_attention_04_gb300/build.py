@@ -44,13 +44,18 @@ def up_to_date(path: str = LIB_PATH) -> bool:
 
 
 def source_digest() -> str:
-    """Hash of the library's sources: ties recorded profiles to one kernel build."""
+    """Hash of the library's code (comments and blank lines left out): ties
+    recorded profiles to one kernel build."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for p in sorted(_sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))):
         h.update(os.path.basename(p).encode())
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 

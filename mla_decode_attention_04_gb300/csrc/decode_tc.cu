@@ -17,15 +17,18 @@
 // columns next to Q (288) and S (64).  For fp32 outputs P enters the value
 // product as two bf16 terms (hi + lo, both accumulated into O^T), so the
 // probabilities keep fp32-level precision; for bf16 outputs one bf16 term.
-// The MMA warp issues QK^T of tile j+1 before PV of tile j, so the score
-// product overlaps the softmax.
+// QK^T and PV are issued by two threads in different warps (one thread
+// cannot issue these small MMAs fast enough to keep the tensor pipe busy),
+// and S is double-buffered for NR = 16, so the score product of tile j+1
+// overlaps the softmax and the value product of tile j.
 //
 // Warp roles: producer (TMA tile loads through the block table; for sparse,
-// 4 warps of 16-byte cp.async row gathers), one MMA-issuing warp, and four
-// softmax warps (one per TMEM lane quarter) that also rescale O^T, zero the
-// value rows of keys past the chunk end, and write the outputs.  A 3-stage
-// shared-memory ring of 64-key tiles (72 KB each) keeps ~144 KB of KV loads
-// in flight per SM.  The online softmax rescales O^T lazily: the running
+// 4 warps of 16-byte cp.async row gathers), the QK^T warp (also owns TMEM),
+// four softmax warps (one per TMEM lane quarter) that also rescale O^T, zero
+// the value rows of keys past the chunk end, write the outputs and merge
+// split chunks, and the PV warp.  A 3-stage shared-memory ring of 64-key
+// tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM.  The
+// online softmax rescales O^T lazily: the running
 // reference max only moves when a tile's max exceeds it by more than 2^8.
 #include "common.cuh"
 #include "decode_args.h"
