@@ -48,7 +48,7 @@ struct ReqInfo {
   int32_t local_len;  // keys this shard holds
   int32_t rows;       // q_len * H (token-major: row = i * H + h)
   int32_t pair_base;  // first (request, row group) pair of the request
-  int32_t pad[2];
+  int64_t item_base;  // the request's first item in the flattened work list
 };
 
 // One (request, row group): rows [row0, row0 + nrows) of request b and the
@@ -73,14 +73,10 @@ struct __align__(16) PairInfo {
   int32_t q_len;
   int32_t seq_len;    // global
   int32_t local_len;  // keys this shard holds
+  int32_t cta0;       // decode CTA that owns item0 (chunk index = CTA - cta0)
+  int32_t pad[3];
 };
-static_assert(sizeof(PairInfo) == 48, "pair size");
-
-// CTA that owns work item i when W items are divided over G CTAs as
-// [floor(c W / G), floor((c + 1) W / G)).
-__host__ __device__ __forceinline__ int64_t item_owner(int64_t i, int64_t W, int64_t G) {
-  return ((i + 1) * G + W - 1) / W - 1;
-}
+static_assert(sizeof(PairInfo) == 64, "pair size");
 
 __device__ __forceinline__ void record_check(WorkspaceHeader* hdr, int32_t code) {
   if (atomicCAS(&hdr->status, 0, (int32_t)MLA_ERR_DEVICE_CHECK) == 0) hdr->detail = code;

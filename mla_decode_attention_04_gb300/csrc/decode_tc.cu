@@ -69,6 +69,7 @@ struct TcShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
+  uint64_t merge_full;  // bulk loads of a split pair's partials (end-of-CTA merges)
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
@@ -121,13 +122,16 @@ struct UnitIter {
       u = blockIdx.x;
       units = a.num_tokens * a.groups_per_token;
     } else {
-      // the scheduler balanced the W items over min(grid, W) non-empty ranges
+      // the scheduler balanced the W items over min(grid, W) non-empty ranges;
+      // this CTA's first pair is read together with W (one memory latency)
+      // and used only if the CTA has a range
+      const int p_first = a.cta_pair0[blockIdx.x];
       W = a.hdr->total_items;
       G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
       if ((int64_t)blockIdx.x < G && W > 0) {
         i = (int64_t)blockIdx.x * W / G;
         hi = ((int64_t)blockIdx.x + 1) * W / G;
-        p = a.cta_pair0[blockIdx.x];
+        p = p_first;
         nxt = a.pairs[p];
       } else {
         i = hi = 0;
@@ -177,7 +181,7 @@ struct UnitIter {
       w.key1 = min((int)(end - pi.item0) * kKeyTile, pi.local_len);
       w.n_kt = (int)(end - i);
       w.nsplit = pi.nsplit;
-      w.split = pi.nsplit > 1 ? (int)(item_owner(i, W, G) - item_owner(pi.item0, W, G)) : 0;
+      w.split = pi.nsplit > 1 ? (int)blockIdx.x - pi.cta0 : 0;  // the unit's items are this CTA's
       w.pbase = pi.pbase;
       w.q0 = pi.q0;
       w.q_len = pi.q_len;
@@ -314,6 +318,94 @@ __device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Un
   }
 }
 
+// The same merge once this CTA has no more tiles to stream: the ring's shared
+// memory is idle, so the pair's partials (LSE and o of every chunk, one
+// contiguous run of slots) arrive with one bulk copy instead of several
+// dependent rounds of loads.  Returns false, having done nothing, when they
+// do not fit (the caller then merges through registers).
+template <int NR>
+__device__ __forceinline__ bool merge_split_chunks_smem(const DecodeArgs& a, const Unit& u, TcShared& sh, int st_tid,
+                                                        uint8_t* ring, uint32_t& merge_phase, bool& ok) {
+  const uint32_t o_bytes = (uint32_t)u.nsplit * NR * kNope * 4, l_bytes = (uint32_t)u.nsplit * NR * 4;
+  if (o_bytes + l_bytes > (uint32_t)(kStages * kStageBytes)) return false;
+  float* so = reinterpret_cast<float*>(ring);              // [nsplit * NR][512]
+  float* sl = reinterpret_cast<float*>(ring + o_bytes);    // [nsplit * NR]
+  if (st_tid == 0) {
+    __threadfence();
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(&sh.merge_full, o_bytes + l_bytes);
+    bulk_load(so, a.part_o + (int64_t)u.pbase * kNope, o_bytes, &sh.merge_full);
+    bulk_load(sl, a.part_lse + u.pbase, l_bytes, &sh.merge_full);
+    sh.wait_ok = mbar_wait(&sh.merge_full, merge_phase) ? 1 : 0;
+  }
+  named_bar_sync(1, 128);
+  if (!sh.wait_ok) {
+    ok = false;
+    merge_phase ^= 1;
+    return true;
+  }
+  // every reader observes the completed phase itself (returns at once)
+  if (st_tid != 0) mbar_wait(&sh.merge_full, merge_phase);
+  merge_phase ^= 1;
+  // (1) each row's LSE over the chunks (thread n < nrows)
+  if (st_tid < u.nrows) {
+    const int n = st_tid;
+    float m = -INFINITY;
+    for (int sp = 0; sp < u.nsplit; ++sp) m = fmaxf(m, sl[sp * NR + n]);
+    float lse = -INFINITY;
+    if (m > -INFINITY) {
+      float z = 0.f;
+      for (int sp = 0; sp < u.nsplit; ++sp) z += fast_exp2((sl[sp * NR + n] - m) * kLog2e);
+      lse = m + __logf(z);
+    }
+    sh.alpha[n] = lse;
+    a.lse[(int64_t)u.q0 * a.num_heads + u.row0 + n] = lse;
+  }
+  named_bar_sync(1, 128);
+  // (2) weighted sum: thread st_tid owns latent dims [4 st_tid, 4 st_tid + 4)
+  // of 8 rows at a time (independent chains, so their latencies overlap)
+  const int d0 = st_tid * 4;
+#pragma unroll 1
+  for (int n0 = 0; n0 < u.nrows; n0 += 8) {
+    float4 acc[8];
+    float lrow[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      lrow[k] = n0 + k < u.nrows ? sh.alpha[n0 + k] : -INFINITY;
+    }
+#pragma unroll 1
+    for (int sp = 0; sp < u.nsplit; ++sp) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float lv = n0 + k < u.nrows ? sl[sp * NR + n0 + k] : -INFINITY;
+        if (lrow[k] > -INFINITY && lv > -INFINITY) {
+          const float wgt = fast_exp2((lv - lrow[k]) * kLog2e);
+          const float4 v = *reinterpret_cast<const float4*>(so + (int64_t)(sp * NR + n0 + k) * kNope + d0);
+          acc[k].x += wgt * v.x;
+          acc[k].y += wgt * v.y;
+          acc[k].z += wgt * v.z;
+          acc[k].w += wgt * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (n0 + k >= u.nrows) break;
+      const int64_t g = (int64_t)u.q0 * a.num_heads + u.row0 + n0 + k;
+      if (a.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
+      } else {
+        const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+        const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
+      }
+    }
+  }
+  return true;
+}
+
 template <int NR, bool SPARSE>
 __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeArgs a) {
@@ -346,6 +438,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.unit_done, 1);
     mbar_init(&sh.q_ready, 1);
+    mbar_init(&sh.merge_full, 1);
     sh.any_rescale[0] = sh.any_rescale[1] = 0;
     fence_mbar_init();
   }
@@ -626,6 +719,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     bool have_pend = false;
     Unit mrg;                // pair whose chunks this CTA merges next
     bool have_mrg = false;
+    uint32_t merge_phase = 0;
     bool more = it.next(a, wn);
     if (more && wn.n_kt > 0) load_q(wn);
     while (ok && more) {
@@ -817,12 +911,17 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
       named_bar_sync(1, 128);
       if (have_mrg) {
-        merge_split_chunks<NR>(a, mrg, sh, st_tid);
+        // after this CTA's last unit the ring is idle: merge through it
+        if (more || !merge_split_chunks_smem<NR>(a, mrg, sh, st_tid, kv, merge_phase, ok))
+          merge_split_chunks<NR>(a, mrg, sh, st_tid);
         have_mrg = false;
         named_bar_sync(1, 128);
       }
     }
-    if (ok && have_pend && count_chunk(pend)) merge_split_chunks<NR>(a, pend, sh, st_tid);
+    if (ok && have_pend && count_chunk(pend)) {
+      if (!merge_split_chunks_smem<NR>(a, pend, sh, st_tid, kv, merge_phase, ok))
+        merge_split_chunks<NR>(a, pend, sh, st_tid);
+    }
   }
 
   if (!ok) record_check(a.hdr, kCheckWaitTimeout);

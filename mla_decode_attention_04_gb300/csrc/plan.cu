@@ -23,32 +23,35 @@ namespace mla {
 
 namespace {
 
-// Exclusive block-wide scan of one int per thread (blockDim.x == 1024).
-__device__ long long block_exclusive_scan(long long v, long long* warp_sums, long long* total) {
+// Exclusive block-wide scans of two values per thread (blockDim.x == 1024)
+// with one set of barriers; totals in tot[0..1].
+__device__ void block_exclusive_scan2(long long v0, long long v1, longlong2* warp_sums, long long* tot,
+                                      long long& r0, long long& r1) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long x = v;
+  long long x0 = v0, x1 = v1;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const long long y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    if (lane >= o) x0 += y0, x1 += y1;
   }
-  if (lane == 31) warp_sums[warp] = x;
+  if (lane == 31) warp_sums[warp] = make_longlong2(x0, x1);
   __syncthreads();
   if (warp == 0) {
-    long long w = warp_sums[lane];
-    long long s = w;
+    const longlong2 w = warp_sums[lane];
+    long long s0 = w.x, s1 = w.y;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      long long y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
+      const long long y0 = __shfl_up_sync(0xffffffffu, s0, o), y1 = __shfl_up_sync(0xffffffffu, s1, o);
+      if (lane >= o) s0 += y0, s1 += y1;
     }
-    warp_sums[lane] = s - w;
-    if (lane == 31) *total = s;
+    warp_sums[lane] = make_longlong2(s0 - w.x, s1 - w.y);
+    if (lane == 31) tot[0] = s0, tot[1] = s1;
   }
   __syncthreads();
-  long long r = warp_sums[warp] + x - v;
+  const longlong2 base = warp_sums[warp];
+  r0 = base.x + x0 - v0;
+  r1 = base.y + x1 - v1;
   __syncthreads();
-  return r;
 }
 
 struct ReqPlan {
@@ -72,12 +75,13 @@ __device__ ReqPlan plan_request(const SchedArgs& a, int b) {
 }  // namespace
 
 __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
-  __shared__ long long warp_sums[32];
-  __shared__ long long s_total;
+  __shared__ longlong2 warp_sums[32];
+  __shared__ long long s_tot[2];
   __shared__ int s_overflow;
   grid_dep_sync();
   WorkspaceHeader* hdr = a.hdr;
   const int H = a.num_heads, NR = a.rows_per_group;
+  const long long pen = a.unit_penalty;
   if (threadIdx.x == 0) {
     s_overflow = 0;
     hdr->status = 0;  // this call's checks start clean (no kernel of it has run yet)
@@ -85,18 +89,24 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
   }
   for (int t = threadIdx.x; t < a.num_tokens; t += blockDim.x) a.tok2req[t] = -1;
   __syncthreads();
+  // with at most one request per thread (every workload the decode targets)
+  // pass 2 takes pass 1's values from registers instead of re-reading them
+  const bool single = a.num_requests <= (int)blockDim.x;
 
   // pass 1: pair and item prefix sums over requests
   long long pair_carry = 0, item_carry = 0;
+  ReqPlan p1{};
+  long long pair_off1 = 0, item_off1 = 0;
   for (int base = 0; base < a.num_requests; base += blockDim.x) {
     const int b = base + threadIdx.x;
     ReqPlan p{};
     if (b < a.num_requests) p = plan_request(a, b);
-    const long long pair_off = block_exclusive_scan(p.groups, warp_sums, &s_total) + pair_carry;
-    const long long pair_tot = s_total;
-    const long long vlen = p.nt > 0 ? (long long)p.nt + a.unit_penalty : 0;  // list items of one pair
-    const long long item_off = block_exclusive_scan((long long)p.groups * vlen, warp_sums, &s_total) + item_carry;
-    const long long item_tot = s_total;
+    const long long vlen = p.nt > 0 ? (long long)p.nt + pen : 0;  // list items of one pair
+    long long pair_off, item_off;
+    block_exclusive_scan2(p.groups, (long long)p.groups * vlen, warp_sums, s_tot, pair_off, item_off);
+    pair_off += pair_carry;
+    item_off += item_carry;
+    const long long pair_tot = s_tot[0], item_tot = s_tot[1];
     if (b < a.num_requests) {
       if (!p.ok) record_check(hdr, kCheckBadQueryLayout);
       ReqInfo ri{};
@@ -106,27 +116,12 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
       ri.local_len = p.Lr;
       ri.rows = p.q_len * H;
       ri.pair_base = (int)pair_off;
+      ri.item_base = item_off;
       a.req[b] = ri;
       if (pair_off + p.groups > a.max_pairs) {
         s_overflow = 1;
       } else {
-        // provisional pair entries (split plan filled in pass 2)
-        for (int g = 0; g < p.groups; ++g) {
-          PairInfo pi{};
-          pi.item0 = item_off + (long long)g * vlen + (p.nt > 0 ? a.unit_penalty : 0);
-          pi.b = b;
-          pi.row0 = g * NR;
-          pi.nrows = min(NR, ri.rows - g * NR);
-          pi.nt = p.nt;
-          pi.nsplit = 1;
-          pi.pbase = 0;
-          pi.q0 = ri.q0;
-          pi.q_len = ri.q_len;
-          pi.seq_len = ri.seq_len;
-          pi.local_len = ri.local_len;
-          a.pairs[pair_off + g] = pi;
-          a.pair_done[pair_off + g] = 0;
-        }
+        for (int g = 0; g < p.groups; ++g) a.pair_done[pair_off + g] = 0;
       }
       if (p.nt == 0 && p.q_len > 0) {
         // no local key: the rows' final result (no decode unit covers them)
@@ -151,6 +146,9 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
         }
       }
     }
+    p1 = p;
+    pair_off1 = pair_off;
+    item_off1 = item_off;
     pair_carry += pair_tot;
     item_carry += item_tot;
   }
@@ -159,45 +157,89 @@ __global__ void __launch_bounds__(1024) schedule_kernel(SchedArgs a) {
   // range boundary inside a pair starts a real chunk and the chunk index of
   // a unit is its owner minus the owner of the pair's first item
   const long long W = item_carry, G = (long long)a.grid < W ? (long long)a.grid : (W > 0 ? W : 1);
+  // Range ownership: CTA c's range is [floor(c W / G), floor((c + 1) W / G)).
+  // Integer division is a long dependent sequence on the GPU and these run
+  // several times per pair on few threads, so each quotient is a float
+  // estimate (t * (1 / W)) corrected with exact integer products.
+  const float rW = W > 0 ? 1.0f / (float)W : 0.f;
+  auto quot_floor = [&](long long t) -> long long {  // floor(t / W), t >= 0
+    long long q = (long long)((float)t * rW);
+    while (q > 0 && q * W > t) --q;
+    while ((q + 1) * W <= t) ++q;
+    return q;
+  };
+  // largest c with c W < (i + 1) G, i.e. ceil((i + 1) G / W) - 1
+  auto owner = [&](long long i) -> long long { return quot_floor((i + 1) * G - 1); };
+  // smallest c with c W >= v G, i.e. ceil(v G / W)
+  auto first_start_at_or_after = [&](long long v) -> long long { return v > 0 ? quot_floor(v * G - 1) + 1 : 0; };
 
-  // pass 2: chunks per pair (how many CTA ranges cut it) and partial slots
+  // pass 2: chunks per pair (how many CTA ranges cut it), partial slots, and
+  // the final pair records
   long long part_carry = 0;
   for (int base = 0; base < a.num_requests; base += blockDim.x) {
     const int b = base + threadIdx.x;
-    long long parts = 0;
-    int pb = 0, groups = 0;
-    if (b < a.num_requests && !s_overflow) {
-      pb = a.req[b].pair_base;
-      const ReqPlan p = plan_request(a, b);
-      groups = p.groups;
-      for (int g = 0; g < groups; ++g) {
-        PairInfo& pi = a.pairs[pb + g];
-        int ns = 1;
-        if (pi.nt > 0 && W > 0) {
-          ns = (int)(item_owner(pi.item0 + pi.nt - 1, W, G) - item_owner(pi.item0, W, G) + 1);
-          // CTA c's range starts at item floor(c W / G): the CTAs whose range
-          // starts inside the pair's list items [item0 - penalty, item0 + nt)
-          // begin with this pair
-          const long long v0 = pi.item0 - a.unit_penalty;
-          const long long c_lo = (v0 * G + W - 1) / W, c_hi = ((pi.item0 + pi.nt) * G + W - 1) / W;
-          for (long long c = c_lo; c < c_hi; ++c) a.cta_pair0[c] = pb + g;
-        }
-        pi.nsplit = ns;
-        if (ns > 1) parts += (long long)ns * NR;
+    const bool mine = b < a.num_requests && !s_overflow;
+    ReqPlan p{};
+    long long pb = 0, ib = 0;
+    if (mine) {
+      if (single) {
+        p = p1;
+        pb = pair_off1;
+        ib = item_off1;
+      } else {
+        p = plan_request(a, b);
+        const ReqInfo ri = a.req[b];
+        pb = ri.pair_base;
+        ib = ri.item_base;
       }
     }
-    long long part_off = block_exclusive_scan(parts, warp_sums, &s_total) + part_carry;
-    const long long part_tot = s_total;
-    if (b < a.num_requests && !s_overflow) {
+    const long long vlen = p.nt > 0 ? (long long)p.nt + pen : 0;
+    const int rows = p.q_len * H;
+    // chunks of pair g: CTA c's range starts at item floor(c W / G)
+    auto nsplit_of = [&](long long item0) -> int {
+      return (p.nt > 0 && W > 0) ? (int)(owner(item0 + p.nt - 1) - owner(item0) + 1) : 1;
+    };
+    long long parts = 0;
+    if (mine) {
+      for (int g = 0; g < p.groups; ++g) {
+        const long long item0 = ib + g * vlen + (p.nt > 0 ? pen : 0);
+        const int ns = nsplit_of(item0);
+        if (ns > 1) parts += (long long)ns * NR;
+        if (p.nt > 0 && W > 0) {
+          // the CTAs whose range starts inside the pair's list items
+          // [item0 - penalty, item0 + nt) begin with this pair
+          const long long c_lo = first_start_at_or_after(item0 - pen), c_hi = first_start_at_or_after(item0 + p.nt);
+          for (long long c = c_lo; c < c_hi; ++c) a.cta_pair0[c] = (int)(pb + g);
+        }
+      }
+    }
+    long long part_off, unused;
+    block_exclusive_scan2(parts, 0, warp_sums, s_tot, part_off, unused);
+    part_off += part_carry;
+    const long long part_tot = s_tot[0];
+    if (mine) {
       if (part_off + parts > a.max_partial_rows) {
         s_overflow = 1;
       } else {
-        for (int g = 0; g < groups; ++g) {
-          PairInfo& pi = a.pairs[pb + g];
+        for (int g = 0; g < p.groups; ++g) {
+          PairInfo pi{};
+          pi.item0 = ib + g * vlen + (p.nt > 0 ? pen : 0);
+          pi.b = b;
+          pi.row0 = g * NR;
+          pi.nrows = min(NR, rows - g * NR);
+          pi.nt = p.nt;
+          pi.cta0 = (p.nt > 0 && W > 0) ? (int)owner(pi.item0) : 0;
+          pi.nsplit = (p.nt > 0 && W > 0) ? (int)(owner(pi.item0 + p.nt - 1) - pi.cta0 + 1) : 1;
+          pi.pbase = 0;
           if (pi.nsplit > 1) {
             pi.pbase = (int)part_off;
             part_off += (long long)pi.nsplit * NR;
           }
+          pi.q0 = p.q0;
+          pi.q_len = p.q_len;
+          pi.seq_len = p.L;
+          pi.local_len = p.Lr;
+          a.pairs[pb + g] = pi;
         }
       }
     }
