@@ -64,6 +64,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // hi at offset 0 and lo = bf16(P - hi) at offset kPBytes.
 constexpr int kPBytes = 32 * 128;
 constexpr int kPChunk = 8;  // the k_pe chunk of a stage
+// Dense units: the unit's Q rows travel through the ring as one slot ahead of
+// its key tiles (row r at r * kQRowBytes; the 16-byte pad puts consecutive
+// rows in different banks for the softmax warps' row reads).
+constexpr int kQRowBytes = kRow * 2 + 16;
 
 struct TcShared {
   uint64_t full[kStages];
@@ -467,6 +471,22 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       Unit w;
       int cache_b = -1, cache_col = 0, my_page = -1;
       while (ok && it.next(a, w)) {
+        if (w.n_kt > 0) {
+          // the unit's Q rows: one slot of the ring, a bulk copy per row half
+          if (lane == 0) {
+            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) ok = false;
+            else mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          uint8_t* qdst = kv + stage * kStageBytes;
+          for (int r = lane; r < w.nrows; r += 32) {
+            const int64_t grow = (int64_t)w.q0 * a.num_heads + w.row0 + r;
+            bulk_load(qdst + r * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
+            bulk_load(qdst + r * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage]);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
           const int k = w.key0 + kt * kKeyTile;
           int pages[kKeyTile / 8];
@@ -574,6 +594,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         // landed and the softmax has copied S(j - SB) out of that buffer.
         while (ok && it.next(a, w)) {
           if (w.n_kt == 0) continue;
+          if (!SPARSE && ++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
           if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
           q_ph ^= 1;
           tc_fence_after();
@@ -601,6 +622,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         // reader, completed before the softmax saw S(j)).
         while (ok && it.next(a, w)) {
           if (w.n_kt == 0) continue;
+          if (!SPARSE && ++stage == kStages) stage = 0;  // the unit's Q slot
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
             if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
             tc_fence_after();
@@ -644,7 +666,8 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     const float scale_log2 = a.scale * kLog2e;
     const int H = a.num_heads;
     uint32_t j = 0, u_ph = 0;
-    int stage = 0;
+    int stage = 0;          // ring slot of the next tile (dense: or of the next unit's Q)
+    uint32_t sphase = 0;    // its full-barrier parity
     // One thread waits; the named barrier hands its verdict to the group, so
     // the 128 threads always take the same branch (no thread is left at a
     // barrier the others skipped).  Consecutive calls are separated by at
@@ -663,42 +686,67 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     };
     // Q rows of unit u into TMEM, then q_ready.  Called once every QK^T
     // issued so far is complete (the softmax has read all their S).
-    auto load_q = [&](const Unit& u) {
+    auto load_q = [&](const Unit& u) -> bool {
       // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
-      // (the TPR lanes of a row read the same addresses: one request per warp)
+      // (the TPR lanes of a row read the same addresses)
       const bool have = row < u.nrows;
-      const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow_of(u, row) * a.q_nope_stride) : nullptr;
-      const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow_of(u, row) * a.q_pe_stride) : nullptr;
-      // batches of 64-dim chunks (dense: five then four; sparse, with fewer
-      // registers per thread: three): all loads of a batch are in flight
-      // before its first store, so a unit pays two or three load latencies
-      constexpr int kQB = SPARSE ? 3 : 5;
+      if constexpr (!SPARSE) {
+        // dense: the rows are in this unit's Q slot of the ring
+        if (!group_wait(&sh.full[stage], sphase)) return false;
+        mbar_wait(&sh.full[stage], sphase);  // every reader observes the phase (returns at once)
+        const uint8_t* qrow = kv + stage * kStageBytes + row * kQRowBytes;
 #pragma unroll 1
-      for (int cb = 0; cb < 9; cb += kQB) {
-        uint4 x[8 * kQB];
-#pragma unroll
-        for (int q = 0; q < kQB; ++q) {
-          const int c = cb + q;
-          const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) x[8 * q + v] = have && c < 9 ? src[v] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int q = 0; q < kQB; ++q) {
-          if (cb + q >= 9) break;
+        for (int c = 0; c < 9; ++c) {
           uint32_t r[32];
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
-            r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
+            const uint4 x = have ? *reinterpret_cast<const uint4*>(qrow + c * 128 + v * 16) : make_uint4(0, 0, 0, 0);
+            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
           }
-          tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
+          tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
         }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) {
+          mbar_arrive(&sh.empty[stage]);
+          mbar_arrive(&sh.q_ready);
+        }
+        if (++stage == kStages) { stage = 0; sphase ^= 1; }
+      } else {
+        const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow_of(u, row) * a.q_nope_stride) : nullptr;
+        const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow_of(u, row) * a.q_pe_stride) : nullptr;
+        // three 64-dim chunks per batch: all loads of a batch are in flight
+        // before its first store, so a unit pays three load latencies
+        constexpr int kQB = 3;
+#pragma unroll 1
+        for (int cb = 0; cb < 9; cb += kQB) {
+          uint4 x[8 * kQB];
+#pragma unroll
+          for (int q = 0; q < kQB; ++q) {
+            const int c = cb + q;
+            const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int q = 0; q < kQB; ++q) {
+            uint32_t r[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
+              r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
+            }
+            tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(1, 128);
+        if (st_tid == 0) mbar_arrive(&sh.q_ready);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(1, 128);
-      if (st_tid == 0) mbar_arrive(&sh.q_ready);
+      return true;
     };
     // A split pair's chunk is counted one tile after its epilogue (or at the
     // end), so the fence and the atomic's round trip overlap the next unit's
@@ -721,7 +769,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     bool have_mrg = false;
     uint32_t merge_phase = 0;
     bool more = it.next(a, wn);
-    if (more && wn.n_kt > 0) load_q(wn);
+    if (more && wn.n_kt > 0 && !load_q(wn)) ok = false;
     while (ok && more) {
       w = wn;
       more = it.next(a, wn);
@@ -845,7 +893,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         tc_fence_before();
         named_bar_sync(1, 128);
         if (st_tid == 0) mbar_arrive(&sh.p_ready);
-        if (++stage == kStages) stage = 0;
+        if (++stage == kStages) { stage = 0; sphase ^= 1; }
         if (have_pend) {
           if (count_chunk(pend)) {
             mrg = pend;
@@ -857,7 +905,10 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       if (!ok) break;
       // the next unit's Q goes in now, so that its first QK^T overlaps this
       // unit's epilogue
-      if (more && wn.n_kt > 0) load_q(wn);
+      if (more && wn.n_kt > 0 && !load_q(wn)) {
+        ok = false;
+        break;
+      }
 
       // ---- epilogue of the unit
       if (w.n_kt > 0) {
