@@ -17,7 +17,7 @@ constexpr int kKeyTile = 64;             // keys per pipeline tile of the decode
 // A decode CTA that starts a (request, row group) unit pays for loading its Q
 // into TMEM and for the previous unit's epilogue, about as long as streaming
 // this many key tiles; the split scheduler charges it to every unit.
-constexpr int kUnitPenalty = 6;
+constexpr int kUnitPenalty = 4;
 constexpr int kMaxHeads = 128;
 
 // Device status word codes (first failure wins).
