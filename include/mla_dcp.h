@@ -219,7 +219,10 @@ int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
  *    per device, with that device current); make that first call before any
  *    stream capture on the device.
  *  - Problems whose scratch (mla_dcp_decode_workspace_size) exceeds the
- *    array are refused with MLA_ERR_WORKSPACE before anything runs.
+ *    array are refused with MLA_ERR_WORKSPACE before anything runs.  The
+ *    dense workspace is bounded by the GPU's SM count (at most 2 x SMs x 32
+ *    partial rows of 2 KB plus small tables), so on a 152-SM GB300 every
+ *    problem fits.
  *  - Every call shares the one array: calls that may overlap on the GPU
  *    (unordered streams) race on it.  Calls on one stream are fine.  The
  *    array keeps the last call's contents; what must start at zero (the
@@ -228,7 +231,7 @@ int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
  *    variant are not reported.
  *  - It allocates nothing and calls no allocating routine.
  * ---------------------------------------------------------------------- */
-#define MLA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define MLA_STATIC_SCRATCH_BYTES (24u * 1024u * 1024u)
 
 int mla_dcp_decode_static_scratch(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe,
                                   int64_t q_pe_row_stride, const void *kv_cache, int64_t num_blocks, int32_t page_size,

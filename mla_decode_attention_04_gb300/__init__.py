@@ -37,7 +37,7 @@ EXPORTS = [
 # Size of the library's fixed device scratch array used by
 # mla_dcp_decode_static_scratch (the entry point for callers that cannot
 # allocate device memory); see include/mla_dcp.h.
-MLA_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+MLA_STATIC_SCRATCH_BYTES = 24 * 1024 * 1024
 
 
 class MlaError(RuntimeError):

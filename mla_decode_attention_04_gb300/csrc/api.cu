@@ -136,31 +136,29 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
 
   cudaError_t e;
-  mla::SchedArgs sa{};
-  sa.seq_lens = seq_lens;
-  sa.query_start_loc = query_start_loc;
-  sa.num_requests = num_requests;
-  sa.num_tokens = num_tokens;
-  sa.num_heads = num_heads;
-  sa.dcp_world = dcp_world;
-  sa.dcp_rank = dcp_rank;
-  sa.rows_per_group = plan.rows_per_group;
-  sa.grid = plan.grid;
-  sa.unit_penalty = plan.unit_penalty;
-  sa.max_pairs = plan.max_pairs;
-  sa.max_partial_rows = (int32_t)plan.max_partial_rows;
-  sa.hdr = hdr;
-  sa.req = reinterpret_cast<mla::ReqInfo*>(ws + plan.off_req);
-  sa.pairs = reinterpret_cast<mla::PairInfo*>(ws + plan.off_pairs);
-  sa.tok2req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
-  sa.pair_done = reinterpret_cast<int32_t*>(ws + plan.off_cnt);
-  sa.cta_pair0 = reinterpret_cast<int32_t*>(ws + plan.off_cta);
-  sa.row_counts = row_counts;
-  sa.out = out;
-  sa.out_f32 = out_dtype == MLA_DTYPE_F32;
-  sa.lse = lse;
-  if ((e = mla::launch_pdl(mla::schedule_kernel, dim3(1), dim3(1024), 0, st, sa)) != cudaSuccess)
-    return cuda_fail(e, "schedule_kernel launch");
+  mla::PrepArgs pa{};
+  pa.seq_lens = seq_lens;
+  pa.query_start_loc = query_start_loc;
+  pa.num_requests = num_requests;
+  pa.num_tokens = num_tokens;
+  pa.num_heads = num_heads;
+  pa.dcp_world = dcp_world;
+  pa.dcp_rank = dcp_rank;
+  pa.rows_per_group = plan.rows_per_group;
+  pa.grid = plan.grid;
+  pa.hdr = hdr;
+  pa.pair_done = reinterpret_cast<int32_t*>(ws + plan.off_cnt);
+  pa.row_counts = row_counts;
+  pa.out = out;
+  pa.out_f32 = out_dtype == MLA_DTYPE_F32;
+  pa.lse = lse;
+  {
+    const int work = num_requests > plan.grid ? num_requests : plan.grid;
+    int blocks = (work + 255) / 256;
+    if (blocks > 64) blocks = 64;
+    if ((e = mla::launch_pdl(mla::prep_kernel, dim3(blocks), dim3(256), 0, st, pa)) != cudaSuccess)
+      return cuda_fail(e, "prep_kernel launch");
+  }
   count_launch();
 
   mla::DecodeArgs da{};
@@ -181,10 +179,11 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
   da.lse = lse;
   da.hdr = hdr;
-  da.req = sa.req;
-  da.pairs = sa.pairs;
-  da.pair_done = sa.pair_done;
-  da.cta_pair0 = sa.cta_pair0;
+  da.seq_lens = seq_lens;
+  da.query_start_loc = query_start_loc;
+  da.num_requests = num_requests;
+  da.unit_penalty = plan.unit_penalty;
+  da.pair_done = pa.pair_done;
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
   da.num_tokens = num_tokens;

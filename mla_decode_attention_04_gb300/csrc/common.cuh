@@ -14,9 +14,9 @@ constexpr int kRope = MLA_ROPE_DIM;      // 64: width of k_pe and q_pe
 constexpr int kRow = MLA_KV_ROW;         // 576: one latent cache row
 constexpr int kVHead = MLA_V_HEAD_DIM;   // 128: W_UV output width per head
 constexpr int kKeyTile = 64;             // keys per pipeline tile of the decode kernels
-// A decode CTA that starts a (request, row group) unit pays for loading its Q
+// A decode CTA that starts a (request, row group) unit pays for moving its Q
 // into TMEM and for the previous unit's epilogue, about as long as streaming
-// this many key tiles; the split scheduler charges it to every unit.
+// this many key tiles; the split-KV balance charges it to every unit.
 constexpr int kUnitPenalty = 4;
 constexpr int kMaxHeads = 128;
 
@@ -31,52 +31,11 @@ enum DeviceCheck : int32_t {
 
 // Workspace header, at offset 0 of every decode workspace.
 struct WorkspaceHeader {
-  int32_t status;       // 0 or MLA_ERR_DEVICE_CHECK
-  int32_t detail;       // DeviceCheck code of the first failure
-  int32_t num_pairs;    // (request, row group) pairs written by the scheduler
-  int32_t pad0;
-  int64_t total_items;  // key tiles over all pairs (0: nothing to run)
-  int32_t pad[58];      // header is 256 bytes
+  int32_t status;  // 0 or MLA_ERR_DEVICE_CHECK
+  int32_t detail;  // DeviceCheck code of the first failure
+  int32_t pad[62];  // header is 256 bytes
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header size");
-
-// Per-request facts derived on the device by the scheduler.
-struct ReqInfo {
-  int32_t q0;         // query_start_loc[b]
-  int32_t q_len;
-  int32_t seq_len;    // global
-  int32_t local_len;  // keys this shard holds
-  int32_t rows;       // q_len * H (token-major: row = i * H + h)
-  int32_t pair_base;  // first (request, row group) pair of the request
-  int64_t item_base;  // the request's first item in the flattened work list
-};
-
-// One (request, row group): rows [row0, row0 + nrows) of request b and the
-// nt 64-key tiles of its local keys, which are the work items
-// [item0, item0 + nt) of the flattened list that the decode grid divides into
-// equal contiguous ranges.  Each pair with keys is preceded in that list by
-// kUnitPenalty items without work (the cost of starting a unit), so a range
-// that starts units gets fewer key tiles.  A pair crossing range boundaries is computed in
-// nsplit chunks whose partial results sit at slots pbase + split * NR + row
-// and are merged by the decode CTA that finishes the pair's last chunk.  The
-// request's facts are repeated here so that a decode CTA reads one record per
-// unit.
-struct __align__(16) PairInfo {
-  int64_t item0;
-  int32_t b;
-  int32_t row0;
-  int32_t nrows;
-  int32_t nt;
-  int32_t nsplit;
-  int32_t pbase;
-  int32_t q0;         // the request's query_start_loc
-  int32_t q_len;
-  int32_t seq_len;    // global
-  int32_t local_len;  // keys this shard holds
-  int32_t cta0;       // decode CTA that owns item0 (chunk index = CTA - cta0)
-  int32_t pad[3];
-};
-static_assert(sizeof(PairInfo) == 64, "pair size");
 
 __device__ __forceinline__ void record_check(WorkspaceHeader* hdr, int32_t code) {
   if (atomicCAS(&hdr->status, 0, (int32_t)MLA_ERR_DEVICE_CHECK) == 0) hdr->detail = code;
@@ -94,14 +53,53 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int32_t P, int32_t D, i
   return P >= r ? (P - r) / D + 1 : 0;
 }
 
+// What the dense decode needs to know about request b, from seq_lens and
+// query_start_loc alone (the prep kernel and every decode CTA derive it the
+// same way).  A malformed query range (ok false) is treated as q_len 0.
+struct ReqFacts {
+  int32_t q0, q_len, seq_len, local_len, groups, nt;
+  bool ok;
+};
+
+__device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const int32_t* query_start_loc, int b,
+                                                  int num_tokens, int H, int D, int r, int NR) {
+  ReqFacts f;
+  const int q0 = query_start_loc[b], q1 = query_start_loc[b + 1], L = seq_lens[b];
+  f.ok = !(q1 - q0 < 0 || q1 - q0 > L || q0 < 0 || q1 > num_tokens);
+  f.q0 = q0 < 0 ? 0 : q0;
+  f.q_len = f.ok ? q1 - q0 : 0;
+  f.seq_len = L;
+  f.local_len = local_len(L, D, r);
+  f.groups = (f.q_len * H + NR - 1) / NR;
+  f.nt = (f.local_len + kKeyTile - 1) / kKeyTile;
+  return f;
+}
+
+// floor(t / W) for t >= 0, W > 0: a float estimate of the quotient corrected
+// with exact integer products (64-bit division is a long dependent sequence).
+__device__ __forceinline__ int64_t quot_floor(int64_t t, int64_t W) {
+  int64_t q = (int64_t)((float)t * (1.0f / (float)W));
+  while (q > 0 && q * W > t) --q;
+  while ((q + 1) * W <= t) ++q;
+  return q;
+}
+
+// CTA owning item i when W items are cut into G ranges
+// [floor(c W / G), floor((c + 1) W / G)): ceil((i + 1) G / W) - 1.
+__device__ __forceinline__ int64_t range_owner(int64_t i, int64_t W, int64_t G) {
+  return quot_floor((i + 1) * G - 1, W);
+}
+
 // Programmatic dependent launch.  Every kernel of the library is launched
-// so that it may start while the previous kernel in the stream finishes;
-// it lets its own successor launch at once and waits, before its first
-// global access, until the predecessor has completed and its writes are
-// visible (a no-op when launched without the attribute).
+// so that it may start while the previous kernel in the stream finishes.
+// grid_dep_launch lets this kernel's successor launch; grid_dep_wait blocks
+// until the predecessor has completed and its writes are visible (both are
+// no-ops when the kernel was launched without the attribute).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_sync() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dep_launch();
+  grid_dep_wait();
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

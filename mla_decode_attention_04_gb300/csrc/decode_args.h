@@ -21,13 +21,14 @@ struct DecodeArgs {
   int32_t out_f32;
   float* lse;  // [T, H]
   WorkspaceHeader* hdr;
-  // dense
-  const ReqInfo* req;
-  const PairInfo* pairs;
-  int32_t* pair_done;  // finished KV chunks per pair (the last finisher merges)
-  const int32_t* cta_pair0;  // pair holding the first item of each CTA's range
-  float* part_lse;
-  float* part_o;
+  // dense: the requests (every CTA derives the split plan from them)
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_requests;
+  int32_t unit_penalty;
+  int32_t* pair_done;  // [grid] finished chunks of the split pair whose first chunk CTA c holds
+  float* part_lse;     // [2 grid NR]
+  float* part_o;       // [2 grid NR, 512]
   // sparse
   const int32_t* lists;       // [T, list_stride] shard-local slots
   const int32_t* list_count;  // [T]

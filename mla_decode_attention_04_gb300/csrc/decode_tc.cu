@@ -81,6 +81,11 @@ struct TcShared {
   float alpha[32], inv_l[32];
   float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
   float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
+  // dense split plan of this CTA (written once at the start)
+  int64_t plan_lo, plan_hi, plan_W, plan_G, plan_ib;
+  int32_t plan_b;  // request holding the range's first item, -1: no work
+  ReqFacts plan_f;
+  int64_t scan_tmp[16];
 };
 
 // 2^x with the hardware ex2 instruction (flush-to-zero; 2^-inf = 0).
@@ -103,43 +108,52 @@ struct Roles {
 struct Unit {
   int b, row0, nrows, key0, key1, n_kt;
   int q0, q_len, seq_len, local_len;
-  int split, nsplit, pbase;
-  int pair;   // dense: index of the (request, row group) pair
+  int split, nsplit;
+  int cta0;   // dense: CTA holding the pair's first chunk (its counter, its slots)
   int token;  // sparse: the token
 };
 
-// The sequence of units of one CTA.  Dense: the CTA's equal share
-// [c W / G, (c + 1) W / G) of the scheduler's flattened key-tile list, cut at
-// (request, row group) boundaries; the scheduler names the pair holding the
-// range's first item, later units are the following pairs, and the record of
-// the next pair is loaded one unit ahead.  Sparse: (token, head group) units
+// First partial row of chunk k of a split pair whose first chunk CTA cta0
+// holds: chunk 0 is cta0's last unit (its second slot), chunk k > 0 is the
+// first unit of CTA cta0 + k (that CTA's first slot).
+template <int NR>
+__device__ __forceinline__ int64_t chunk_slot(int cta0, int k) {
+  return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k)) * NR;
+}
+
+// The sequence of units of one CTA.  Dense: every (request, row group) pair
+// contributes unit_penalty work-free items (the cost of starting a unit)
+// followed by its 64-key tiles to one flattened list of W items; CTA c takes
+// items [c W / G, (c + 1) W / G), cut at pair boundaries.  The CTA found the
+// request holding its first item at start-up (plan_cta); later requests'
+// facts are loaded one request ahead.  Sparse: (token, head group) units
 // dealt round-robin.  Every role walks the same sequence.
 template <int NR, bool SPARSE>
 struct UnitIter {
-  int64_t i, hi, W, G;
-  int p;         // dense: pair of the next unit
-  PairInfo nxt;  // dense: its record (loaded ahead)
+  int64_t i, hi, W, G, ib;  // dense: next item, range end, plan, item base of request b
+  int b;
+  ReqFacts cur, nxt;
   int u, units;
 
-  __device__ void init(const DecodeArgs& a) {
+  __device__ void init(const DecodeArgs& a, const TcShared& sh) {
     if constexpr (SPARSE) {
       u = blockIdx.x;
       units = a.num_tokens * a.groups_per_token;
     } else {
-      // the scheduler balanced the W items over min(grid, W) non-empty ranges;
-      // this CTA's first pair is read together with W (one memory latency)
-      // and used only if the CTA has a range
-      const int p_first = a.cta_pair0[blockIdx.x];
-      W = a.hdr->total_items;
-      G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
-      if ((int64_t)blockIdx.x < G && W > 0) {
-        i = (int64_t)blockIdx.x * W / G;
-        hi = ((int64_t)blockIdx.x + 1) * W / G;
-        p = p_first;
-        nxt = a.pairs[p];
-      } else {
+      if (sh.plan_b < 0) {
         i = hi = 0;
+        return;
       }
+      i = sh.plan_lo;
+      hi = sh.plan_hi;
+      W = sh.plan_W;
+      G = sh.plan_G;
+      b = sh.plan_b;
+      ib = sh.plan_ib;
+      cur = sh.plan_f;
+      if (b + 1 < a.num_requests)
+        nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
+                            a.dcp_rank, NR);
     }
   }
 
@@ -148,7 +162,7 @@ struct UnitIter {
       for (; u < units; u += gridDim.x) {
         const int t = u / a.groups_per_token, g = u % a.groups_per_token;
         w.token = t;
-        w.pair = -1;
+        w.cta0 = -1;
         w.b = a.tok_req[t];
         w.row0 = g * NR;
         w.nrows = min(NR, a.num_heads - w.row0);
@@ -156,7 +170,6 @@ struct UnitIter {
         w.key1 = a.list_count[t];
         w.split = 0;
         w.nsplit = 1;
-        w.pbase = 0;
         w.q0 = t;
         w.q_len = 1;
         w.seq_len = 0;
@@ -168,35 +181,139 @@ struct UnitIter {
       }
       return false;
     } else {
-      if (i >= hi) return false;
-      while (nxt.nt == 0) nxt = a.pairs[++p];  // pairs without keys own no item
-      const PairInfo pi = nxt;
-      // the range may start among the items that only carry the pair's
-      // start-up cost; a range holding none of its key tiles has no unit
-      if (i < pi.item0) i = pi.item0;
-      if (i >= hi) return false;
-      const int64_t end = min(hi, pi.item0 + pi.nt);
-      w.token = -1;
-      w.pair = p;
-      w.b = pi.b;
-      w.row0 = pi.row0;
-      w.nrows = pi.nrows;
-      w.key0 = (int)(i - pi.item0) * kKeyTile;
-      w.key1 = min((int)(end - pi.item0) * kKeyTile, pi.local_len);
-      w.n_kt = (int)(end - i);
-      w.nsplit = pi.nsplit;
-      w.split = pi.nsplit > 1 ? (int)blockIdx.x - pi.cta0 : 0;  // the unit's items are this CTA's
-      w.pbase = pi.pbase;
-      w.q0 = pi.q0;
-      w.q_len = pi.q_len;
-      w.seq_len = pi.seq_len;
-      w.local_len = pi.local_len;
-      i = end;
-      if (i < hi) nxt = a.pairs[++p];
-      return true;
+      const int64_t pen = a.unit_penalty;
+      while (true) {
+        if (i >= hi) return false;
+        const int64_t vlen = cur.nt > 0 ? (int64_t)cur.nt + pen : 0;
+        const int64_t rend = ib + (int64_t)cur.groups * vlen;  // end of request b's items
+        if (i >= rend) {
+          // request b is done (or owns no item): the next one
+          if (b + 1 >= a.num_requests) {
+            i = hi;
+            return false;
+          }
+          ib = rend;
+          ++b;
+          cur = nxt;
+          if (b + 1 < a.num_requests)
+            nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
+                                a.dcp_rank, NR);
+          continue;
+        }
+        const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
+        const int64_t item0 = ib + (int64_t)g * vlen + pen;
+        // the range may start among the items that only carry the pair's
+        // start-up cost; a range holding none of its key tiles has no unit
+        if (i < item0) i = item0;
+        if (i >= hi) return false;
+        const int64_t end = min(hi, item0 + cur.nt);
+        w.token = -1;
+        w.b = b;
+        w.row0 = g * NR;
+        w.nrows = min(NR, cur.q_len * a.num_heads - g * NR);
+        w.key0 = (int)(i - item0) * kKeyTile;
+        w.key1 = min((int)(end - item0) * kKeyTile, cur.local_len);
+        w.n_kt = (int)(end - i);
+        w.cta0 = (int)range_owner(item0, W, G);
+        w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - w.cta0 + 1);
+        w.split = (int)blockIdx.x - w.cta0;  // the unit's items are this CTA's
+        w.q0 = cur.q0;
+        w.q_len = cur.q_len;
+        w.seq_len = cur.seq_len;
+        w.local_len = cur.local_len;
+        i = end;
+        return true;
+      }
     }
   }
 };
+
+// Dense split plan of this CTA, by all its threads before the roles start:
+// W = the list length (a block-wide sum over the requests), this CTA's range,
+// and the request holding the range's first item (published in sh).
+template <int NR>
+__device__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int B = a.num_requests;
+  const int64_t pen = a.unit_penalty;
+  // exclusive block scan of v; returns the prefix, adds the block total to *tot
+  auto scan = [&](int64_t v, int64_t& tot) -> int64_t {
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.scan_tmp[warp] = x;
+    __syncthreads();
+    int64_t before = 0, all = 0;
+    for (int k = 0; k < nwarps; ++k) {
+      const int64_t t = sh.scan_tmp[k];
+      if (k < warp) before += t;
+      all += t;
+    }
+    __syncthreads();
+    tot += all;
+    return before + x - v;
+  };
+  auto items_of = [&](const ReqFacts& f) -> int64_t {
+    return f.nt > 0 ? (int64_t)f.groups * ((int64_t)f.nt + pen) : 0;
+  };
+  // pass 1: the list length (with one chunk of requests, the facts stay in
+  // registers for pass 2)
+  const bool single = B <= (int)blockDim.x;
+  ReqFacts f1{};
+  int64_t ex1 = 0, W = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + tid;
+    ReqFacts f{};
+    if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
+                                 a.dcp_rank, NR);
+    const int64_t carry = W;
+    const int64_t ex = scan(items_of(f), W) + carry;
+    if (single) {
+      f1 = f;
+      ex1 = ex;
+    }
+  }
+  const int64_t G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
+  const bool has = W > 0 && (int64_t)blockIdx.x < G;
+  const int64_t lo = has ? (int64_t)blockIdx.x * W / G : 0, hi = has ? ((int64_t)blockIdx.x + 1) * W / G : 0;
+  if (tid == 0) {
+    sh.plan_b = -1;
+    sh.plan_lo = lo;
+    sh.plan_hi = hi;
+    sh.plan_W = W;
+    sh.plan_G = G;
+  }
+  __syncthreads();
+  // pass 2: the request whose items contain lo
+  if (has) {
+    int64_t run = 0;
+    for (int base = 0; base < B; base += blockDim.x) {
+      const int b = base + tid;
+      ReqFacts f{};
+      int64_t ex;
+      if (single) {
+        f = f1;
+        ex = ex1;
+      } else {
+        if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
+                                     a.dcp_rank, NR);
+        const int64_t carry = run;
+        ex = scan(items_of(f), run) + carry;
+      }
+      const int64_t n = items_of(f);
+      if (b < B && n > 0 && ex <= lo && lo < ex + n) {
+        sh.plan_b = b;
+        sh.plan_ib = ex;
+        sh.plan_f = f;
+      }
+      if (single) break;
+    }
+  }
+  __syncthreads();
+}
 
 // cache slot (page * page_size + offset) of shard-local key j of request b, or -1
 __device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
@@ -239,7 +356,7 @@ __device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Un
 #pragma unroll
     for (int i = 0; i < NR / 4; ++i) {
       const int n = sw + 4 * i;
-      v[i] = (n < u.nrows && sp < u.nsplit) ? __ldcg(a.part_lse + u.pbase + (int64_t)sp * NR + n) : -INFINITY;
+      v[i] = (n < u.nrows && sp < u.nsplit) ? __ldcg(a.part_lse + chunk_slot<NR>(u.cta0, sp) + n) : -INFINITY;
     }
 #pragma unroll
     for (int i = 0; i < NR / 4; ++i) {
@@ -290,7 +407,7 @@ __device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Un
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const bool use = sp0 + q < u.nsplit && lrow[k] > -INFINITY;
-          const int64_t slot = (int64_t)u.pbase + (int64_t)(sp0 + q) * NR + n0 + k;
+          const int64_t slot = chunk_slot<NR>(u.cta0, sp0 + q) + n0 + k;
           lv[q][k] = use ? __ldcg(a.part_lse + slot) : -INFINITY;
           v[q][k] = use ? __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0))
                         : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -323,9 +440,9 @@ __device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Un
 }
 
 // The same merge once this CTA has no more tiles to stream: the ring's shared
-// memory is idle, so the pair's partials (LSE and o of every chunk, one
-// contiguous run of slots) arrive with one bulk copy instead of several
-// dependent rounds of loads.  Returns false, having done nothing, when they
+// memory is idle, so the pair's partials (LSE and o of every chunk) arrive
+// with one round of bulk copies instead of several dependent rounds of
+// loads.  Returns false, having done nothing, when they
 // do not fit (the caller then merges through registers).
 template <int NR>
 __device__ __forceinline__ bool merge_split_chunks_smem(const DecodeArgs& a, const Unit& u, TcShared& sh, int st_tid,
@@ -338,8 +455,11 @@ __device__ __forceinline__ bool merge_split_chunks_smem(const DecodeArgs& a, con
     __threadfence();
     fence_proxy_async_global();
     mbar_arrive_expect_tx(&sh.merge_full, o_bytes + l_bytes);
-    bulk_load(so, a.part_o + (int64_t)u.pbase * kNope, o_bytes, &sh.merge_full);
-    bulk_load(sl, a.part_lse + u.pbase, l_bytes, &sh.merge_full);
+    for (int sp = 0; sp < u.nsplit; ++sp) {
+      const int64_t slot = chunk_slot<NR>(u.cta0, sp);
+      bulk_load(so + (int64_t)sp * NR * kNope, a.part_o + slot * kNope, NR * kNope * 4, &sh.merge_full);
+      bulk_load(sl + sp * NR, a.part_lse + slot, NR * 4, &sh.merge_full);
+    }
     sh.wait_ok = mbar_wait(&sh.merge_full, merge_phase) ? 1 : 0;
   }
   named_bar_sync(1, 128);
@@ -447,12 +567,19 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     fence_mbar_init();
   }
   if (!SPARSE && threadIdx.x == 32 * R::kMmaWarp) prefetch_tmap(&kv_map);
-  grid_dep_sync();
+  // The dense decode reads only its inputs until its first global write (a
+  // unit's epilogue), so it starts at once, plans its range itself and
+  // streams, and waits for the kernels before it in the stream only there;
+  // the sparse decode reads the lists kernel's output right away.
+  grid_dep_launch();
+  if constexpr (SPARSE) grid_dep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (!SPARSE) plan_cta<NR>(a, sh);
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
+  bool bad_page = false;
 
   if (warp < R::kProducerWarps) {
     // ------------------------------------------------------------ producer
@@ -467,7 +594,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const int ps = a.page_size;
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
       UnitIter<NR, SPARSE> it;
-      it.init(a);
+      it.init(a, sh);
       Unit w;
       int cache_b = -1, cache_col = 0, my_page = -1;
       while (ok && it.next(a, w)) {
@@ -506,7 +633,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             pages[i] = -1;
             if (j < w.local_len) {
               if (page < 0 || page >= a.num_blocks || col >= a.bt_stride) {
-                if (lane == 0) record_check(a.hdr, kCheckPageOutOfRange);
+                bad_page = true;  // recorded at the end, once the status word is this call's
               } else {
                 pages[i] = page;
                 ++nvalid;
@@ -535,7 +662,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       // sparse: 4 warps gather 64 rows x 72 16-byte pieces per tile with cp.async
       const int pt = threadIdx.x;  // 0..127
       UnitIter<NR, SPARSE> it;
-      it.init(a);
+      it.init(a, sh);
       Unit w;
       while (ok && it.next(a, w)) {
         const int32_t* list = a.lists + (int64_t)w.token * a.list_stride;
@@ -578,7 +705,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_pv = idesc_bf16_f32(128, NR, 1, 0);
       UnitIter<NR, SPARSE> it;
-      it.init(a);
+      it.init(a, sh);
       Unit w;
       // Descriptors are linear in the start address (its field is addr >> 4
       // and every address here is below 256 KB), so each operand is a base
@@ -754,14 +881,15 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     // (threadfence-reduction pattern: publish, count, re-fence, read) at its
     // next epilogue, outside the tile loop.
     auto count_chunk = [&](const Unit& u) -> bool {
+      grid_dep_wait();  // the prep kernel zeroed the counters
       __threadfence();
       named_bar_sync(1, 128);
-      if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[u.pair], 1) == u.nsplit - 1;
+      if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[u.cta0], 1) == u.nsplit - 1;
       named_bar_sync(1, 128);
       return sh.is_last != 0;
     };
     UnitIter<NR, SPARSE> it;
-    it.init(a);
+    it.init(a, sh);
     Unit w, wn;
     Unit pend;               // split chunk written but not yet counted
     bool have_pend = false;
@@ -915,6 +1043,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         if (!group_wait(&sh.unit_done, u_ph)) { ok = false; break; }
         u_ph ^= 1;
       }
+      // first global write of this kernel: everything before it in the
+      // stream (the previous call's readers of these outputs) has finished
+      grid_dep_wait();
       sh.lpart[kslice][row] = l_sum;
       named_bar_sync(1, 128);
       if (row_lead) {
@@ -925,7 +1056,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         sh.inv_l[row] = live ? 1.f / lt : 0.f;
         if (row < w.nrows) {
           const float lse = live ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
-          if (partial) a.part_lse[(int64_t)w.pbase + (int64_t)w.split * NR + row] = lse;
+          if (partial) a.part_lse[chunk_slot<NR>(w.cta0, w.split) + row] = lse;
           else a.lse[grow(row)] = lse;
         }
       }
@@ -946,7 +1077,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           if (n >= w.nrows) break;
           const float v = __uint_as_float(o[n]) * sh.inv_l[n];
           if (partial) {
-            const int64_t slot = (int64_t)w.pbase + (int64_t)w.split * NR + n;
+            const int64_t slot = chunk_slot<NR>(w.cta0, w.split) + n;
             a.part_o[slot * kNope + dim] = v;
           } else if (a.out_f32) {
             static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
@@ -975,7 +1106,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     }
   }
 
+  // this kernel completes after the prep kernel, so kernels that wait for it
+  // also see the prep kernel's outputs (rows without keys, per-token counts);
+  // checks are recorded after it reset the status word
+  grid_dep_wait();
   if (!ok) record_check(a.hdr, kCheckWaitTimeout);
+  if (bad_page) record_check(a.hdr, kCheckPageOutOfRange);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -8,7 +8,7 @@
 // workspace; this file gives such callers a variant whose scratch lives in a
 // fixed, file-scope device array instead.
 //
-// The array is MLA_STATIC_SCRATCH_BYTES (16 MiB) per device and lives as long
+// The array is MLA_STATIC_SCRATCH_BYTES (24 MiB) per device and lives as long
 // as the library stays loaded: every GPU that loads the library holds it until
 // the process exits.  All calls share it, so calls that may overlap on the GPU
 // (different streams without ordering between them) race on it; calls issued

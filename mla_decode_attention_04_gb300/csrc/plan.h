@@ -1,4 +1,5 @@
-// plan.h -- host-side split plan, workspace layout and kernel argument blocks.
+// plan.h -- host-side workspace layout of the decode calls and the argument
+// block of the dense prep kernel.
 #pragma once
 
 #include <stddef.h>
@@ -8,36 +9,30 @@
 
 namespace mla {
 
-struct SchedArgs {
+struct PrepArgs {
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
   int32_t num_requests, num_tokens, num_heads, dcp_world, dcp_rank;
   int32_t rows_per_group;
-  int32_t grid;              // CTAs of the decode launch that the items are balanced over
-  int32_t unit_penalty;      // items of balancing cost charged to every pair with keys
-  int32_t max_pairs;
-  int32_t max_partial_rows;
+  int32_t grid;         // decode CTAs (one split counter each)
   WorkspaceHeader* hdr;
-  ReqInfo* req;
-  PairInfo* pairs;
-  int32_t* pair_done;   // per-pair finished-chunk counters, zeroed here
-  int32_t* cta_pair0;   // [grid] pair holding the first item of each decode CTA's range
-  int32_t* tok2req;
+  int32_t* pair_done;   // [grid] finished-chunk counters, zeroed here
   int32_t* row_counts;  // may be NULL
-  // rows of pairs without keys get their final result here (out 0, lse -inf)
+  // rows of requests without local keys get their final result here
   void* out;
   int32_t out_f32;
   float* lse;
 };
 
 // Where everything lives inside a dense-decode workspace (byte offsets).
+// Split partials are addressed by decode CTA: CTA c owns rows
+// [2 c NR, 2 c NR + NR) for the chunk its first unit continues and
+// [(2 c + 1) NR, (2 c + 2) NR) for the chunk its last unit starts.
 struct DecodePlan {
-  int32_t rows_per_group;    // rows (token, head) per work unit: 16 or 32
-  int32_t grid;              // decode CTAs
-  int32_t unit_penalty;      // balancing cost of a unit start, in 64-key tiles
-  int32_t max_pairs;         // capacity of the (request, row group) list
-  int64_t max_partial_rows;  // capacity of the split partials
-  size_t off_req, off_tok, off_pairs, off_cnt, off_cta, off_plse, off_po, total;
+  int32_t rows_per_group;  // rows (token, head) per work unit: 16 or 32
+  int32_t grid;            // decode CTAs
+  int32_t unit_penalty;    // balancing cost of a unit start, in 64-key tiles
+  size_t off_cnt, off_plse, off_po, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -53,7 +48,7 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   const int64_t max_local = (max_seq_len + D - 1) / D;
   const int64_t max_key_tiles = (max_local + kKeyTile - 1) / kKeyTile;
   const int64_t groups_ub = ((int64_t)T * H + NR - 1) / NR + B;  // >= sum_b ceil(q_len_b H / NR)
-  int64_t items_ub = groups_ub * max_key_tiles;
+  const int64_t items_ub = groups_ub * max_key_tiles;
   int64_t g = num_sms > 0 ? num_sms : 148;
   // num_splits > 0 caps the grid at num_splits CTAs per row group; with
   // balanced ranges a row group of average size is then cut into about
@@ -66,23 +61,13 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   if (g > items_ub) g = items_ub;
   if (g < 1) g = 1;
   p.grid = (int32_t)g;
-  p.max_pairs = (int32_t)(groups_ub > 0 ? groups_ub : 1);
-  p.max_partial_rows = (groups_ub + g) * NR;
   size_t off = sizeof(WorkspaceHeader);
-  p.off_req = off;
-  off = align_up(off + sizeof(ReqInfo) * (size_t)(B > 0 ? B : 1), 256);
-  p.off_tok = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)(T > 0 ? T : 1), 256);
-  p.off_pairs = off;
-  off = align_up(off + sizeof(PairInfo) * (size_t)p.max_pairs, 256);
-  p.off_cnt = off;  // per-pair count of finished KV chunks
-  off = align_up(off + sizeof(int32_t) * (size_t)p.max_pairs, 256);
-  p.off_cta = off;  // first pair of each decode CTA's item range
+  p.off_cnt = off;
   off = align_up(off + sizeof(int32_t) * (size_t)p.grid, 256);
   p.off_plse = off;
-  off = align_up(off + sizeof(float) * (size_t)p.max_partial_rows, 256);
+  off = align_up(off + sizeof(float) * 2 * (size_t)p.grid * NR, 256);
   p.off_po = off;
-  off = align_up(off + sizeof(float) * kNope * (size_t)p.max_partial_rows, 256);
+  off = align_up(off + sizeof(float) * kNope * 2 * (size_t)p.grid * NR, 256);
   p.total = off;
   return p;
 }
@@ -103,6 +88,6 @@ inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk) {
   return p;
 }
 
-__global__ void schedule_kernel(SchedArgs a);
+__global__ void prep_kernel(PrepArgs a);
 
 }  // namespace mla
