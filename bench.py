@@ -423,7 +423,7 @@ def run_ours(args):
         "merge_hbm_frac": s["merge_hbm_frac"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_dense_" + HEADLINE),
-                     "kernel": "shard decode call (scheduler + decode with its split-chunk merge) as a CUDA graph, "
+                     "kernel": "shard decode call (prep + decode with its split-chunk merge) as a CUDA graph, "
                                "CUDA events around each replay on the launching stream",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
         "e2e": head["e2e"],

@@ -112,7 +112,15 @@ const char *mla_last_error(void);
  *  num_splits  0 = automatic split-KV plan, else an upper bound on the KV
  *           chunks per request (fix it for CUDA-graph capture).
  *  workspace   device scratch of at least mla_dcp_decode_workspace_size()
- *           bytes, 256-byte aligned; contents need not be initialised.
+ *           bytes, 256-byte aligned; contents need not be initialised.  Its
+ *           size is bounded by the GPU's SM count (two slots of up to 32
+ *           partial rows per SM), not by the batch.
+ *  Stream order: every kernel of this library writes nothing before all
+ *  earlier work on the stream has finished, but this call starts reading its
+ *  inputs (q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_loc)
+ *  while the previous kernel on the stream finishes when that kernel is one
+ *  of this library's.  So these inputs must not be outputs of the
+ *  immediately preceding call of this library on the same stream.
  *  Errors: INVALID_ARG (NULL/misaligned pointers, sizes < 0, dcp_rank not in
  *  [0, dcp_world), num_heads not in [1, 128]), UNSUPPORTED (page size),
  *  WORKSPACE, CUDA.  num_tokens == 0 is a successful no-op.
@@ -195,8 +203,8 @@ int dcp_lse_merge(const void *partials, int32_t partial_dtype, const float *lses
  * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
  * with *detail set to the first failing check's code: 1 = a page id (or its
  * block-table column) out of range, 2 = q_len > seq_len or a bad
- * query_start_loc, 3 = a pipeline wait gave up, 4 = the split plan did not
- * fit the workspace.  This is the one call that blocks the host.
+ * query_start_loc, 3 = a pipeline wait gave up.  This is the one call that
+ * blocks the host.
  * ---------------------------------------------------------------------- */
 int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
 

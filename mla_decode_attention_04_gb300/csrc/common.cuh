@@ -26,7 +26,6 @@ enum DeviceCheck : int32_t {
   kCheckPageOutOfRange = 1,
   kCheckBadQueryLayout = 2,
   kCheckWaitTimeout = 3,
-  kCheckTileOverflow = 4,
 };
 
 // Workspace header, at offset 0 of every decode workspace.
