@@ -59,8 +59,10 @@ def peaks():
 # ------------------------------------------------------------ algorithmic work
 
 
-def work_of(w, partial_bytes=4):
-    """Algorithmic KV bytes, FLOPs and merge bytes of one step of workload w."""
+def work_of(w, partial_bytes=4, fused=False):
+    """Algorithmic KV bytes, FLOPs and merge bytes of one step of workload w
+    (fused: the merge is inside the decode; only the W_UV projection of the
+    one merged fp32 result remains)."""
     L = w.seq_lens.cpu().numpy().astype(np.int64)
     qsl = w.query_start_loc.cpu().numpy().astype(np.int64)
     D, H = w.dcp_world, w.num_heads
@@ -91,7 +93,10 @@ def work_of(w, partial_bytes=4):
         flops = int(used.sum()) * H * FLOPS_PER_KEY_ROW
     T = w.num_tokens
     out_w = 128 if w.w_uv is not None else 512
-    merge_bytes = D * T * H * (512 * partial_bytes + 4) + D * T * 4 + T * H * (out_w * 2 + 4)
+    if fused:
+        merge_bytes = 0 if w.w_uv is None else T * H * (512 * 4 + 4) + T * H * (out_w * 2 + 4)
+    else:
+        merge_bytes = D * T * H * (512 * partial_bytes + 4) + D * T * 4 + T * H * (out_w * 2 + 4)
     if w.w_uv is not None:
         merge_bytes += H * 512 * 128 * 2
     q_bytes = T * H * 576 * 2
@@ -165,13 +170,17 @@ def flush_l2(buf):
     buf.add_(1)
 
 
-def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
+def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True, fused=False):
+    """Time one workload's decode step.  ``fused``: the dense step as one
+    shard-fused decode launch (all D shards, merge built in; + the W_UV
+    projection when the workload has one) instead of D shard calls + the
+    merge call."""
     import mla_decode_attention_04_gb300 as mla
     from mla_decode_attention_04_gb300 import pipeline, workloads as wl
 
     w = wl.NAMED[name](device="cuda")
-    step = pipeline.step_for_workload(w)
-    work = work_of(w, step.partials.element_size())
+    step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
+    work = work_of(w, 4 if fused else step.partials.element_size(), fused=fused)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda") if l2_flush else None
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -184,7 +193,7 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
     # The step runs as a CUDA graph (how a serving engine replays its decode
     # step): the library launches nothing per replay from the host, so the
     # events time the kernels, not the Python launch path.  One graph for the
-    # whole step, and one per shard call and for the merge for the breakdown.
+    # whole step, and one per decode call and for the merge for the breakdown.
     D = w.dcp_world
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -196,15 +205,25 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
     with torch.cuda.graph(g_step):
         step.run()
     launches_per_step = mla.kernel_launch_count() - launches0
-    g_shard = []
-    for r, (cache, bt) in enumerate(step.shards):
+    g_dec, g_merge = [], None
+    if fused:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            step_shard(step, r, cache, bt)
-        g_shard.append(g)
-    g_merge = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_merge):
-        step_merge(step)
+            fused_decode_only(step)
+        g_dec.append(g)
+        if step.w_uv is not None:
+            g_merge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_merge):
+                mla.dcp_lse_merge(step.merged, step.merged_lse, None, step.w_uv, out=step.out, lse_out=step.lse)
+    else:
+        for r, (cache, bt) in enumerate(step.shards):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step_shard(step, r, cache, bt)
+            g_dec.append(g)
+        g_merge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_merge):
+            step_merge(step)
     torch.cuda.synchronize()
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
@@ -216,27 +235,38 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True):
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    # breakdown: each shard call and the merge, each after an L2 flush
-    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * (D + 1))] for _ in range(steps)]
+    # breakdown: each decode call and the merge, each after an L2 flush
+    parts = g_dec + ([g_merge] if g_merge is not None else [])
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(parts))] for _ in range(steps)]
     for k in range(steps):
-        for i, g in enumerate(g_shard + [g_merge]):
+        for i, g in enumerate(parts):
             if flush is not None:
                 flush_l2(flush)
             bev[k][2 * i].record(stream)
             g.replay()
             bev[k][2 * i + 1].record(stream)
     torch.cuda.synchronize()
-    decode_ms = [[e[2 * r].elapsed_time(e[2 * r + 1]) for r in range(D)] for e in bev]
-    merge_ms = [e[2 * D].elapsed_time(e[2 * D + 1]) for e in bev]
+    nd = len(g_dec)
+    decode_ms = [[e[2 * r].elapsed_time(e[2 * r + 1]) for r in range(nd)] for e in bev]
+    merge_ms = [e[2 * nd].elapsed_time(e[2 * nd + 1]) if g_merge is not None else 0.0 for e in bev]
     launches = launches_per_step * steps
     rc, detail = mla.workspace_status(step.workspace)
     if rc != mla.MLA_OK:
         raise RuntimeError(f"device check {detail} in {name} (graph replays)")
     res = dict(name=name, w=w, step=step, work=work, step_ms=step_ms, decode_ms=decode_ms, merge_ms=merge_ms,
-               launches=launches)
+               launches=launches, fused=fused)
     if with_e2e:
         res["e2e"] = time_e2e(w, step, steps, flush)
     return res
+
+
+def fused_decode_only(step):
+    import mla_decode_attention_04_gb300 as mla
+    out = step.merged[0] if step.w_uv is not None else step.out
+    lse = step.merged_lse[0] if step.w_uv is not None else step.lse
+    mla.mla_dcp_decode_fused(step.q_nope, step.q_pe, step.caches, step.tables, step.seq_lens, step.qsl,
+                             step.max_query_len, step.max_seq_len, step.scale, out=out, lse=lse,
+                             num_splits=step.num_splits, workspace=step.workspace)
 
 
 def step_shard(step, r, cache, bt):
@@ -267,7 +297,7 @@ def time_e2e(w, step, steps, flush):
     hsparse = [] if w.topk is None else [w.topk.cpu().pin_memory(), w.topk_valid.cpu().pin_memory()]
     hout = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     dev_meta = [step.seq_lens, step.qsl]
-    dev_tabs = [s[1] for s in step.shards]
+    dev_tabs = list(step.tables) if hasattr(step, "tables") else [s[1] for s in step.shards]
     dev_sparse = [] if w.topk is None else [step.topk, step.topk_valid]
     h2d = sum(t.numel() * t.element_size() for t in [hq_n, hq_p] + hmeta + htabs + hsparse)
     d2h = hout.numel() * hout.element_size()
@@ -310,8 +340,8 @@ def summarize(res, pk):
         roofline_ms=t_roof * 1e3,
         step_roofline_frac=t_roof * 1e3 / step_ms,
         decode_roofline_frac=t_roof * 1e3 / dec_total,
-        merge_gbs=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9,
-        merge_hbm_frac=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+        merge_gbs=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 else None,
+        merge_hbm_frac=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 / pk["hbm_gbs"] if merge_ms > 0 else None,
         kv_bytes=work["kv_bytes"], flops=work["flops"],
     )
 
@@ -373,11 +403,13 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True)
+        head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True, fused=True)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        shards_route = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True)
     clocks = clk.summary()
     s = summarize(head, pk)
+    s_shards = summarize(shards_route, pk)
     step_ms = replica_max_ms(s["ms_per_step"], "cuda")
     tokens = head["work"]["tokens"]
     value = whole_job_value(tokens, world, step_ms)
@@ -387,17 +419,20 @@ def run_ours(args):
         names = [n for n in ("plain_decode_d1", "mtp", "long_context", "sparse_mixed")
                  if args.configs == "all" or n in args.configs.split(",")]
         for n in names:
-            r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)))
-            cs = summarize(r, pk)
-            configs[n] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cs.items()}
-            configs[n]["workload"] = DESCR[n]
-            del r
-            torch.cuda.empty_cache()
+            for fused in ((False, True) if n != "sparse_mixed" else (False,)):
+                r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)), fused=fused)
+                cs = summarize(r, pk)
+                key = n + ("_fused" if fused else "")
+                configs[key] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cs.items()}
+                configs[key]["workload"] = DESCR[n] + ("; one shard-fused decode launch" if fused else
+                                                      "; D shard calls + merge call")
+                del r
+                torch.cuda.empty_cache()
 
-    dec_ms = statistics.mean(statistics.median([d[r] for d in head["decode_ms"]])
-                             for r in range(len(head["decode_ms"][0])))
-    per_launch_bytes = head["work"]["kv_bytes"] / len(head["work"]["kv_bytes_shard"])
-    achieved = per_launch_bytes / (dec_ms * 1e-3) / 1e9
+    # dominant kernel: the shard-fused decode call (prep + one decode launch
+    # over every shard), timed as its own CUDA graph
+    dec_ms = statistics.median(d[0] for d in head["decode_ms"])
+    achieved = head["work"]["kv_bytes"] / (dec_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -412,21 +447,27 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded torch/numpy draws; no dataset)",
         "config": {"workload": DESCR[HEADLINE],
+                   "route": "one shard-fused decode launch over both DCP shards (the online softmax runs over "
+                            "shard 0's keys, then shard 1's: the LSE merge), plus its prep kernel",
                    "l2": "256 MB buffer written before every timed step (KV 302 MB > 129 MB L2 as well)",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "partials": f"{str(head['step'].partials.dtype).replace('torch.', '')} per-shard outputs "
-                               "into the merge (fp32 where W_UV follows)"},
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
         "kv_gbs": s["kv_gbs"],
         "tflops": s["tflops"],
         "step_roofline_frac": s["step_roofline_frac"],
         "decode_roofline_frac": s["decode_roofline_frac"],
         "merge_hbm_frac": s["merge_hbm_frac"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_dense_" + HEADLINE),
-                     "kernel": "shard decode call (prep + decode with its split-chunk merge) as a CUDA graph, "
-                               "CUDA events around each replay on the launching stream",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_fused_" + HEADLINE),
+                     "kernel": "shard-fused decode call (prep + one decode launch over both shards) as a CUDA "
+                               "graph, CUDA events around each replay on the launching stream",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
         "e2e": head["e2e"],
+        "shard_calls_route": {
+            "what": "the same step as D mla_dcp_decode calls + dcp_lse_merge (bf16 partials)",
+            "value": whole_job_value(tokens, world, s_shards["ms_per_step"]), "unit": UNIT,
+            "ms_per_step": s_shards["ms_per_step"], "decode_ms": s_shards["decode_ms"],
+            "merge_ms": s_shards["merge_ms"], "decode_roofline_frac": s_shards["decode_roofline_frac"],
+            "e2e": shards_route["e2e"]},
         "clocks": clocks,
         "gpu_launches": head["launches"],
         "wall_s": wall,

@@ -199,6 +199,45 @@ int dcp_lse_merge(const void *partials, int32_t partial_dtype, const float *lses
                   int32_t out_dtype, float *lse_out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * mla_dcp_decode_fused -- every DCP shard of one decode step in one launch,
+ * with the LSE merge built in, for one GPU that holds all D shard slices.
+ * The pages define the D shard attentions ("[Attention] add DCP support for
+ * FLASH_ATTN_MLA backend", the per-rank mask tables) and their LSE merge
+ * ("[Attention] DCP sparse MLA output-merge optimizations"); a softmax that
+ * continues over shard r's keys after shard r-1's computes exactly that
+ * merge.  Each (request, row group) streams shard 0's visible
+ * keys, then shard 1's, ..., each through its own cache slice, block table
+ * and DCP mask (key j of shard r is seen by the query at position P iff
+ * j*D + r <= P), so the D partial outputs never reach memory.
+ *
+ *  kv_caches    host array of D device pointers, shard r's cache slice
+ *               [num_blocks[r], page_size, 576] bf16 (as mla_dcp_decode's
+ *               kv_cache for rank r).
+ *  num_blocks   host array of D page counts.
+ *  block_tables host array of D device pointers, shard r's block table
+ *               [num_requests, block_table_stride] int32 (shard-local ids).
+ *  dcp_world    D, 1..8.
+ *  out, lse     the merged result: out [num_tokens, num_heads, 512] of
+ *               out_dtype (BF16 or F32), lse float32 [num_tokens, num_heads]
+ *               = log of the sum of exp(scores) over every shard's visible
+ *               keys.  (For the W_UV projection, pass F32 out to
+ *               dcp_lse_merge with dcp_world 1.)
+ *  workspace    device scratch of at least mla_dcp_decode_fused_workspace_size()
+ *               bytes, 256-byte aligned.
+ *  Other arguments, errors and the stream-order rule as mla_dcp_decode.
+ * ---------------------------------------------------------------------- */
+size_t mla_dcp_decode_fused_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                           int32_t max_query_len, int32_t max_seq_len, int32_t num_splits);
+
+int mla_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe, int64_t q_pe_row_stride,
+                         const void *const *kv_caches, const int64_t *num_blocks, int32_t page_size,
+                         int32_t kv_cache_dtype, const int32_t *const *block_tables, int32_t block_table_stride,
+                         const int32_t *seq_lens, const int32_t *query_start_loc, int32_t num_requests,
+                         int32_t num_tokens, int32_t num_heads, int32_t max_query_len, int32_t max_seq_len,
+                         int32_t dcp_world, float scale, void *out, int32_t out_dtype, float *lse,
+                         int32_t num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * mla_workspace_status -- synchronises `stream`, then reads the status word
  * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
  * with *detail set to the first failing check's code: 1 = a page id (or its

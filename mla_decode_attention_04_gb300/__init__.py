@@ -31,7 +31,7 @@ MLA_DTYPE_BF16, MLA_DTYPE_F32, MLA_DTYPE_FP8_E4M3 = 0, 1, 2
 EXPORTS = [
     "mla_last_error", "mla_dcp_decode_workspace_size", "mla_dcp_decode", "mla_sparse_dcp_decode_workspace_size",
     "mla_sparse_dcp_decode", "dcp_lse_merge", "mla_workspace_status", "mla_kernel_launch_count",
-    "mla_dcp_decode_static_scratch",
+    "mla_dcp_decode_static_scratch", "mla_dcp_decode_fused_workspace_size", "mla_dcp_decode_fused",
 ]
 
 # Size of the library's fixed device scratch array used by
@@ -69,6 +69,11 @@ def _bind(lib):
     lib.mla_workspace_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.mla_kernel_launch_count.restype = i64
     lib.mla_kernel_launch_count.argtypes = []
+    lib.mla_dcp_decode_fused_workspace_size.restype = sz
+    lib.mla_dcp_decode_fused_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.mla_dcp_decode_fused.restype = ctypes.c_int
+    lib.mla_dcp_decode_fused.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                         i32, i32, ctypes.c_float, vp, i32, vp, i32, vp, sz, vp]
     lib.mla_dcp_decode_static_scratch.restype = ctypes.c_int
     lib.mla_dcp_decode_static_scratch.argtypes = [vp, i64, vp, i64, vp, i64, i32, i32, vp, i32, vp, vp, i32, i32, i32,
                                                   i32, i32, i32, i32, f32, vp, i32, vp, vp, i32, vp]
@@ -160,6 +165,55 @@ def mla_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_lo
                               _ptr(out), _DT[out.dtype], _ptr(lse), _ptr(row_counts), int(num_splits),
                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse, row_counts
+
+
+def fused_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, num_splits=0) -> int:
+    return int(load_library().mla_dcp_decode_fused_workspace_size(num_requests, num_tokens, num_heads, max_query_len,
+                                                                   max_seq_len, num_splits))
+
+
+def mla_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_start_loc, max_query_len,
+                         max_seq_len, scale, out=None, lse=None, out_dtype=torch.bfloat16, num_splits=0,
+                         workspace=None, stream=None):
+    """All D DCP shards of a decode step in one launch: the shard caches and
+    block tables (lists of D tensors) are read in turn by one online softmax,
+    which is the LSE merge over the shards.  Returns the merged (out
+    [T,H,512], lse [T,H])."""
+    lib = load_library()
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    D = len(kv_caches)
+    if len(block_tables) != D or D < 1:
+        raise ValueError("kv_caches and block_tables need one entry per shard")
+    sn, sp = _row_stride(q_nope, KV_LORA_RANK, "q_nope"), _row_stride(q_pe, ROPE_DIM, "q_pe")
+    kv_args = [_kv_args(c) for c in kv_caches]
+    ps, kv_dt = kv_args[0][1], kv_args[0][2]
+    if any(a[1] != ps or a[2] != kv_dt for a in kv_args):
+        raise ValueError("all shard caches need the same page size and dtype")
+    bt_stride = block_tables[0].shape[1]
+    for bt in block_tables:
+        _i32(bt, "block_table")
+        if bt.shape[1] != bt_stride:
+            raise ValueError("all block tables need the same row stride")
+    _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc")
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, KV_LORA_RANK), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    need = fused_workspace_size(B, T, H, max_query_len, max_seq_len, num_splits)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
+    nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
+    bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    _check(lib.mla_dcp_decode_fused(_ptr(q_nope), sn, _ptr(q_pe), sp, ctypes.cast(kv_ptrs, ctypes.c_void_p),
+                                    ctypes.cast(nbs, ctypes.c_void_p), ps, kv_dt,
+                                    ctypes.cast(bt_ptrs, ctypes.c_void_p), bt_stride, _ptr(seq_lens),
+                                    _ptr(query_start_loc), B, T, H, int(max_query_len), int(max_seq_len), D,
+                                    float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), int(num_splits),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
 
 
 def mla_sparse_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_loc, topk_indices, topk_valid,

@@ -112,23 +112,24 @@ size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, i
       .total;
 }
 
-int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
-                   const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
-                   const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
-                   const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
-                   int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
-                   void* out, int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits,
-                   void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
-                               kv_cache_dtype, block_table, block_table_stride, seq_lens, query_start_loc,
-                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
-                               workspace);
-  if (rc != MLA_OK) return rc;
+}  // extern "C"
+
+namespace {
+
+// The dense decode over nshard consecutive shards from rank shard0 (one
+// shard: mla_dcp_decode; all D: mla_dcp_decode_fused).  Arguments checked.
+int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                 int nshard, int shard0, const void* const* kv_caches, const int64_t* num_blocks, int32_t page_size,
+                 const int32_t* const* block_tables, int32_t block_table_stride, const int32_t* seq_lens,
+                 const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                 int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, float scale, void* out,
+                 int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits, void* workspace,
+                 size_t workspace_bytes, void* stream) {
   if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
     return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
   if (num_tokens == 0) return ok();
   const mla::DecodePlan plan = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len,
-                                                     dcp_world, num_splits, current_sm_count());
+                                                     dcp_world / nshard, num_splits, current_sm_count());
   if (workspace_bytes < plan.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -143,7 +144,8 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   pa.num_tokens = num_tokens;
   pa.num_heads = num_heads;
   pa.dcp_world = dcp_world;
-  pa.dcp_rank = dcp_rank;
+  pa.shard0 = shard0;
+  pa.nshard = nshard;
   pa.rows_per_group = plan.rows_per_group;
   pa.grid = plan.grid;
   pa.hdr = hdr;
@@ -166,14 +168,21 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   da.q_nope_stride = q_nope_row_stride;
   da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   da.q_pe_stride = q_pe_row_stride;
-  da.kv = static_cast<const __nv_bfloat16*>(kv_cache);
-  da.num_blocks = num_blocks;
+  da.kv = static_cast<const __nv_bfloat16*>(kv_caches[0]);
+  da.num_blocks = num_blocks[0];
   da.page_size = page_size;
-  da.block_table = block_table;
+  da.block_table = block_tables[0];
   da.bt_stride = block_table_stride;
+  da.nshard = nshard;
+  da.shard0 = shard0;
+  for (int k = 0; k < nshard; ++k) {
+    da.kvs[k] = static_cast<const __nv_bfloat16*>(kv_caches[k]);
+    da.bts[k] = block_tables[k];
+    da.nblocks[k] = num_blocks[k];
+  }
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;
-  da.dcp_rank = dcp_rank;
+  da.dcp_rank = shard0;
   da.scale = scale;
   da.out = out;
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
@@ -190,8 +199,63 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
   if ((e = mla::launch_decode_tc(da, plan.rows_per_group, false, plan.grid, plan.grid, st)) != cudaSuccess)
     return cuda_fail(e, "decode launch");
   count_launch();
-
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                   const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                   const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                   int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
+                   void* out, int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
+                               kv_cache_dtype, block_table, block_table_stride, seq_lens, query_start_loc,
+                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                               workspace);
+  if (rc != MLA_OK) return rc;
+  const void* kvs[1] = {kv_cache};
+  const int64_t nbs[1] = {num_blocks};
+  const int32_t* bts[1] = {block_table};
+  return dense_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, 1, dcp_rank, kvs, nbs, page_size, bts,
+                      block_table_stride, seq_lens, query_start_loc, num_requests, num_tokens, num_heads,
+                      max_query_len, max_seq_len, dcp_world, scale, out, out_dtype, lse, row_counts, num_splits,
+                      workspace, workspace_bytes, stream);
+}
+
+size_t mla_dcp_decode_fused_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                           int32_t max_query_len, int32_t max_seq_len, int32_t num_splits) {
+  return mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, 1, num_splits,
+                               current_sm_count())
+      .total;
+}
+
+int mla_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                         const void* const* kv_caches, const int64_t* num_blocks, int32_t page_size,
+                         int32_t kv_cache_dtype, const int32_t* const* block_tables, int32_t block_table_stride,
+                         const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_requests,
+                         int32_t num_tokens, int32_t num_heads, int32_t max_query_len, int32_t max_seq_len,
+                         int32_t dcp_world, float scale, void* out, int32_t out_dtype, float* lse, int32_t num_splits,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (dcp_world < 1 || dcp_world > mla::kMaxShards)
+    return fail(MLA_ERR_INVALID_ARG, "dcp_world %d not in [1, %d] for the fused call", dcp_world, mla::kMaxShards);
+  if (kv_caches == nullptr || num_blocks == nullptr || block_tables == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "kv_caches / num_blocks / block_tables arrays are NULL");
+  for (int r = 0; r < dcp_world; ++r) {
+    int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_caches[r], num_blocks[r],
+                                 page_size, kv_cache_dtype, block_tables[r], block_table_stride, seq_lens,
+                                 query_start_loc, num_requests, num_tokens, num_heads, dcp_world, r, scale, out,
+                                 out_dtype, lse, workspace);
+    if (rc != MLA_OK) return rc;
+  }
+  return dense_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, dcp_world, 0, kv_caches, num_blocks,
+                      page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests,
+                      num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, scale, out, out_dtype, lse,
+                      nullptr, num_splits, workspace, workspace_bytes, stream);
 }
 
 size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t dcp_world) {
@@ -251,6 +315,11 @@ int mla_sparse_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const v
   da.num_blocks = num_blocks;
   da.page_size = page_size;
   da.block_table = block_table;
+  da.nshard = 1;
+  da.shard0 = dcp_rank;
+  da.kvs[0] = static_cast<const __nv_bfloat16*>(kv_cache);
+  da.bts[0] = block_table;
+  da.nblocks[0] = num_blocks;
   da.bt_stride = block_table_stride;
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;

@@ -52,27 +52,62 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int32_t P, int32_t D, i
   return P >= r ? (P - r) / D + 1 : 0;
 }
 
+// Most DCP shards one dense call can cover (the shard-fused entry point).
+constexpr int kMaxShards = 8;
+
 // What the dense decode needs to know about request b, from seq_lens and
 // query_start_loc alone (the prep kernel and every decode CTA derive it the
-// same way).  A malformed query range (ok false) is treated as q_len 0.
+// same way).  A call covers nshard consecutive shards from rank shard0 (one
+// shard, or all D when fused); nt is the request's key tiles over all of
+// them, each shard's local keys padded to whole tiles.  A malformed query
+// range (ok false) is treated as q_len 0.
 struct ReqFacts {
-  int32_t q0, q_len, seq_len, local_len, groups, nt;
+  int32_t q0, q_len, seq_len, local_len, groups, nt;  // local_len: on shard0
   bool ok;
 };
 
 __device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const int32_t* query_start_loc, int b,
-                                                  int num_tokens, int H, int D, int r, int NR) {
+                                                  int num_tokens, int H, int D, int shard0, int nshard, int NR) {
   ReqFacts f;
   const int q0 = query_start_loc[b], q1 = query_start_loc[b + 1], L = seq_lens[b];
   f.ok = !(q1 - q0 < 0 || q1 - q0 > L || q0 < 0 || q1 > num_tokens);
   f.q0 = q0 < 0 ? 0 : q0;
   f.q_len = f.ok ? q1 - q0 : 0;
   f.seq_len = L;
-  f.local_len = local_len(L, D, r);
+  f.local_len = local_len(L, D, shard0);
   f.groups = (f.q_len * H + NR - 1) / NR;
-  f.nt = (f.local_len + kKeyTile - 1) / kKeyTile;
+  f.nt = 0;
+  for (int k = 0; k < nshard; ++k) f.nt += (local_len(L, D, shard0 + k) + kKeyTile - 1) / kKeyTile;
   return f;
 }
+
+// Walks a request's key-tile sequence (shard k's local keys as whole tiles,
+// k = 0 .. nshard-1 in turn) in increasing tile order: for tile t it names
+// the shard index k within the call, the shard's tiles [t_begin, t_end) and
+// the request's local length Lr on that shard.  A unit's tiles are visited
+// in order, so moving on costs nothing until a shard boundary.
+struct ShardCursor {
+  int32_t k, t_begin, t_end, Lr;
+
+  __device__ __forceinline__ void start(int L, int D, int shard0) {
+    k = 0;
+    t_begin = 0;
+    Lr = local_len(L, D, shard0);
+    t_end = (Lr + kKeyTile - 1) / kKeyTile;
+  }
+  // moves to the shard holding tile t (t >= t_begin); true if it moved
+  __device__ __forceinline__ bool seek(int t, int L, int D, int shard0, int nshard) {
+    bool moved = false;
+    while (t >= t_end && k + 1 < nshard) {
+      ++k;
+      t_begin = t_end;
+      Lr = local_len(L, D, shard0 + k);
+      t_end += (Lr + kKeyTile - 1) / kKeyTile;
+      moved = true;
+    }
+    return moved;
+  }
+};
 
 // floor(t / W) for t >= 0, W > 0: a float estimate of the quotient corrected
 // with exact integer products (64-bit division is a long dependent sequence).

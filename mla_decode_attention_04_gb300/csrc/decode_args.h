@@ -10,11 +10,17 @@ struct DecodeArgs {
   int64_t q_nope_stride;  // elements between consecutive (token, head) rows
   const __nv_bfloat16* q_pe;
   int64_t q_pe_stride;
-  const __nv_bfloat16* kv;  // [num_blocks, page_size, 576]
+  const __nv_bfloat16* kv;  // [num_blocks, page_size, 576] (sparse; dense: shard 0 of the call)
   int64_t num_blocks;
   int32_t page_size;
-  const int32_t* block_table;
+  const int32_t* block_table;  // (sparse; dense: shard 0 of the call)
   int32_t bt_stride;
+  // dense: the call covers shards shard0 .. shard0 + nshard - 1 (one shard,
+  // or all D when fused); shard k's cache pages and block table
+  int32_t nshard, shard0;
+  const __nv_bfloat16* kvs[kMaxShards];
+  const int32_t* bts[kMaxShards];
+  int64_t nblocks[kMaxShards];
   int32_t num_heads, dcp_world, dcp_rank;
   float scale;
   void* out;  // [T, H, 512]

@@ -30,6 +30,8 @@
 // tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM.  The
 // online softmax rescales O^T lazily: the running
 // reference max only moves when a tile's max exceeds it by more than 2^8.
+#include <string.h>
+
 #include "common.cuh"
 #include "decode_args.h"
 #include "decode_kernels.h"
@@ -107,6 +109,7 @@ struct Roles {
 // Work unit description, identical for every role.
 struct Unit {
   int b, row0, nrows, key0, key1, n_kt;
+  int t0;     // dense: first tile of the unit in the request's tile sequence
   int q0, q_len, seq_len, local_len;
   int split, nsplit;
   int cta0;   // dense: CTA holding the pair's first chunk (its counter, its slots)
@@ -153,7 +156,7 @@ struct UnitIter {
       cur = sh.plan_f;
       if (b + 1 < a.num_requests)
         nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
-                            a.dcp_rank, NR);
+                            a.shard0, a.nshard, NR);
     }
   }
 
@@ -197,7 +200,7 @@ struct UnitIter {
           cur = nxt;
           if (b + 1 < a.num_requests)
             nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
-                                a.dcp_rank, NR);
+                                a.shard0, a.nshard, NR);
           continue;
         }
         const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
@@ -211,8 +214,9 @@ struct UnitIter {
         w.b = b;
         w.row0 = g * NR;
         w.nrows = min(NR, cur.q_len * a.num_heads - g * NR);
-        w.key0 = (int)(i - item0) * kKeyTile;
-        w.key1 = min((int)(end - item0) * kKeyTile, cur.local_len);
+        w.t0 = (int)(i - item0);
+        w.key0 = w.t0 * kKeyTile;
+        w.key1 = (int)(end - item0) * kKeyTile;
         w.n_kt = (int)(end - i);
         w.cta0 = (int)range_owner(item0, W, G);
         w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - w.cta0 + 1);
@@ -268,7 +272,7 @@ __device__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
     const int b = base + tid;
     ReqFacts f{};
     if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
-                                 a.dcp_rank, NR);
+                                 a.shard0, a.nshard, NR);
     const int64_t carry = W;
     const int64_t ex = scan(items_of(f), W) + carry;
     if (single) {
@@ -299,7 +303,7 @@ __device__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
         ex = ex1;
       } else {
         if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
-                                     a.dcp_rank, NR);
+                                     a.shard0, a.nshard, NR);
         const int64_t carry = run;
         ex = scan(items_of(f), run) + carry;
       }
@@ -530,9 +534,34 @@ __device__ __forceinline__ bool merge_split_chunks_smem(const DecodeArgs& a, con
   return true;
 }
 
+// A tile of a request's sequence: shard index k within the call, tile lt of
+// that shard's local keys, the request's local length Lr on that shard.
+struct TileLoc {
+  int32_t k, lt, Lr;
+};
+
+// The dense call's cache tensor maps, one per shard it covers.
+struct KvMaps {
+  CUtensorMap m[kMaxShards];
+};
+
+// Address of shard k's map in the kernel's parameter space (static indices).
+__device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int k) {
+  switch (k) {
+    case 0: return &maps.m[0];
+    case 1: return &maps.m[1];
+    case 2: return &maps.m[2];
+    case 3: return &maps.m[3];
+    case 4: return &maps.m[4];
+    case 5: return &maps.m[5];
+    case 6: return &maps.m[6];
+    default: return &maps.m[7];
+  }
+}
+
 template <int NR, bool SPARSE>
 __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap kv_map, DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ KvMaps maps, DecodeArgs a) {
   using R = Roles<SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -566,7 +595,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     sh.any_rescale[0] = sh.any_rescale[1] = 0;
     fence_mbar_init();
   }
-  if (!SPARSE && threadIdx.x == 32 * R::kMmaWarp) prefetch_tmap(&kv_map);
+  if (!SPARSE && warp == R::kMmaWarp && lane < a.nshard) prefetch_tmap(kv_map_of(maps, lane));
   // The dense decode reads only its inputs until its first global write (a
   // unit's epilogue), so it starts at once, plans its range itself and
   // streams, and waits for the kernels before it in the stream only there;
@@ -596,7 +625,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       UnitIter<NR, SPARSE> it;
       it.init(a, sh);
       Unit w;
-      int cache_b = -1, cache_col = 0, my_page = -1;
+      int cache_b = -1, cache_k = -1, cache_col = 0, my_page = -1;
       while (ok && it.next(a, w)) {
         if (w.n_kt > 0) {
           // the unit's Q rows: one slot of the ring, a bulk copy per row half
@@ -614,25 +643,33 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        ShardCursor cur_sh;
+        cur_sh.start(w.seq_len, a.dcp_world, a.shard0);
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-          const int k = w.key0 + kt * kKeyTile;
+          // tile t of the request's sequence: a tile of shard cur_sh.k's local keys
+          cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, a.nshard);
+          const TileLoc loc{cur_sh.k, w.t0 + kt - cur_sh.t_begin, cur_sh.Lr};
+          const int k = loc.lt * kKeyTile;
+          const int32_t* bt = a.bts[loc.k];
+          const int64_t nblk = a.nblocks[loc.k];
           int pages[kKeyTile / 8];
           int nvalid = 0;
 #pragma unroll 1
           for (int i = 0; i < nsub; ++i) {
             const int j = k + i * ps;  // first key of this page's part of the tile
             const int col = j / ps;
-            if (w.b != cache_b || col < cache_col || col >= cache_col + 32) {
+            if (w.b != cache_b || loc.k != cache_k || col < cache_col || col >= cache_col + 32) {
               cache_b = w.b;
+              cache_k = loc.k;
               cache_col = col;
               const int c2 = col + lane;
-              const int last_col = (w.local_len - 1) / ps;
-              my_page = (c2 <= last_col && c2 < a.bt_stride) ? a.block_table[(int64_t)w.b * a.bt_stride + c2] : -1;
+              const int last_col = (loc.Lr - 1) / ps;
+              my_page = (c2 <= last_col && c2 < a.bt_stride) ? bt[(int64_t)w.b * a.bt_stride + c2] : -1;
             }
             const int page = __shfl_sync(0xffffffffu, my_page, col - cache_col);
             pages[i] = -1;
-            if (j < w.local_len) {
-              if (page < 0 || page >= a.num_blocks || col >= a.bt_stride) {
+            if (j < loc.Lr) {
+              if (page < 0 || page >= nblk || col >= a.bt_stride) {
                 bad_page = true;  // recorded at the end, once the status word is this call's
               } else {
                 pages[i] = page;
@@ -648,10 +685,11 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
               const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
               mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)nvalid * rows * 128u * 9u);
               const int off = ps >= kKeyTile ? k % ps : 0;
+              const CUtensorMap* map = kv_map_of(maps, loc.k);
               for (int i = 0; i < nsub; ++i)
                 if (pages[i] >= 0)
                   for (int c = 0; c < 9; ++c)
-                    tma_load_3d(dst + c * kChunk + i * ps * 128, &kv_map, c * 64, off, pages[i], &sh.full[stage], pol);
+                    tma_load_3d(dst + c * kChunk + i * ps * 128, map, c * 64, off, pages[i], &sh.full[stage], pol);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -903,15 +941,18 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       more = it.next(a, wn);
       auto grow = [&](int n) -> int64_t { return grow_of(w, n); };
       const bool partial = !SPARSE && w.nsplit > 1;
-      int kend = w.key0;  // keys [key0, kend) visible to this thread's row
-      if (row < w.nrows) {
-        if constexpr (SPARSE) {
-          kend = w.key1;
-        } else {
-          const int i = (w.row0 + row) / H;
-          const int P = w.seq_len - w.q_len + i;
-          kend = min(visible_keys(P, a.dcp_world, a.dcp_rank), w.key1);
-        }
+      // sparse: keys [0, kend) of the row's list; dense: the row's global
+      // position P and the keys it sees on the current tile's shard (lim),
+      // updated when the unit's tiles move to the next shard
+      int kend = 0, P_row = -1, lim = 0;
+      ShardCursor cur_sh;
+      if constexpr (SPARSE) {
+        if (row < w.nrows) kend = w.key1;
+      } else {
+        if (row < w.nrows) P_row = w.seq_len - w.q_len + (w.row0 + row) / H;
+        cur_sh.start(w.seq_len, a.dcp_world, a.shard0);
+        cur_sh.seek(w.t0, w.seq_len, a.dcp_world, a.shard0, a.nshard);
+        lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
       }
       float m_ref = -INFINITY, l_sum = 0.f;
 
@@ -929,8 +970,18 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             for (int e = 0; e < KPT; ++e) s[e] = __uint_as_float(v[e]);
           }
         }
-        const int kbase = w.key0 + kt * kKeyTile;
-        const int valid = max(0, min(kend - kbase, kKeyTile));
+        int valid, tile_valid;  // keys of the tile this row sees / that exist
+        if constexpr (SPARSE) {
+          const int kbase = kt * kKeyTile;
+          valid = max(0, min(kend - kbase, kKeyTile));
+          tile_valid = min(w.key1 - kbase, kKeyTile);
+        } else {
+          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, a.nshard))
+            lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
+          const int kbase = (w.t0 + kt - cur_sh.t_begin) * kKeyTile;
+          valid = max(0, min(lim - kbase, kKeyTile));
+          tile_valid = min(cur_sh.Lr - kbase, kKeyTile);
+        }
         float pmax = -INFINITY;
 #pragma unroll
         for (int e = 0; e < KPT; ++e) {
@@ -987,7 +1038,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
         // value rows of keys past the chunk end: zero them (P is 0 there, and
         // 0 * (garbage) must not reach the accumulator)
-        const int tile_valid = min(w.key1 - kbase, kKeyTile);
         if (tile_valid < kKeyTile) {
           uint8_t* st = kv + stage * kStageBytes;
           const int nz = (kKeyTile - tile_valid) * 64;  // 16-byte pieces over 8 value chunks
@@ -1119,12 +1169,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 }
 
 template <int NR, bool SPARSE>
-cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cudaStream_t stream) {
+cudaError_t launch_tc(const DecodeArgs& a, const KvMaps& maps, int grid, cudaStream_t stream) {
   const size_t smem = 1024 + kStages * kStageBytes + sizeof(TcShared);
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<NR, SPARSE>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream, map, a);
+  return launch_pdl(decode_tc_kernel<NR, SPARSE>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream, maps, a);
 }
 
 }  // namespace
@@ -1132,12 +1182,15 @@ cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap& map, int grid, cud
 cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool sparse, int max_units, int num_sms,
                              cudaStream_t stream) {
   if (max_units <= 0) return cudaSuccess;
-  CUtensorMap map;
-  if (!make_kv_tensor_map(&map, a.kv, a.num_blocks, a.page_size)) return cudaErrorInvalidValue;
+  if (a.nshard < 1 || a.nshard > kMaxShards) return cudaErrorInvalidValue;
+  KvMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int k = 0; k < a.nshard; ++k)
+    if (!make_kv_tensor_map(&maps.m[k], a.kvs[k], a.nblocks[k], a.page_size)) return cudaErrorInvalidValue;
   const int grid = max_units < num_sms ? max_units : num_sms;
   if (sparse)
-    return rows_per_group == 16 ? launch_tc<16, true>(a, map, grid, stream) : launch_tc<32, true>(a, map, grid, stream);
-  return rows_per_group == 16 ? launch_tc<16, false>(a, map, grid, stream) : launch_tc<32, false>(a, map, grid, stream);
+    return rows_per_group == 16 ? launch_tc<16, true>(a, maps, grid, stream) : launch_tc<32, true>(a, maps, grid, stream);
+  return rows_per_group == 16 ? launch_tc<16, false>(a, maps, grid, stream) : launch_tc<32, false>(a, maps, grid, stream);
 }
 
 }  // namespace mla

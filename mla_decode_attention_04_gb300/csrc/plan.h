@@ -12,7 +12,8 @@ namespace mla {
 struct PrepArgs {
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
-  int32_t num_requests, num_tokens, num_heads, dcp_world, dcp_rank;
+  int32_t num_requests, num_tokens, num_heads, dcp_world;
+  int32_t shard0, nshard;  // the shards the decode covers (one, or all D when fused)
   int32_t rows_per_group;
   int32_t grid;         // decode CTAs (one split counter each)
   WorkspaceHeader* hdr;

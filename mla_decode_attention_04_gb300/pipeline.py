@@ -11,8 +11,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (KV_LORA_RANK, V_HEAD_DIM, decode_workspace_size, dcp_lse_merge, mla_dcp_decode, mla_sparse_dcp_decode,
-               sparse_workspace_size)
+from . import (KV_LORA_RANK, V_HEAD_DIM, decode_workspace_size, dcp_lse_merge, fused_workspace_size, mla_dcp_decode,
+               mla_dcp_decode_fused, mla_sparse_dcp_decode, sparse_workspace_size)
 
 
 class DcpStep:
@@ -67,6 +67,56 @@ class DcpStep:
         dcp_lse_merge(self.partials, self.lses, self.counts if self.use_counts else None, self.w_uv, out=self.out,
                       lse_out=self.lse, stream=stream)
         return self.out, self.lse
+
+
+class FusedDcpStep:
+    """The dense step in one decode launch over all D shards
+    (``mla_dcp_decode_fused``: the online softmax runs over shard 0's keys,
+    then shard 1's, ..., which is the LSE merge), followed, with W_UV, by the
+    projection (``dcp_lse_merge`` of the one merged result).  Same outputs as
+    ``DcpStep`` (``out``, ``lse``); no per-shard partials or counts."""
+
+    def __init__(self, q_nope, q_pe, shards, seq_lens, query_start_loc, max_query_len, max_seq_len, scale, w_uv=None,
+                 out_dtype=torch.bfloat16, num_splits=0):
+        self.q_nope, self.q_pe = q_nope, q_pe
+        self.caches = [c for c, _ in shards]
+        self.tables = [bt for _, bt in shards]
+        self.seq_lens, self.qsl = seq_lens, query_start_loc
+        self.max_query_len, self.max_seq_len, self.scale = int(max_query_len), int(max_seq_len), float(scale)
+        self.w_uv, self.num_splits = w_uv, num_splits
+        T, H = q_nope.shape[0], q_nope.shape[1]
+        dev = q_nope.device
+        self.D, self.T, self.H = len(shards), T, H
+        width = V_HEAD_DIM if w_uv is not None else KV_LORA_RANK
+        self.out = torch.empty((T, H, width), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+        # with W_UV the merged 512-wide output stays fp32 until the projection
+        self.merged = (torch.empty((1, T, H, KV_LORA_RANK), dtype=torch.float32, device=dev)
+                       if w_uv is not None else None)
+        self.merged_lse = torch.empty((1, T, H), dtype=torch.float32, device=dev) if w_uv is not None else None
+        need = fused_workspace_size(seq_lens.shape[0], T, H, max_query_len, max_seq_len, num_splits)
+        self.workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None):
+        if self.w_uv is None:
+            mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
+                                 self.max_query_len, self.max_seq_len, self.scale, out=self.out, lse=self.lse,
+                                 num_splits=self.num_splits, workspace=self.workspace, stream=stream)
+        else:
+            mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
+                                 self.max_query_len, self.max_seq_len, self.scale, out=self.merged[0],
+                                 lse=self.merged_lse[0], num_splits=self.num_splits, workspace=self.workspace,
+                                 stream=stream)
+            dcp_lse_merge(self.merged, self.merged_lse, None, self.w_uv, out=self.out, lse_out=self.lse,
+                          stream=stream)
+        return self.out, self.lse
+
+
+def fused_step_for_workload(w, num_splits=0):
+    """FusedDcpStep for a dense ``workloads.Workload`` already on the GPU."""
+    shards = [(s.cache, s.block_table) for s in w.shards]
+    return FusedDcpStep(w.q_nope, w.q_pe, shards, w.seq_lens, w.query_start_loc, w.max_query_len, w.max_seq_len,
+                        w.scale, w_uv=w.w_uv, num_splits=num_splits)
 
 
 def step_for_workload(w, partial_dtype=None, num_splits=0, sparse=None):

@@ -1,0 +1,94 @@
+"""GPU parity of the shard-fused dense decode (mla_dcp_decode_fused): one
+launch over all D shards whose online softmax runs over every shard's
+visible keys, checked against the oracle's D shard attentions merged by LSE
+(and, with W_UV, projected), element by element."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import mla_decode_attention_04_gb300 as mla
+from mla_decode_attention_04_gb300 import build as mla_build
+from mla_decode_attention_04_gb300 import pipeline, workloads as wl
+from parity_utils import HostInputs, assert_lse_close, assert_out_close, oracle_step, oracle_step_threaded, to_np
+from test_gpu_parity import EDGE, _sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mla_build.build()
+    mla.load_library()
+
+
+def _fused(w, out_dtype=torch.float32, num_splits=0):
+    out, lse = mla.mla_dcp_decode_fused(w.q_nope, w.q_pe, [s.cache for s in w.shards],
+                                        [s.block_table for s in w.shards], w.seq_lens, w.query_start_loc,
+                                        w.max_query_len, w.max_seq_len, w.scale, out_dtype=out_dtype,
+                                        num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_tiny_fused(out_dtype, num_splits):
+    w = wl.tiny().to("cuda")
+    out, lse = _fused(w, out_dtype, num_splits)
+    ref = oracle_step(HostInputs(w))
+    assert_out_close(to_np(out), ref["merged"], "fused merged output")
+    assert_lse_close(to_np(lse), ref["lse"], "fused merged lse")
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_fused_edge_shapes(name):
+    w = wl.custom(seed=sorted(EDGE).index(name), **EDGE[name]).to("cuda")
+    out, lse = _fused(w)
+    ref = oracle_step(HostInputs(w))
+    assert_out_close(to_np(out), ref["merged"], f"{name} fused output")
+    assert_lse_close(to_np(lse), ref["lse"], f"{name} fused lse")
+
+
+def test_tiny_fused_step_with_wuv():
+    w = wl.tiny().to("cuda")
+    step = pipeline.fused_step_for_workload(w)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    ref = oracle_step(HostInputs(w))
+    assert_out_close(to_np(out), ref["out"], "fused step W_UV output")
+    assert_lse_close(to_np(lse), ref["lse"], "fused step lse")
+
+
+def test_fused_needs_one_cache_and_table_per_shard():
+    w = wl.tiny().to("cuda")
+    with pytest.raises(ValueError):
+        mla.mla_dcp_decode_fused(w.q_nope, w.q_pe, [w.shards[0].cache], [], w.seq_lens, w.query_start_loc,
+                                 w.max_query_len, w.max_seq_len, w.scale)
+
+
+@pytest.mark.parametrize("name", ["plain_decode_d1", "plain_decode_d2", "mtp", "long_context"])
+def test_fused_benchmark_workload_sampled(name):
+    w = wl.NAMED[name](device="cuda")
+    step = pipeline.fused_step_for_workload(w)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    rc, detail = mla.workspace_status(step.workspace)
+    assert rc == mla.MLA_OK, detail
+    tokens = _sample_tokens(w)
+    ref = oracle_step_threaded(HostInputs(w), tokens)
+    assert_out_close(to_np(out[tokens]), ref["out"], f"{name} fused step")
+    assert_lse_close(to_np(lse[tokens]), ref["lse"], f"{name} fused lse")
+
+
+def test_fused_matches_shard_calls_on_every_token():
+    # the two routes on the GPU agree everywhere (the oracle checks samples)
+    w = wl.NAMED["plain_decode_d2"](device="cuda")
+    fused_out, fused_lse = pipeline.fused_step_for_workload(w).run()
+    step = pipeline.step_for_workload(w, partial_dtype=torch.float32)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    assert_out_close(to_np(fused_out), to_np(out).astype(np.float64), "fused vs shard calls")
+    assert_lse_close(to_np(fused_lse), to_np(lse).astype(np.float64), "fused vs shard calls lse")
