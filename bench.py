@@ -108,7 +108,11 @@ def work_of(w, partial_bytes=4, fused=False):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples every 100 ms; the summary keeps
+    the samples taken inside the window marked around the timed region
+    (which the bench pads with a sustained run of the same replays, so that
+    the window holds several samples under load)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -116,6 +120,7 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.window = None
 
     def __enter__(self):
         try:
@@ -123,12 +128,15 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
+
+    def mark(self, start, end):
+        self.window = (start, end)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -140,27 +148,35 @@ class ClockSampler:
             self.fh.close()
 
     def summary(self):
+        import datetime
         if not self.path or not os.path.exists(self.path):
             return None
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, outside = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 p = [x.strip() for x in line.split(",")]
-                if len(p) < 9:
+                if len(p) < 10:
                     continue
                 try:
-                    sm.append(float(p[1]))
-                    mx.append(float(p[2]))
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, cmax = float(p[2]), float(p[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, p[5:9]):
+                if self.window and not (self.window[0] <= ts <= self.window[1]):
+                    outside += 1
+                    continue
+                sm.append(clk)
+                mx.append(cmax)
+                for n, v in zip(names, p[6:10]):
                     if v.lower() == "active":
                         reasons.add(n)
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm), "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "window_s": round(self.window[1] - self.window[0], 3) if self.window else None,
+                "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ our arm
@@ -170,7 +186,7 @@ def flush_l2(buf):
     buf.add_(1)
 
 
-def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True, fused=False):
+def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True, fused=False, clock=None, sustain_s=1.5):
     """Time one workload's decode step.  ``fused``: the dense step as one
     shard-fused decode launch (all D shards, merge built in; + the W_UV
     projection when the workload has one) instead of D shard calls + the
@@ -226,6 +242,16 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True, fused=Fals
             step_merge(step)
     torch.cuda.synchronize()
 
+    if clock is not None:
+        # the clock window: a sustained run of the same replays (untimed),
+        # then the K timed steps right after it
+        t_start = time.time()
+        while time.time() - t_start < sustain_s:
+            for _ in range(20):
+                if flush is not None:
+                    flush_l2(flush)
+                g_step.replay()
+            torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     for k in range(steps):
         if flush is not None:
@@ -234,6 +260,8 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=True, fused=Fals
         g_step.replay()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
+    if clock is not None:
+        clock.mark(t_start, time.time())
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     # breakdown: each decode call and the merge, each after an L2 flush
     parts = g_dec + ([g_merge] if g_merge is not None else [])
@@ -403,7 +431,7 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True, fused=True)
+        head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True, fused=True, clock=clk)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         shards_route = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True)

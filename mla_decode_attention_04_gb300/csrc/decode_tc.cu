@@ -545,6 +545,21 @@ struct KvMaps {
   CUtensorMap m[kMaxShards];
 };
 
+// Element k of a per-shard kernel-parameter array, read with a static index.
+template <typename T>
+__device__ __forceinline__ T pick_shard(const T (&arr)[kMaxShards], int k) {
+  switch (k) {
+    case 0: return arr[0];
+    case 1: return arr[1];
+    case 2: return arr[2];
+    case 3: return arr[3];
+    case 4: return arr[4];
+    case 5: return arr[5];
+    case 6: return arr[6];
+    default: return arr[7];
+  }
+}
+
 // Address of shard k's map in the kernel's parameter space (static indices).
 __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int k) {
   switch (k) {
@@ -559,7 +574,7 @@ __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int 
   }
 }
 
-template <int NR, bool SPARSE>
+template <int NR, bool SPARSE, bool FUSED>
 __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ KvMaps maps, DecodeArgs a) {
   using R = Roles<SPARSE>;
@@ -573,6 +588,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   // outputs get bf16 P, already finer than the output rounding
   const bool p_split = a.out_f32 != 0;
   constexpr int SB = TmemPlan<NR>::kSBufs;
+  // shards this launch covers: the one-shard instance knows it is one at
+  // compile time, so its shard walk folds away
+  const int nshard = FUSED ? a.nshard : 1;
 
   if (warp == R::kMmaWarp) {
     tmem_alloc(&sh.tmem_base, 512);
@@ -595,7 +613,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     sh.any_rescale[0] = sh.any_rescale[1] = 0;
     fence_mbar_init();
   }
-  if (!SPARSE && warp == R::kMmaWarp && lane < a.nshard) prefetch_tmap(kv_map_of(maps, lane));
+  if (!SPARSE && warp == R::kMmaWarp && lane < nshard) prefetch_tmap(kv_map_of(maps, lane));
   // The dense decode reads only its inputs until its first global write (a
   // unit's epilogue), so it starts at once, plans its range itself and
   // streams, and waits for the kernels before it in the stream only there;
@@ -645,13 +663,21 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
         ShardCursor cur_sh;
         cur_sh.start(w.seq_len, a.dcp_world, a.shard0);
+        cur_sh.seek(w.t0, w.seq_len, a.dcp_world, a.shard0, nshard);
+        // the current shard's block table, page count and tensor map, picked
+        // with static indices when the unit's tiles move to another shard
+        const int32_t* bt = pick_shard(a.bts, cur_sh.k);
+        int64_t nblk = pick_shard(a.nblocks, cur_sh.k);
+        const CUtensorMap* map = kv_map_of(maps, cur_sh.k);
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
           // tile t of the request's sequence: a tile of shard cur_sh.k's local keys
-          cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, a.nshard);
+          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, nshard)) {
+            bt = pick_shard(a.bts, cur_sh.k);
+            nblk = pick_shard(a.nblocks, cur_sh.k);
+            map = kv_map_of(maps, cur_sh.k);
+          }
           const TileLoc loc{cur_sh.k, w.t0 + kt - cur_sh.t_begin, cur_sh.Lr};
           const int k = loc.lt * kKeyTile;
-          const int32_t* bt = a.bts[loc.k];
-          const int64_t nblk = a.nblocks[loc.k];
           int pages[kKeyTile / 8];
           int nvalid = 0;
 #pragma unroll 1
@@ -685,7 +711,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
               const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
               mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)nvalid * rows * 128u * 9u);
               const int off = ps >= kKeyTile ? k % ps : 0;
-              const CUtensorMap* map = kv_map_of(maps, loc.k);
               for (int i = 0; i < nsub; ++i)
                 if (pages[i] >= 0)
                   for (int c = 0; c < 9; ++c)
@@ -951,7 +976,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       } else {
         if (row < w.nrows) P_row = w.seq_len - w.q_len + (w.row0 + row) / H;
         cur_sh.start(w.seq_len, a.dcp_world, a.shard0);
-        cur_sh.seek(w.t0, w.seq_len, a.dcp_world, a.shard0, a.nshard);
+        cur_sh.seek(w.t0, w.seq_len, a.dcp_world, a.shard0, nshard);
         lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
       }
       float m_ref = -INFINITY, l_sum = 0.f;
@@ -976,7 +1001,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           valid = max(0, min(kend - kbase, kKeyTile));
           tile_valid = min(w.key1 - kbase, kKeyTile);
         } else {
-          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, a.nshard))
+          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, nshard))
             lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
           const int kbase = (w.t0 + kt - cur_sh.t_begin) * kKeyTile;
           valid = max(0, min(lim - kbase, kKeyTile));
@@ -1168,13 +1193,14 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   if (warp == R::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int NR, bool SPARSE>
+template <int NR, bool SPARSE, bool FUSED>
 cudaError_t launch_tc(const DecodeArgs& a, const KvMaps& maps, int grid, cudaStream_t stream) {
   const size_t smem = 1024 + kStages * kStageBytes + sizeof(TcShared);
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE, FUSED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<NR, SPARSE>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream, maps, a);
+  return launch_pdl(decode_tc_kernel<NR, SPARSE, FUSED>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream,
+                    maps, a);
 }
 
 }  // namespace
@@ -1182,15 +1208,18 @@ cudaError_t launch_tc(const DecodeArgs& a, const KvMaps& maps, int grid, cudaStr
 cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool sparse, int max_units, int num_sms,
                              cudaStream_t stream) {
   if (max_units <= 0) return cudaSuccess;
-  if (a.nshard < 1 || a.nshard > kMaxShards) return cudaErrorInvalidValue;
+  if (a.nshard < 1 || a.nshard > kMaxShards || (sparse && a.nshard != 1)) return cudaErrorInvalidValue;
   KvMaps maps;
   memset(&maps, 0, sizeof(maps));
   for (int k = 0; k < a.nshard; ++k)
     if (!make_kv_tensor_map(&maps.m[k], a.kvs[k], a.nblocks[k], a.page_size)) return cudaErrorInvalidValue;
   const int grid = max_units < num_sms ? max_units : num_sms;
+  const bool nr16 = rows_per_group == 16;
   if (sparse)
-    return rows_per_group == 16 ? launch_tc<16, true>(a, maps, grid, stream) : launch_tc<32, true>(a, maps, grid, stream);
-  return rows_per_group == 16 ? launch_tc<16, false>(a, maps, grid, stream) : launch_tc<32, false>(a, maps, grid, stream);
+    return nr16 ? launch_tc<16, true, false>(a, maps, grid, stream) : launch_tc<32, true, false>(a, maps, grid, stream);
+  if (a.nshard > 1)
+    return nr16 ? launch_tc<16, false, true>(a, maps, grid, stream) : launch_tc<32, false, true>(a, maps, grid, stream);
+  return nr16 ? launch_tc<16, false, false>(a, maps, grid, stream) : launch_tc<32, false, false>(a, maps, grid, stream);
 }
 
 }  // namespace mla
