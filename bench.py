@@ -585,16 +585,17 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_profile_case(name, repeat):
+def run_profile_case(name, repeat, route="fused"):
     """Run the step of one benchmark workload ``repeat`` times, untimed: the
     command the ncu summaries under profiles/ are captured from."""
     from mla_decode_attention_04_gb300 import pipeline, workloads as wl
     w = wl.NAMED[name](device="cuda")
-    step = pipeline.step_for_workload(w)
+    fused = route == "fused" and w.topk is None
+    step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
     for _ in range(repeat):
         step.run()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": name, "repeat": repeat}), flush=True)
+    print(json.dumps({"profile_case": name, "repeat": repeat, "route": "fused" if fused else "shards"}), flush=True)
 
 
 def main():
@@ -606,9 +607,11 @@ def main():
     ap.add_argument("--configs", default="all", help="all | headline | comma list of workload names")
     ap.add_argument("--profile-case", default=None, help="run one workload's step untimed (for ncu), print no bench line")
     ap.add_argument("--repeat", type=int, default=3, help="steps of --profile-case")
+    ap.add_argument("--route", default="fused", choices=["fused", "shards"],
+                    help="--profile-case: one shard-fused decode launch, or D shard calls + merge")
     args = ap.parse_args()
     if args.profile_case:
-        run_profile_case(args.profile_case, args.repeat)
+        run_profile_case(args.profile_case, args.repeat, args.route)
         return
     if args.warmup < 3:
         args.warmup = 3
