@@ -121,9 +121,12 @@ const char *mla_last_error(void);
  *  while the previous kernel on the stream finishes when that kernel is one
  *  of this library's.  So these inputs must not be outputs of the
  *  immediately preceding call of this library on the same stream.
+ *  Launches: three kernels on `stream` (prep, decode, and the LSE merge of
+ *  the KV chunks of row groups the decode split over several CTAs).
  *  Errors: INVALID_ARG (NULL/misaligned pointers, sizes < 0, dcp_rank not in
- *  [0, dcp_world), num_heads not in [1, 128]), UNSUPPORTED (page size),
- *  WORKSPACE, CUDA.  num_tokens == 0 is a successful no-op.
+ *  [0, dcp_world), num_heads not in [1, 128], num_tokens * num_heads >=
+ *  2^31), UNSUPPORTED (page size), WORKSPACE, CUDA.  num_tokens == 0 is a
+ *  successful no-op.
  * ---------------------------------------------------------------------- */
 size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                                      int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
@@ -242,7 +245,8 @@ int mla_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, const vo
  * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
  * with *detail set to the first failing check's code: 1 = a page id (or its
  * block-table column) out of range, 2 = q_len > seq_len or a bad
- * query_start_loc, 3 = a pipeline wait gave up.  This is the one call that
+ * query_start_loc, 3 = a pipeline wait gave up, 4 = a split-table entry
+ * out of range (an internal inconsistency).  This is the one call that
  * blocks the host.
  * ---------------------------------------------------------------------- */
 int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);

@@ -128,6 +128,9 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
     return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
   if (num_tokens == 0) return ok();
+  if ((int64_t)num_tokens * num_heads > 0x7fffffff)
+    return fail(MLA_ERR_INVALID_ARG, "num_tokens * num_heads = %lld exceeds 2^31 - 1",
+                (long long)num_tokens * num_heads);
   const mla::DecodePlan plan = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len,
                                                      dcp_world / nshard, num_splits, current_sm_count());
   if (workspace_bytes < plan.total)
@@ -147,16 +150,13 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   pa.shard0 = shard0;
   pa.nshard = nshard;
   pa.rows_per_group = plan.rows_per_group;
-  pa.grid = plan.grid;
   pa.hdr = hdr;
-  pa.pair_done = reinterpret_cast<int32_t*>(ws + plan.off_cnt);
   pa.row_counts = row_counts;
   pa.out = out;
   pa.out_f32 = out_dtype == MLA_DTYPE_F32;
   pa.lse = lse;
   {
-    const int work = num_requests > plan.grid ? num_requests : plan.grid;
-    int blocks = (work + 255) / 256;
+    int blocks = (num_requests + 255) / 256;
     if (blocks > 64) blocks = 64;
     if ((e = mla::launch_pdl(mla::prep_kernel, dim3(blocks), dim3(256), 0, st, pa)) != cudaSuccess)
       return cuda_fail(e, "prep_kernel launch");
@@ -192,12 +192,28 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.query_start_loc = query_start_loc;
   da.num_requests = num_requests;
   da.unit_penalty = plan.unit_penalty;
-  da.pair_done = pa.pair_done;
+  da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
   da.num_tokens = num_tokens;
   if ((e = mla::launch_decode_tc(da, plan.rows_per_group, false, plan.grid, plan.grid, st)) != cudaSuccess)
     return cuda_fail(e, "decode launch");
+  count_launch();
+
+  mla::SplitMergeArgs sa{};
+  sa.split_desc = da.split_desc;
+  sa.part_lse = da.part_lse;
+  sa.part_o = da.part_o;
+  sa.rows_per_group = plan.rows_per_group;
+  sa.grid = plan.grid;
+  sa.num_rows = (int64_t)num_tokens * num_heads;
+  sa.out = out;
+  sa.out_f32 = da.out_f32;
+  sa.lse = lse;
+  sa.hdr = hdr;
+  const int sm_blocks = plan.grid * (plan.rows_per_group / mla::kSplitMergeRows);
+  if ((e = mla::launch_pdl(mla::split_merge_kernel, dim3(sm_blocks), dim3(128), 0, st, sa)) != cudaSuccess)
+    return cuda_fail(e, "split_merge_kernel launch");
   count_launch();
   return ok();
 }

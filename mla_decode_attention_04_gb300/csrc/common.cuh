@@ -26,6 +26,7 @@ enum DeviceCheck : int32_t {
   kCheckPageOutOfRange = 1,
   kCheckBadQueryLayout = 2,
   kCheckWaitTimeout = 3,
+  kCheckBadSplitEntry = 4,  // a split-table entry out of range (internal consistency)
 };
 
 // Workspace header, at offset 0 of every decode workspace.
@@ -50,6 +51,13 @@ __host__ __device__ __forceinline__ int32_t local_len(int32_t L, int32_t D, int3
 // j with j*D + r <= P.
 __host__ __device__ __forceinline__ int32_t visible_keys(int32_t P, int32_t D, int32_t r) {
   return P >= r ? (P - r) / D + 1 : 0;
+}
+
+// First partial row of chunk k of a split row group whose first chunk decode
+// CTA cta0 holds: chunk 0 is cta0's last unit (its second slot), chunk k > 0
+// is the first unit of CTA cta0 + k (that CTA's first slot).  NR rows each.
+__host__ __device__ __forceinline__ int64_t chunk_slot(int cta0, int k, int NR) {
+  return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k)) * NR;
 }
 
 // Most DCP shards one dense call can cover (the shard-fused entry point).

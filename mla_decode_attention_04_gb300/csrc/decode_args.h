@@ -32,9 +32,9 @@ struct DecodeArgs {
   const int32_t* query_start_loc;
   int32_t num_requests;
   int32_t unit_penalty;
-  int32_t* pair_done;  // [grid] finished chunks of the split pair whose first chunk CTA c holds
-  float* part_lse;     // [2 grid NR]
-  float* part_o;       // [2 grid NR, 512]
+  int4* split_desc;  // [grid] the split pair whose first chunk CTA c holds (SplitDesc layout)
+  float* part_lse;   // [2 grid NR]
+  float* part_o;     // [2 grid NR, 512]
   // sparse
   const int32_t* lists;       // [T, list_stride] shard-local slots
   const int32_t* list_count;  // [T]

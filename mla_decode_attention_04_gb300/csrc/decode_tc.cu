@@ -25,8 +25,9 @@
 // Warp roles: producer (TMA tile loads through the block table; for sparse,
 // 4 warps of 16-byte cp.async row gathers), the QK^T warp (also owns TMEM),
 // four softmax warps (one per TMEM lane quarter) that also rescale O^T, zero
-// the value rows of keys past the chunk end, write the outputs and merge
-// split chunks, and the PV warp.  A 3-stage shared-memory ring of 64-key
+// the value rows of keys past the chunk end and write the outputs (a chunk
+// of a split row group as a normalised partial with its LSE, merged by the
+// split-merge kernel that runs after this one), and the PV warp.  A 3-stage shared-memory ring of 64-key
 // tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM.  The
 // online softmax rescales O^T lazily: the running
 // reference max only moves when a tile's max exceeds it by more than 2^8.
@@ -75,11 +76,9 @@ struct TcShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
-  uint64_t merge_full;  // bulk loads of a split pair's partials (end-of-CTA merges)
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
-  int32_t is_last;  // this CTA finished the last KV chunk of its pair
   float alpha[32], inv_l[32];
   float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
   float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
@@ -115,14 +114,6 @@ struct Unit {
   int cta0;   // dense: CTA holding the pair's first chunk (its counter, its slots)
   int token;  // sparse: the token
 };
-
-// First partial row of chunk k of a split pair whose first chunk CTA cta0
-// holds: chunk 0 is cta0's last unit (its second slot), chunk k > 0 is the
-// first unit of CTA cta0 + k (that CTA's first slot).
-template <int NR>
-__device__ __forceinline__ int64_t chunk_slot(int cta0, int k) {
-  return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k)) * NR;
-}
 
 // The sequence of units of one CTA.  Dense: every (request, row group) pair
 // contributes unit_penalty work-free items (the cost of starting a unit)
@@ -234,86 +225,71 @@ struct UnitIter {
 
 // Dense split plan of this CTA, by all its threads before the roles start:
 // W = the list length (a block-wide sum over the requests), this CTA's range,
-// and the request holding the range's first item (published in sh).
+// and the request holding the range's first item (published in sh).  Kept
+// to one copy of the scan: the kernel's first instructions are fetched cold
+// while they run, so start-up code is kept short.
 template <int NR>
-__device__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
+__device__ __noinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int B = a.num_requests;
   const int64_t pen = a.unit_penalty;
-  // exclusive block scan of v; returns the prefix, adds the block total to *tot
-  auto scan = [&](int64_t v, int64_t& tot) -> int64_t {
-    int64_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) sh.scan_tmp[warp] = x;
-    __syncthreads();
-    int64_t before = 0, all = 0;
-    for (int k = 0; k < nwarps; ++k) {
-      const int64_t t = sh.scan_tmp[k];
-      if (k < warp) before += t;
-      all += t;
-    }
-    __syncthreads();
-    tot += all;
-    return before + x - v;
-  };
-  auto items_of = [&](const ReqFacts& f) -> int64_t {
-    return f.nt > 0 ? (int64_t)f.groups * ((int64_t)f.nt + pen) : 0;
-  };
-  // pass 1: the list length (with one chunk of requests, the facts stay in
-  // registers for pass 2)
-  const bool single = B <= (int)blockDim.x;
+  const bool single = B <= (int)blockDim.x;  // one chunk of requests: pass 0's facts stay in registers
   ReqFacts f1{};
-  int64_t ex1 = 0, W = 0;
-  for (int base = 0; base < B; base += blockDim.x) {
-    const int b = base + tid;
-    ReqFacts f{};
-    if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
-                                 a.shard0, a.nshard, NR);
-    const int64_t carry = W;
-    const int64_t ex = scan(items_of(f), W) + carry;
-    if (single) {
-      f1 = f;
-      ex1 = ex;
-    }
-  }
-  const int64_t G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
-  const bool has = W > 0 && (int64_t)blockIdx.x < G;
-  const int64_t lo = has ? (int64_t)blockIdx.x * W / G : 0, hi = has ? ((int64_t)blockIdx.x + 1) * W / G : 0;
-  if (tid == 0) {
-    sh.plan_b = -1;
-    sh.plan_lo = lo;
-    sh.plan_hi = hi;
-    sh.plan_W = W;
-    sh.plan_G = G;
-  }
-  __syncthreads();
-  // pass 2: the request whose items contain lo
-  if (has) {
+  int64_t ex1 = 0, lo = 0;
+  // pass 0: the list length W and this CTA's range; pass 1: the request
+  // whose items contain the range's first item lo
+  for (int pass = 0; pass < 2; ++pass) {
     int64_t run = 0;
     for (int base = 0; base < B; base += blockDim.x) {
       const int b = base + tid;
-      ReqFacts f{};
-      int64_t ex;
-      if (single) {
-        f = f1;
-        ex = ex1;
-      } else {
-        if (b < B) f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world,
-                                     a.shard0, a.nshard, NR);
-        const int64_t carry = run;
-        ex = scan(items_of(f), run) + carry;
+      if (pass == 0 || !single) {
+        f1 = ReqFacts{};
+        if (b < B)
+          f1 = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world, a.shard0,
+                             a.nshard, NR);
+        // exclusive block scan of the requests' item counts
+        const int64_t v = f1.nt > 0 ? (int64_t)f1.groups * ((int64_t)f1.nt + pen) : 0;
+        int64_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (lane == 31) sh.scan_tmp[warp] = x;
+        __syncthreads();
+        int64_t before = 0, all = 0;
+        for (int k = 0; k < nwarps; ++k) {
+          const int64_t t = sh.scan_tmp[k];
+          if (k < warp) before += t;
+          all += t;
+        }
+        __syncthreads();
+        ex1 = run + before + x - v;
+        run += all;
       }
-      const int64_t n = items_of(f);
-      if (b < B && n > 0 && ex <= lo && lo < ex + n) {
-        sh.plan_b = b;
-        sh.plan_ib = ex;
-        sh.plan_f = f;
+      if (pass == 1) {
+        const int64_t n = f1.nt > 0 ? (int64_t)f1.groups * ((int64_t)f1.nt + pen) : 0;
+        if (b < B && n > 0 && ex1 <= lo && lo < ex1 + n) {
+          sh.plan_b = b;
+          sh.plan_ib = ex1;
+          sh.plan_f = f1;
+        }
       }
-      if (single) break;
+    }
+    if (pass == 0) {
+      const int64_t W = run;
+      const int64_t G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
+      const bool has = W > 0 && (int64_t)blockIdx.x < G;
+      lo = has ? quot_floor((int64_t)blockIdx.x * W, G) : 0;
+      if (tid == 0) {
+        sh.plan_b = -1;
+        sh.plan_lo = lo;
+        sh.plan_hi = has ? quot_floor(((int64_t)blockIdx.x + 1) * W, G) : 0;
+        sh.plan_W = W;
+        sh.plan_G = G;
+      }
+      __syncthreads();
+      if (!has) break;
     }
   }
   __syncthreads();
@@ -328,210 +304,21 @@ __device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
   return (int64_t)page * a.page_size + j % a.page_size;
 }
 
-// The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T, with
-// the accumulate flags and the P split fixed at compile time so that the
-// issue sequence has no run-time branches.
-template <int NR, bool FIRST, bool SPLIT>
-__device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p0, uint32_t id_pv) {
-#pragma unroll
+// The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T.  The
+// first tile of a unit overwrites O^T; the P split (hi + lo, for fp32
+// outputs) doubles the MMAs.  One rolled copy: the issue rate of a thread,
+// not the loop, bounds it.
+template <int NR>
+__device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p0, uint32_t id_pv, bool first,
+                                              bool split) {
+#pragma unroll 1
   for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-      mma_ss(o0 + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, (FIRST && kk == 0) ? 0u : 1u);
-      if (SPLIT) mma_ss(o0 + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+      mma_ss(o0 + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, (first && kk == 0) ? 0u : 1u);
+      if (split) mma_ss(o0 + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
     }
-}
-
-// Merge of a split pair's chunks by LSE, run by the 128 softmax threads of the
-// CTA that finished the pair's last chunk (dense units only).
-template <int NR>
-__device__ __forceinline__ void merge_split_chunks(const DecodeArgs& a, const Unit& u, TcShared& sh, int st_tid) {
-  const int lane = st_tid & 31, sw = st_tid >> 5;
-  __threadfence();
-  // (1) each row's LSE over the chunks: warp sw owns rows sw, sw+4, ...,
-  // its lanes stride over the chunks (all loads of a pass in flight)
-  float mx[NR / 4], z[NR / 4];
-#pragma unroll
-  for (int i = 0; i < NR / 4; ++i) mx[i] = -INFINITY, z[i] = 0.f;
-  for (int sp0 = 0; sp0 < u.nsplit; sp0 += 32) {
-    const int sp = sp0 + lane;
-    float v[NR / 4];
-#pragma unroll
-    for (int i = 0; i < NR / 4; ++i) {
-      const int n = sw + 4 * i;
-      v[i] = (n < u.nrows && sp < u.nsplit) ? __ldcg(a.part_lse + chunk_slot<NR>(u.cta0, sp) + n) : -INFINITY;
-    }
-#pragma unroll
-    for (int i = 0; i < NR / 4; ++i) {
-      if (v[i] > mx[i]) {
-        z[i] = z[i] * fast_exp2((mx[i] - v[i]) * kLog2e) + 1.f;
-        mx[i] = v[i];
-      } else if (v[i] > -INFINITY) {
-        z[i] += fast_exp2((v[i] - mx[i]) * kLog2e);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < NR / 4; ++i) {
-    float gm = mx[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
-    float zz = mx[i] > -INFINITY ? z[i] * fast_exp2((mx[i] - gm) * kLog2e) : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
-    const int n = sw + 4 * i;
-    if (lane == 0 && n < u.nrows) {
-      const float lse = gm > -INFINITY ? gm + __logf(zz) : -INFINITY;
-      sh.alpha[n] = lse;
-      a.lse[((int64_t)u.q0 * a.num_heads + u.row0 + n)] = lse;
-    }
-  }
-  named_bar_sync(1, 128);
-  // (2) weighted sum of the chunks: thread st_tid owns latent dims
-  // [4 st_tid, 4 st_tid + 4) of 8 rows at a time, kPass chunks per pass
-  // (all 2 * 8 * kPass loads of a pass in flight)
-  constexpr int kPass = 2;
-  const int d0 = st_tid * 4;
-#pragma unroll 1
-  for (int n0 = 0; n0 < u.nrows; n0 += 8) {
-    float4 acc[8];
-    float lrow[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      lrow[k] = n0 + k < u.nrows ? sh.alpha[n0 + k] : -INFINITY;
-    }
-#pragma unroll 1
-    for (int sp0 = 0; sp0 < u.nsplit; sp0 += kPass) {
-      float lv[kPass][8];
-      float4 v[kPass][8];
-#pragma unroll
-      for (int q = 0; q < kPass; ++q)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const bool use = sp0 + q < u.nsplit && lrow[k] > -INFINITY;
-          const int64_t slot = chunk_slot<NR>(u.cta0, sp0 + q) + n0 + k;
-          lv[q][k] = use ? __ldcg(a.part_lse + slot) : -INFINITY;
-          v[q][k] = use ? __ldcg(reinterpret_cast<const float4*>(a.part_o + slot * kNope + d0))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-      for (int q = 0; q < kPass; ++q)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float wgt = lv[q][k] > -INFINITY ? fast_exp2((lv[q][k] - lrow[k]) * kLog2e) : 0.f;
-          acc[k].x += wgt * v[q][k].x;
-          acc[k].y += wgt * v[q][k].y;
-          acc[k].z += wgt * v[q][k].z;
-          acc[k].w += wgt * v[q][k].w;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (n0 + k >= u.nrows) break;
-      const int64_t g = ((int64_t)u.q0 * a.num_heads + u.row0 + n0 + k);
-      if (a.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
-      } else {
-        const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-        const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
-      }
-    }
-  }
-}
-
-// The same merge once this CTA has no more tiles to stream: the ring's shared
-// memory is idle, so the pair's partials (LSE and o of every chunk) arrive
-// with one round of bulk copies instead of several dependent rounds of
-// loads.  Returns false, having done nothing, when they
-// do not fit (the caller then merges through registers).
-template <int NR>
-__device__ __forceinline__ bool merge_split_chunks_smem(const DecodeArgs& a, const Unit& u, TcShared& sh, int st_tid,
-                                                        uint8_t* ring, uint32_t& merge_phase, bool& ok) {
-  const uint32_t o_bytes = (uint32_t)u.nsplit * NR * kNope * 4, l_bytes = (uint32_t)u.nsplit * NR * 4;
-  if (o_bytes + l_bytes > (uint32_t)(kStages * kStageBytes)) return false;
-  float* so = reinterpret_cast<float*>(ring);              // [nsplit * NR][512]
-  float* sl = reinterpret_cast<float*>(ring + o_bytes);    // [nsplit * NR]
-  if (st_tid == 0) {
-    __threadfence();
-    fence_proxy_async_global();
-    mbar_arrive_expect_tx(&sh.merge_full, o_bytes + l_bytes);
-    for (int sp = 0; sp < u.nsplit; ++sp) {
-      const int64_t slot = chunk_slot<NR>(u.cta0, sp);
-      bulk_load(so + (int64_t)sp * NR * kNope, a.part_o + slot * kNope, NR * kNope * 4, &sh.merge_full);
-      bulk_load(sl + sp * NR, a.part_lse + slot, NR * 4, &sh.merge_full);
-    }
-    sh.wait_ok = mbar_wait(&sh.merge_full, merge_phase) ? 1 : 0;
-  }
-  named_bar_sync(1, 128);
-  if (!sh.wait_ok) {
-    ok = false;
-    merge_phase ^= 1;
-    return true;
-  }
-  // every reader observes the completed phase itself (returns at once)
-  if (st_tid != 0) mbar_wait(&sh.merge_full, merge_phase);
-  merge_phase ^= 1;
-  // (1) each row's LSE over the chunks (thread n < nrows)
-  if (st_tid < u.nrows) {
-    const int n = st_tid;
-    float m = -INFINITY;
-    for (int sp = 0; sp < u.nsplit; ++sp) m = fmaxf(m, sl[sp * NR + n]);
-    float lse = -INFINITY;
-    if (m > -INFINITY) {
-      float z = 0.f;
-      for (int sp = 0; sp < u.nsplit; ++sp) z += fast_exp2((sl[sp * NR + n] - m) * kLog2e);
-      lse = m + __logf(z);
-    }
-    sh.alpha[n] = lse;
-    a.lse[(int64_t)u.q0 * a.num_heads + u.row0 + n] = lse;
-  }
-  named_bar_sync(1, 128);
-  // (2) weighted sum: thread st_tid owns latent dims [4 st_tid, 4 st_tid + 4)
-  // of 8 rows at a time (independent chains, so their latencies overlap)
-  const int d0 = st_tid * 4;
-#pragma unroll 1
-  for (int n0 = 0; n0 < u.nrows; n0 += 8) {
-    float4 acc[8];
-    float lrow[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      lrow[k] = n0 + k < u.nrows ? sh.alpha[n0 + k] : -INFINITY;
-    }
-#pragma unroll 1
-    for (int sp = 0; sp < u.nsplit; ++sp) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float lv = n0 + k < u.nrows ? sl[sp * NR + n0 + k] : -INFINITY;
-        if (lrow[k] > -INFINITY && lv > -INFINITY) {
-          const float wgt = fast_exp2((lv - lrow[k]) * kLog2e);
-          const float4 v = *reinterpret_cast<const float4*>(so + (int64_t)(sp * NR + n0 + k) * kNope + d0);
-          acc[k].x += wgt * v.x;
-          acc[k].y += wgt * v.y;
-          acc[k].z += wgt * v.z;
-          acc[k].w += wgt * v.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (n0 + k >= u.nrows) break;
-      const int64_t g = (int64_t)u.q0 * a.num_heads + u.row0 + n0 + k;
-      if (a.out_f32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = acc[k];
-      } else {
-        const __nv_bfloat162 x = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-        const __nv_bfloat162 y = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
-      }
-    }
-  }
-  return true;
 }
 
 // A tile of a request's sequence: shard index k within the call, tile lt of
@@ -576,7 +363,7 @@ __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int 
 
 template <int NR, bool SPARSE, bool FUSED>
 __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ KvMaps maps, DecodeArgs a) {
+    decode_tc_kernel(const __grid_constant__ KvMaps maps, const __grid_constant__ DecodeArgs a) {
   using R = Roles<SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -609,7 +396,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.unit_done, 1);
     mbar_init(&sh.q_ready, 1);
-    mbar_init(&sh.merge_full, 1);
     sh.any_rescale[0] = sh.any_rescale[1] = 0;
     fence_mbar_init();
   }
@@ -819,13 +605,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
             const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
             const uint32_t o0 = tmem + TmemPlan<NR>::kColO;
-            if (p_split) {
-              if (kt == 0) issue_pv_tile<NR, true, true>(o0, v0, p0, id_pv);
-              else issue_pv_tile<NR, false, true>(o0, v0, p0, id_pv);
-            } else {
-              if (kt == 0) issue_pv_tile<NR, true, false>(o0, v0, p0, id_pv);
-              else issue_pv_tile<NR, false, false>(o0, v0, p0, id_pv);
-            }
+            issue_pv_tile<NR>(o0, v0, p0, id_pv, kt == 0, p_split);
             mma_commit(&sh.empty[stage]);
             mma_commit(&sh.pv_done);
             if (kt + 1 == w.n_kt) mma_commit(&sh.unit_done);
@@ -938,27 +718,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
       return true;
     };
-    // A split pair's chunk is counted one tile after its epilogue (or at the
-    // end), so the fence and the atomic's round trip overlap the next unit's
-    // MMAs; the CTA whose count completes the pair merges its chunks by LSE
-    // (threadfence-reduction pattern: publish, count, re-fence, read) at its
-    // next epilogue, outside the tile loop.
-    auto count_chunk = [&](const Unit& u) -> bool {
-      grid_dep_wait();  // the prep kernel zeroed the counters
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (st_tid == 0) sh.is_last = atomicAdd(&a.pair_done[u.cta0], 1) == u.nsplit - 1;
-      named_bar_sync(1, 128);
-      return sh.is_last != 0;
-    };
     UnitIter<NR, SPARSE> it;
     it.init(a, sh);
     Unit w, wn;
-    Unit pend;               // split chunk written but not yet counted
-    bool have_pend = false;
-    Unit mrg;                // pair whose chunks this CTA merges next
-    bool have_mrg = false;
-    uint32_t merge_phase = 0;
+    // the split pair whose first chunk this CTA holds (its last unit), for
+    // the split-merge kernel: {chunks, first global row, rows, 0}
+    int4 desc = make_int4(0, 0, 0, 0);
     bool more = it.next(a, wn);
     if (more && wn.n_kt > 0 && !load_q(wn)) ok = false;
     while (ok && more) {
@@ -1097,13 +862,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         named_bar_sync(1, 128);
         if (st_tid == 0) mbar_arrive(&sh.p_ready);
         if (++stage == kStages) { stage = 0; sphase ^= 1; }
-        if (have_pend) {
-          if (count_chunk(pend)) {
-            mrg = pend;
-            have_mrg = true;
-          }
-          have_pend = false;
-        }
       }
       if (!ok) break;
       // the next unit's Q goes in now, so that its first QK^T overlaps this
@@ -1131,7 +889,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         sh.inv_l[row] = live ? 1.f / lt : 0.f;
         if (row < w.nrows) {
           const float lse = live ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
-          if (partial) a.part_lse[chunk_slot<NR>(w.cta0, w.split) + row] = lse;
+          if (partial) a.part_lse[chunk_slot(w.cta0, w.split, NR) + row] = lse;
           else a.lse[grow(row)] = lse;
         }
       }
@@ -1152,7 +910,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           if (n >= w.nrows) break;
           const float v = __uint_as_float(o[n]) * sh.inv_l[n];
           if (partial) {
-            const int64_t slot = chunk_slot<NR>(w.cta0, w.split) + n;
+            const int64_t slot = chunk_slot(w.cta0, w.split, NR) + n;
             a.part_o[slot * kNope + dim] = v;
           } else if (a.out_f32) {
             static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
@@ -1162,22 +920,14 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
       tc_fence_before();
-      if (partial) {
-        pend = w;
-        have_pend = true;
-      }
+      if (partial && w.split == 0) desc = make_int4(w.nsplit, (int)grow(0), w.nrows, 0);
       named_bar_sync(1, 128);
-      if (have_mrg) {
-        // after this CTA's last unit the ring is idle: merge through it
-        if (more || !merge_split_chunks_smem<NR>(a, mrg, sh, st_tid, kv, merge_phase, ok))
-          merge_split_chunks<NR>(a, mrg, sh, st_tid);
-        have_mrg = false;
-        named_bar_sync(1, 128);
-      }
     }
-    if (ok && have_pend && count_chunk(pend)) {
-      if (!merge_split_chunks_smem<NR>(a, pend, sh, st_tid, kv, merge_phase, ok))
-        merge_split_chunks<NR>(a, pend, sh, st_tid);
+    if constexpr (!SPARSE) {
+      // every CTA publishes its entry (zero chunks: no split pair starts
+      // here), after the wait that precedes every global write
+      grid_dep_wait();
+      if (st_tid == 0) a.split_desc[blockIdx.x] = desc;
     }
   }
 

@@ -8,13 +8,13 @@
 // "vllm.v1.attention.backends.mla.flashattn_mla" (metadata builder,
 // _schedule_decode / num_splits) plans KV splits ahead of the kernel.  What
 // cannot be derived per CTA is done here, once per call: the status word is
-// reset, the per-CTA split counters are zeroed, malformed query ranges are
+// reset, malformed query ranges are
 // recorded, per-token key counts are written, and rows of requests without
 // local keys get their final result (o = 0, lse = -inf).
 //
 // The decode launches as soon as this kernel starts, plans and streams, and
 // waits for this kernel's completion before its first global write (outputs,
-// split counters, the status word).
+// split partials and table, the status word).
 #include "common.cuh"
 #include "plan.h"
 
@@ -32,7 +32,6 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   }
   const int H = a.num_heads;
   const int nthreads = gridDim.x * blockDim.x, tid = blockIdx.x * blockDim.x + threadIdx.x;
-  for (int c = tid; c < a.grid; c += nthreads) a.pair_done[c] = 0;
   for (int b = tid; b < a.num_requests; b += nthreads) {
     const ReqFacts f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, H, a.dcp_world, a.shard0,
                                      a.nshard, a.rows_per_group);

@@ -15,9 +15,7 @@ struct PrepArgs {
   int32_t num_requests, num_tokens, num_heads, dcp_world;
   int32_t shard0, nshard;  // the shards the decode covers (one, or all D when fused)
   int32_t rows_per_group;
-  int32_t grid;         // decode CTAs (one split counter each)
   WorkspaceHeader* hdr;
-  int32_t* pair_done;   // [grid] finished-chunk counters, zeroed here
   int32_t* row_counts;  // may be NULL
   // rows of requests without local keys get their final result here
   void* out;
@@ -26,14 +24,15 @@ struct PrepArgs {
 };
 
 // Where everything lives inside a dense-decode workspace (byte offsets).
-// Split partials are addressed by decode CTA: CTA c owns rows
+// Split partials are addressed by decode CTA (chunk_slot): CTA c owns rows
 // [2 c NR, 2 c NR + NR) for the chunk its first unit continues and
-// [(2 c + 1) NR, (2 c + 2) NR) for the chunk its last unit starts.
+// [(2 c + 1) NR, (2 c + 2) NR) for the chunk its last unit starts; entry c
+// of the split table describes the pair whose first chunk CTA c holds.
 struct DecodePlan {
   int32_t rows_per_group;  // rows (token, head) per work unit: 16 or 32
   int32_t grid;            // decode CTAs
   int32_t unit_penalty;    // balancing cost of a unit start, in 64-key tiles
-  size_t off_cnt, off_plse, off_po, total;
+  size_t off_desc, off_plse, off_po, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -63,8 +62,8 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   if (g < 1) g = 1;
   p.grid = (int32_t)g;
   size_t off = sizeof(WorkspaceHeader);
-  p.off_cnt = off;
-  off = align_up(off + sizeof(int32_t) * (size_t)p.grid, 256);
+  p.off_desc = off;
+  off = align_up(off + 16 * (size_t)p.grid, 256);
   p.off_plse = off;
   off = align_up(off + sizeof(float) * 2 * (size_t)p.grid * NR, 256);
   p.off_po = off;
@@ -90,5 +89,24 @@ inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk) {
 }
 
 __global__ void prep_kernel(PrepArgs a);
+
+// The split-merge kernel: the LSE merge of the chunks of every row group the
+// decode cut over several CTAs (entry c of the split table: {chunks, first
+// global (token, head) row, rows, 0}; chunk k's partial rows at
+// chunk_slot(c, k, NR)).  Block (c, s) merges rows [8 s, 8 s + 8) of entry c.
+struct SplitMergeArgs {
+  const int4* split_desc;  // [grid]
+  const float* part_lse;   // [2 grid NR]
+  const float* part_o;     // [2 grid NR, 512]
+  int32_t rows_per_group, grid;
+  int64_t num_rows;        // T * H
+  void* out;               // [T, H, 512]
+  int32_t out_f32;
+  float* lse;              // [T, H]
+  WorkspaceHeader* hdr;
+};
+constexpr int kSplitMergeRows = 8;  // rows per split-merge block
+
+__global__ void split_merge_kernel(SplitMergeArgs a);
 
 }  // namespace mla
