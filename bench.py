@@ -305,12 +305,9 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=False, fused=Fal
 
 
 def fused_decode_only(step):
-    import mla_decode_attention_04_gb300 as mla
     out = step.merged[0] if step.w_uv is not None else step.out
     lse = step.merged_lse[0] if step.w_uv is not None else step.lse
-    mla.mla_dcp_decode_fused(step.q_nope, step.q_pe, step.caches, step.tables, step.seq_lens, step.qsl,
-                             step.max_query_len, step.max_seq_len, step.scale, out=out, lse=lse,
-                             num_splits=step.num_splits, workspace=step.workspace)
+    step.decode(out, lse)
 
 
 def step_shard(step, r, cache, bt):
@@ -467,7 +464,7 @@ def run_ours(args):
         names = [n for n in ("plain_decode_d1", "mtp", "long_context", "sparse_mixed")
                  if args.configs == "all" or n in args.configs.split(",")]
         for n in names:
-            for fused in ((False, True) if n != "sparse_mixed" else (False,)):
+            for fused in (False, True):
                 r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)), fused=fused)
                 cs = summarize(r, pk)
                 key = n + ("_fused" if fused else "")

@@ -241,6 +241,38 @@ int mla_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, const vo
                          int32_t num_splits, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * mla_sparse_dcp_decode_fused -- the sparse decode of every DCP shard of one
+ * step in one call, with the merge built in, for one GPU that holds all D
+ * shard slices (the sparse counterpart of mla_dcp_decode_fused).  Token t's
+ * result merged over the D shards ("[Attention] DCP sparse MLA output-merge
+ * optimizations": LSE merge with per-row valid counts) is the softmax over
+ * the union of the shards' kept entries, i.e. over every used entry of its
+ * list, each read from its own shard (idx mod D) at local slot idx div D
+ * through that shard's block table.  One key-list kernel resolves every
+ * entry to its cache row, then one decode launch runs each (token, head
+ * group) over the whole list.
+ *
+ *  kv_caches, num_blocks, block_tables  host arrays of D entries, as in
+ *               mla_dcp_decode_fused.
+ *  topk_indices, topk, topk_valid  as in mla_sparse_dcp_decode.
+ *  dcp_world    D, 1..8.
+ *  out, lse     the merged result (as mla_dcp_decode_fused); no used entry
+ *               gives lse = -inf, out = 0.
+ *  kept_counts  device int32 [num_tokens] (the number of used entries over
+ *               all shards), or NULL.
+ *  workspace    >= mla_sparse_dcp_decode_workspace_size() bytes.
+ *  Errors as mla_sparse_dcp_decode; INVALID_ARG if dcp_world > 8.
+ * ---------------------------------------------------------------------- */
+int mla_sparse_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe,
+                                int64_t q_pe_row_stride, const void *const *kv_caches, const int64_t *num_blocks,
+                                int32_t page_size, int32_t kv_cache_dtype, const int32_t *const *block_tables,
+                                int32_t block_table_stride, const int32_t *seq_lens, const int32_t *query_start_loc,
+                                int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                const int32_t *topk_indices, int32_t topk, const int32_t *topk_valid,
+                                int32_t dcp_world, float scale, void *out, int32_t out_dtype, float *lse,
+                                int32_t *kept_counts, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * mla_workspace_status -- synchronises `stream`, then reads the status word
  * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
  * with *detail set to the first failing check's code: 1 = a page id (or its

@@ -32,6 +32,7 @@ EXPORTS = [
     "mla_last_error", "mla_dcp_decode_workspace_size", "mla_dcp_decode", "mla_sparse_dcp_decode_workspace_size",
     "mla_sparse_dcp_decode", "dcp_lse_merge", "mla_workspace_status", "mla_kernel_launch_count",
     "mla_dcp_decode_static_scratch", "mla_dcp_decode_fused_workspace_size", "mla_dcp_decode_fused",
+    "mla_sparse_dcp_decode_fused",
 ]
 
 # Size of the library's fixed device scratch array used by
@@ -74,6 +75,9 @@ def _bind(lib):
     lib.mla_dcp_decode_fused.restype = ctypes.c_int
     lib.mla_dcp_decode_fused.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, i32,
                                          i32, i32, ctypes.c_float, vp, i32, vp, i32, vp, sz, vp]
+    lib.mla_sparse_dcp_decode_fused.restype = ctypes.c_int
+    lib.mla_sparse_dcp_decode_fused.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32,
+                                                vp, i32, vp, i32, f32, vp, i32, vp, vp, vp, sz, vp]
     lib.mla_dcp_decode_static_scratch.restype = ctypes.c_int
     lib.mla_dcp_decode_static_scratch.argtypes = [vp, i64, vp, i64, vp, i64, i32, i32, vp, i32, vp, vp, i32, i32, i32,
                                                   i32, i32, i32, i32, f32, vp, i32, vp, vp, i32, vp]
@@ -214,6 +218,53 @@ def mla_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_
                                     float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), int(num_splits),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
+
+
+def mla_sparse_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_start_loc, topk_indices,
+                                topk_valid, scale, out=None, lse=None, kept_counts=None, out_dtype=torch.bfloat16,
+                                workspace=None, stream=None):
+    """Sparse decode of all D DCP shards in one call (the shard caches and
+    block tables are lists of D tensors): each token attends over every used
+    entry of its list, which is the merge of the D shard results.  Returns
+    the merged (out [T,H,512], lse [T,H], kept_counts [T] or None)."""
+    lib = load_library()
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    D = len(kv_caches)
+    if len(block_tables) != D or D < 1:
+        raise ValueError("kv_caches and block_tables need one entry per shard")
+    sn, sp = _row_stride(q_nope, KV_LORA_RANK, "q_nope"), _row_stride(q_pe, ROPE_DIM, "q_pe")
+    kv_args = [_kv_args(c) for c in kv_caches]
+    ps, kv_dt = kv_args[0][1], kv_args[0][2]
+    if any(a[1] != ps or a[2] != kv_dt for a in kv_args):
+        raise ValueError("all shard caches need the same page size and dtype")
+    bt_stride = block_tables[0].shape[1]
+    for bt in block_tables:
+        _i32(bt, "block_table")
+        if bt.shape[1] != bt_stride:
+            raise ValueError("all block tables need the same row stride")
+    _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc")
+    _i32(topk_indices, "topk_indices"), _i32(topk_valid, "topk_valid")
+    K = topk_indices.shape[1]
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, KV_LORA_RANK), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    need = sparse_workspace_size(T, H, K, D)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
+    nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
+    bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    _check(lib.mla_sparse_dcp_decode_fused(_ptr(q_nope), sn, _ptr(q_pe), sp, ctypes.cast(kv_ptrs, ctypes.c_void_p),
+                                           ctypes.cast(nbs, ctypes.c_void_p), ps, kv_dt,
+                                           ctypes.cast(bt_ptrs, ctypes.c_void_p), bt_stride, _ptr(seq_lens),
+                                           _ptr(query_start_loc), B, T, H, _ptr(topk_indices), K, _ptr(topk_valid), D,
+                                           float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), _ptr(kept_counts),
+                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
+    return out, lse, kept_counts
 
 
 def mla_sparse_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_loc, topk_indices, topk_valid,

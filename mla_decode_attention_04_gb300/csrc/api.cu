@@ -218,6 +218,89 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   return ok();
 }
 
+// The sparse decode over nshard consecutive shards from rank shard0 (one
+// shard: mla_sparse_dcp_decode; all D: mla_sparse_dcp_decode_fused).
+// Arguments other than the list inputs checked by the caller.
+int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                  int nshard, int shard0, const void* const* kv_caches, const int64_t* num_blocks, int32_t page_size,
+                  const int32_t* const* block_tables, int32_t block_table_stride, const int32_t* seq_lens,
+                  const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                  const int32_t* topk_indices, int32_t topk, const int32_t* topk_valid, int32_t dcp_world,
+                  float scale, void* out, int32_t out_dtype, float* lse, int32_t* counts_out, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (!topk_indices || !topk_valid) return fail(MLA_ERR_INVALID_ARG, "topk_indices and topk_valid are required");
+  if (topk < 1 || topk > 65536) return fail(MLA_ERR_INVALID_ARG, "topk %d not in [1, 65536]", topk);
+  if (num_tokens == 0) return ok();
+  const mla::SparsePlan plan = mla::make_sparse_plan(num_tokens, num_heads, topk);
+  if (workspace_bytes < plan.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
+  cudaError_t e = cudaMemsetAsync(hdr, 0, 16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+
+  mla::SparseListArgs la{};
+  la.topk = topk_indices;
+  la.topk_valid = topk_valid;
+  la.seq_lens = seq_lens;
+  la.query_start_loc = query_start_loc;
+  la.num_requests = num_requests;
+  la.num_tokens = num_tokens;
+  la.topk_k = topk;
+  la.dcp_world = dcp_world;
+  la.shard0 = shard0;
+  la.nshard = nshard;
+  for (int k = 0; k < nshard; ++k) {
+    la.kvs[k] = kv_caches[k];
+    la.bts[k] = block_tables[k];
+    la.nblocks[k] = num_blocks[k];
+  }
+  la.page_size = page_size;
+  la.bt_stride = block_table_stride;
+  la.key_rows = reinterpret_cast<int64_t*>(ws + plan.off_lists);
+  la.counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(ws + plan.off_cnt);
+  la.tok_req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
+  la.hdr = hdr;
+  if ((e = mla::launch_sparse_lists(la, st)) != cudaSuccess) return cuda_fail(e, "sparse list launch");
+  count_launch();
+
+  mla::DecodeArgs da{};
+  da.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  da.q_nope_stride = q_nope_row_stride;
+  da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  da.q_pe_stride = q_pe_row_stride;
+  da.kv = static_cast<const __nv_bfloat16*>(kv_caches[0]);
+  da.num_blocks = num_blocks[0];
+  da.page_size = page_size;
+  da.block_table = block_tables[0];
+  da.nshard = 1;  // the key lists hold row addresses: the decode reads no shard table
+  da.shard0 = shard0;
+  da.kvs[0] = static_cast<const __nv_bfloat16*>(kv_caches[0]);
+  da.bts[0] = block_tables[0];
+  da.nblocks[0] = num_blocks[0];
+  da.bt_stride = block_table_stride;
+  da.num_heads = num_heads;
+  da.dcp_world = dcp_world;
+  da.dcp_rank = shard0;
+  da.scale = scale;
+  da.out = out;
+  da.out_f32 = out_dtype == MLA_DTYPE_F32;
+  da.lse = lse;
+  da.hdr = hdr;
+  da.key_rows = la.key_rows;
+  da.list_count = la.counts;
+  da.tok_req = la.tok_req;
+  da.list_stride = topk;
+  da.num_tokens = num_tokens;
+  da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
+  const int grid = num_tokens * da.groups_per_token;
+  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, true, grid, current_sm_count(), st)) != cudaSuccess)
+    return cuda_fail(e, "sparse decode launch");
+  count_launch();
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -292,70 +375,36 @@ int mla_sparse_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const v
                                num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
                                workspace);
   if (rc != MLA_OK) return rc;
-  if (!topk_indices || !topk_valid || !local_counts)
-    return fail(MLA_ERR_INVALID_ARG, "topk_indices, topk_valid and local_counts are required");
-  if (topk < 1 || topk > 65536) return fail(MLA_ERR_INVALID_ARG, "topk %d not in [1, 65536]", topk);
-  if (num_tokens == 0) return ok();
-  const mla::SparsePlan plan = mla::make_sparse_plan(num_tokens, num_heads, topk);
-  if (workspace_bytes < plan.total)
-    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  mla::WorkspaceHeader* hdr = reinterpret_cast<mla::WorkspaceHeader*>(ws);
-  cudaError_t e = cudaMemsetAsync(hdr, 0, 16, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace header reset");
+  if (!local_counts) return fail(MLA_ERR_INVALID_ARG, "local_counts is required");
+  return sparse_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, 1, dcp_rank, &kv_cache, &num_blocks,
+                       page_size, &block_table, block_table_stride, seq_lens, query_start_loc, num_requests,
+                       num_tokens, num_heads, topk_indices, topk, topk_valid, dcp_world, scale, out, out_dtype, lse,
+                       local_counts, workspace, workspace_bytes, stream);
+}
 
-  mla::SparseListArgs la{};
-  la.topk = topk_indices;
-  la.topk_valid = topk_valid;
-  la.seq_lens = seq_lens;
-  la.query_start_loc = query_start_loc;
-  la.num_requests = num_requests;
-  la.num_tokens = num_tokens;
-  la.topk_k = topk;
-  la.dcp_world = dcp_world;
-  la.dcp_rank = dcp_rank;
-  la.lists = reinterpret_cast<int32_t*>(ws + plan.off_lists);
-  la.local_counts = local_counts;
-  la.tok_req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
-  la.hdr = hdr;
-  if ((e = mla::launch_sparse_lists(la, st)) != cudaSuccess) return cuda_fail(e, "sparse list launch");
-  count_launch();
-
-  mla::DecodeArgs da{};
-  da.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
-  da.q_nope_stride = q_nope_row_stride;
-  da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
-  da.q_pe_stride = q_pe_row_stride;
-  da.kv = static_cast<const __nv_bfloat16*>(kv_cache);
-  da.num_blocks = num_blocks;
-  da.page_size = page_size;
-  da.block_table = block_table;
-  da.nshard = 1;
-  da.shard0 = dcp_rank;
-  da.kvs[0] = static_cast<const __nv_bfloat16*>(kv_cache);
-  da.bts[0] = block_table;
-  da.nblocks[0] = num_blocks;
-  da.bt_stride = block_table_stride;
-  da.num_heads = num_heads;
-  da.dcp_world = dcp_world;
-  da.dcp_rank = dcp_rank;
-  da.scale = scale;
-  da.out = out;
-  da.out_f32 = out_dtype == MLA_DTYPE_F32;
-  da.lse = lse;
-  da.hdr = hdr;
-  da.lists = la.lists;
-  da.list_count = local_counts;
-  da.tok_req = la.tok_req;
-  da.list_stride = topk;
-  da.num_tokens = num_tokens;
-  da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
-  const int grid = num_tokens * da.groups_per_token;
-  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, true, grid, current_sm_count(), st)) != cudaSuccess)
-    return cuda_fail(e, "sparse decode launch");
-  count_launch();
-  return ok();
+int mla_sparse_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe,
+                                int64_t q_pe_row_stride, const void* const* kv_caches, const int64_t* num_blocks,
+                                int32_t page_size, int32_t kv_cache_dtype, const int32_t* const* block_tables,
+                                int32_t block_table_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                                int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                const int32_t* topk_indices, int32_t topk, const int32_t* topk_valid,
+                                int32_t dcp_world, float scale, void* out, int32_t out_dtype, float* lse,
+                                int32_t* kept_counts, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dcp_world < 1 || dcp_world > mla::kMaxShards)
+    return fail(MLA_ERR_INVALID_ARG, "dcp_world %d not in [1, %d] for the fused call", dcp_world, mla::kMaxShards);
+  if (!kv_caches || !num_blocks || !block_tables)
+    return fail(MLA_ERR_INVALID_ARG, "kv_caches, num_blocks and block_tables are required");
+  for (int r = 0; r < dcp_world; ++r) {
+    int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_caches[r], num_blocks[r],
+                                 page_size, kv_cache_dtype, block_tables[r], block_table_stride, seq_lens,
+                                 query_start_loc, num_requests, num_tokens, num_heads, dcp_world, r, scale, out,
+                                 out_dtype, lse, workspace);
+    if (rc != MLA_OK) return rc;
+  }
+  return sparse_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, dcp_world, 0, kv_caches, num_blocks,
+                       page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests,
+                       num_tokens, num_heads, topk_indices, topk, topk_valid, dcp_world, scale, out, out_dtype, lse,
+                       kept_counts, workspace, workspace_bytes, stream);
 }
 
 int dcp_lse_merge(const void* partials, int32_t partial_dtype, const float* lses, const int32_t* valid_counts,

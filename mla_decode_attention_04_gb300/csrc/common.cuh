@@ -60,8 +60,23 @@ __host__ __device__ __forceinline__ int64_t chunk_slot(int cta0, int k, int NR) 
   return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k)) * NR;
 }
 
-// Most DCP shards one dense call can cover (the shard-fused entry point).
+// Most DCP shards one call can cover (the shard-fused entry points).
 constexpr int kMaxShards = 8;
+
+// Element k of a per-shard kernel-parameter array, read with a static index.
+template <typename T>
+__device__ __forceinline__ T pick_shard(const T (&arr)[kMaxShards], int k) {
+  switch (k) {
+    case 0: return arr[0];
+    case 1: return arr[1];
+    case 2: return arr[2];
+    case 3: return arr[3];
+    case 4: return arr[4];
+    case 5: return arr[5];
+    case 6: return arr[6];
+    default: return arr[7];
+  }
+}
 
 // What the dense decode needs to know about request b, from seq_lens and
 // query_start_loc alone (the prep kernel and every decode CTA derive it the
@@ -74,10 +89,11 @@ struct ReqFacts {
   bool ok;
 };
 
-__device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const int32_t* query_start_loc, int b,
-                                                  int num_tokens, int H, int D, int shard0, int nshard, int NR) {
+// The facts of request b from its raw inputs q0 = query_start_loc[b],
+// q1 = query_start_loc[b + 1] and L = seq_lens[b].
+__device__ __forceinline__ ReqFacts request_facts_of(int q0, int q1, int L, int num_tokens, int H, int D, int shard0,
+                                                     int nshard, int NR) {
   ReqFacts f;
-  const int q0 = query_start_loc[b], q1 = query_start_loc[b + 1], L = seq_lens[b];
   f.ok = !(q1 - q0 < 0 || q1 - q0 > L || q0 < 0 || q1 > num_tokens);
   f.q0 = q0 < 0 ? 0 : q0;
   f.q_len = f.ok ? q1 - q0 : 0;
@@ -87,6 +103,12 @@ __device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const
   f.nt = 0;
   for (int k = 0; k < nshard; ++k) f.nt += (local_len(L, D, shard0 + k) + kKeyTile - 1) / kKeyTile;
   return f;
+}
+
+__device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const int32_t* query_start_loc, int b,
+                                                  int num_tokens, int H, int D, int shard0, int nshard, int NR) {
+  return request_facts_of(query_start_loc[b], query_start_loc[b + 1], seq_lens[b], num_tokens, H, D, shard0, nshard,
+                          NR);
 }
 
 // Walks a request's key-tile sequence (shard k's local keys as whole tiles,

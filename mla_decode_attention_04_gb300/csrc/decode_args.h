@@ -36,7 +36,7 @@ struct DecodeArgs {
   float* part_lse;   // [2 grid NR]
   float* part_o;     // [2 grid NR, 512]
   // sparse
-  const int32_t* lists;       // [T, list_stride] shard-local slots
+  const int64_t* key_rows;    // [T, list_stride] cache-row addresses of each token's keys
   const int32_t* list_count;  // [T]
   const int32_t* tok_req;     // [T] owning request
   int32_t list_stride;

@@ -14,15 +14,24 @@ namespace mla {
 cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool sparse, int max_units, int num_sms,
                              cudaStream_t stream);
 
+// The sparse decode's key lists: for every token, the cache-row addresses
+// of the entries it keeps on shards shard0 .. shard0 + nshard - 1 (one
+// shard's call, or all D when fused), resolved through that shard's block
+// table once here instead of once per head group in the decode.
 struct SparseListArgs {
   const int32_t* topk;        // [T, K]
   const int32_t* topk_valid;  // [T]
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
-  int32_t num_requests, num_tokens, topk_k, dcp_world, dcp_rank;
-  int32_t* lists;         // [T, K] out: shard-local slots
-  int32_t* local_counts;  // [T] out
-  int32_t* tok_req;       // [T] out
+  int32_t num_requests, num_tokens, topk_k, dcp_world;
+  int32_t shard0, nshard;
+  const void* kvs[kMaxShards];      // shard caches [num_blocks, page_size, 576] bf16
+  const int32_t* bts[kMaxShards];   // shard block tables [B, bt_stride]
+  int64_t nblocks[kMaxShards];
+  int32_t page_size, bt_stride;
+  int64_t* key_rows;  // [T, K] out: device addresses of the kept entries' cache rows, in list order
+  int32_t* counts;    // [T] out: entries kept
+  int32_t* tok_req;   // [T] out
   WorkspaceHeader* hdr;
 };
 cudaError_t launch_sparse_lists(const SparseListArgs& a, cudaStream_t stream);

@@ -119,15 +119,24 @@ struct Unit {
 // contributes unit_penalty work-free items (the cost of starting a unit)
 // followed by its 64-key tiles to one flattened list of W items; CTA c takes
 // items [c W / G, (c + 1) W / G), cut at pair boundaries.  The CTA found the
-// request holding its first item at start-up (plan_cta); later requests'
-// facts are loaded one request ahead.  Sparse: (token, head group) units
+// request holding its first item at start-up (plan_cta); the next request's
+// raw lengths are loaded one request ahead and turned into facts only when
+// the walk reaches it, so no step of the walk waits for a load.  Sparse: (token, head group) units
 // dealt round-robin.  Every role walks the same sequence.
 template <int NR, bool SPARSE>
 struct UnitIter {
   int64_t i, hi, W, G, ib;  // dense: next item, range end, plan, item base of request b
   int b;
-  ReqFacts cur, nxt;
+  ReqFacts cur;
+  int nq0, nq1, nL;  // query_start_loc[b + 1], [b + 2], seq_lens[b + 1]
   int u, units;
+
+  // issues the loads of request b + 1's raw lengths (consumed one request later)
+  __device__ __forceinline__ void fetch_next(const DecodeArgs& a) {
+    nq0 = a.query_start_loc[b + 1];
+    nq1 = a.query_start_loc[b + 2];
+    nL = a.seq_lens[b + 1];
+  }
 
   __device__ void init(const DecodeArgs& a, const TcShared& sh) {
     if constexpr (SPARSE) {
@@ -145,9 +154,7 @@ struct UnitIter {
       b = sh.plan_b;
       ib = sh.plan_ib;
       cur = sh.plan_f;
-      if (b + 1 < a.num_requests)
-        nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
-                            a.shard0, a.nshard, NR);
+      if (b + 1 < a.num_requests) fetch_next(a);
     }
   }
 
@@ -188,10 +195,8 @@ struct UnitIter {
           }
           ib = rend;
           ++b;
-          cur = nxt;
-          if (b + 1 < a.num_requests)
-            nxt = request_facts(a.seq_lens, a.query_start_loc, b + 1, a.num_tokens, a.num_heads, a.dcp_world,
-                                a.shard0, a.nshard, NR);
+          cur = request_facts_of(nq0, nq1, nL, a.num_tokens, a.num_heads, a.dcp_world, a.shard0, a.nshard, NR);
+          if (b + 1 < a.num_requests) fetch_next(a);
           continue;
         }
         const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
@@ -229,7 +234,7 @@ struct UnitIter {
 // to one copy of the scan: the kernel's first instructions are fetched cold
 // while they run, so start-up code is kept short.
 template <int NR>
-__device__ __noinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
+__device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int B = a.num_requests;
   const int64_t pen = a.unit_penalty;
@@ -295,15 +300,6 @@ __device__ __noinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   __syncthreads();
 }
 
-// cache slot (page * page_size + offset) of shard-local key j of request b, or -1
-__device__ __forceinline__ int64_t slot_of(const DecodeArgs& a, int b, int j) {
-  const int pidx = j / a.page_size;
-  if (pidx >= a.bt_stride) return -1;
-  const int page = a.block_table[(int64_t)b * a.bt_stride + pidx];
-  if (page < 0 || page >= a.num_blocks) return -1;
-  return (int64_t)page * a.page_size + j % a.page_size;
-}
-
 // The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T.  The
 // first tile of a unit overwrites O^T; the P split (hi + lo, for fp32
 // outputs) doubles the MMAs.  One rolled copy: the issue rate of a thread,
@@ -331,21 +327,6 @@ struct TileLoc {
 struct KvMaps {
   CUtensorMap m[kMaxShards];
 };
-
-// Element k of a per-shard kernel-parameter array, read with a static index.
-template <typename T>
-__device__ __forceinline__ T pick_shard(const T (&arr)[kMaxShards], int k) {
-  switch (k) {
-    case 0: return arr[0];
-    case 1: return arr[1];
-    case 2: return arr[2];
-    case 3: return arr[3];
-    case 4: return arr[4];
-    case 5: return arr[5];
-    case 6: return arr[6];
-    default: return arr[7];
-  }
-}
 
 // Address of shard k's map in the kernel's parameter space (static indices).
 __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int k) {
@@ -410,6 +391,14 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if constexpr (!SPARSE) plan_cta<NR>(a, sh);
+  // Every role walks the same units; the first one is found here, in code
+  // all warps share (a kernel's instructions are fetched cold as they first
+  // run, so each role running its own copy of this step would pay for it
+  // again before its first tile).
+  UnitIter<NR, SPARSE> it;
+  it.init(a, sh);
+  Unit w0;
+  const bool more0 = it.next(a, w0);
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
   bool bad_page = false;
@@ -426,24 +415,40 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint64_t pol = policy_evict_first();
       const int ps = a.page_size;
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
-      UnitIter<NR, SPARSE> it;
-      it.init(a, sh);
-      Unit w;
+      Unit w = w0;
       int cache_b = -1, cache_k = -1, cache_col = 0, my_page = -1;
-      while (ok && it.next(a, w)) {
+      // the unit's Q rows: one slot of the ring, a bulk copy per row half
+      auto issue_q = [&](const Unit& u, int st, uint32_t ph) -> bool {
+        bool good = true;
+        if (lane == 0) {
+          if (!mbar_wait(&sh.empty[st], ph ^ 1)) good = false;
+          else mbar_arrive_expect_tx(&sh.full[st], (uint32_t)u.nrows * (kRow * 2));
+        }
+        good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+        if (!good) return false;
+        uint8_t* qdst = kv + st * kStageBytes;
+        for (int r = lane; r < u.nrows; r += 32) {
+          const int64_t grow = (int64_t)u.q0 * a.num_heads + u.row0 + r;
+          bulk_load(qdst + r * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[st]);
+          bulk_load(qdst + r * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[st]);
+        }
+        return true;
+      };
+      // The CTA's first unit finds every stage free: its first two key tiles
+      // go out before its Q slot is filled (the slot keeps its place in the
+      // ring), because the tiles are what the first score product waits for.
+      bool first = true;
+      for (bool more = more0; ok && more; more = it.next(a, w)) {
+        int q_stage = -1;  // deferred Q slot of the first unit
+        uint32_t q_phase = 0;
         if (w.n_kt > 0) {
-          // the unit's Q rows: one slot of the ring, a bulk copy per row half
-          if (lane == 0) {
-            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) ok = false;
-            else mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
-          }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          uint8_t* qdst = kv + stage * kStageBytes;
-          for (int r = lane; r < w.nrows; r += 32) {
-            const int64_t grow = (int64_t)w.q0 * a.num_heads + w.row0 + r;
-            bulk_load(qdst + r * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
-            bulk_load(qdst + r * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage]);
+          if (first) {
+            q_stage = stage;
+            q_phase = phase;
+            first = false;
+          } else if (!issue_q(w, stage, phase)) {
+            ok = false;
+            break;
           }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -505,36 +510,47 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (q_stage >= 0 && (kt == 1 || kt + 1 == w.n_kt)) {
+            if (ok && !issue_q(w, q_stage, q_phase)) ok = false;
+            q_stage = -1;
+          }
         }
       }
     } else {
-      // sparse: 4 warps gather 64 rows x 72 16-byte pieces per tile with cp.async
-      const int pt = threadIdx.x;  // 0..127
-      UnitIter<NR, SPARSE> it;
-      it.init(a, sh);
-      Unit w;
-      while (ok && it.next(a, w)) {
-        const int32_t* list = a.lists + (int64_t)w.token * a.list_stride;
+      // sparse: 4 warps gather 64 rows x 72 16-byte pieces per tile with
+      // cp.async; warp pw copies keys [16 pw, 16 pw + 16), one row at a time
+      // with all its lanes (a row's 72 pieces in 3 instructions of
+      // consecutive 16-byte pieces: every instruction reads whole 128-byte
+      // lines), so the memory system sees line-sized requests, not one
+      // 16-byte request per thread and piece.
+      const int pw = warp;  // 0..3
+      Unit w = w0;
+      for (bool more = more0; ok && more; more = it.next(a, w)) {
+        const int64_t* rows = a.key_rows + (int64_t)w.token * a.list_stride;
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-          const int k0 = kt * kKeyTile;
+          const int k0 = kt * kKeyTile + pw * 16;
+          // lane l (< 16) fetches the row address of key k0 + l
+          const int64_t my_row = (lane < 16 && k0 + lane < w.key1) ? rows[k0 + lane] : 0;
           if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
           uint8_t* dst = kv + stage * kStageBytes;
-          // thread pt handles key (pt / 2) and pieces [36 * (pt & 1), +36)
-          const int key = pt >> 1;
-          const int j = k0 + key;
-          int64_t slot = -1;
-          if (j < w.key1) {
-            slot = slot_of(a, w.b, list[j]);
-            if (slot < 0) record_check(a.hdr, kCheckPageOutOfRange);
-          }
-          const char* src = reinterpret_cast<const char*>(a.kv) + (slot < 0 ? 0 : slot) * (kRow * 2);
-          const uint32_t nbytes = slot < 0 ? 0u : 16u;
-          for (int q = 0; q < 36; ++q) {
-            const int piece = 36 * (pt & 1) + q;  // 0..71
-            const int cc = piece >> 3, within = piece & 7;
-            const uint32_t d = smem_u32(dst + cc * kChunk + key * 128 + ((within ^ (key & 7)) << 4));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src + piece * 16), "r"(nbytes)
-                         : "memory");
+#pragma unroll 4
+          for (int kk = 0; kk < 16; ++kk) {
+            const int key = pw * 16 + kk;
+            const int64_t row = __shfl_sync(0xffffffffu, my_row, kk);
+            // a key past the list's end copies no byte (its row is zero-filled)
+            const char* src = row != 0 ? reinterpret_cast<const char*>(row) : reinterpret_cast<const char*>(a.kv);
+            const uint32_t nbytes = row != 0 ? 16u : 0u;
+#pragma unroll
+            for (int q0 = 0; q0 < 72; q0 += 32) {
+              const int piece = q0 + lane;  // 0..71
+              if (piece < 72) {
+                const int cc = piece >> 3, within = piece & 7;
+                const uint32_t d = smem_u32(dst + cc * kChunk + key * 128 + ((within ^ (key & 7)) << 4));
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src + piece * 16),
+                             "r"(nbytes)
+                             : "memory");
+              }
+            }
           }
           asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[stage]))
                        : "memory");
@@ -553,9 +569,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       uint32_t phase = 0, j = 0, q_ph = 0;
       const uint32_t id_qk = idesc_bf16_f32(128, 64, 0, 0);
       const uint32_t id_pv = idesc_bf16_f32(128, NR, 1, 0);
-      UnitIter<NR, SPARSE> it;
-      it.init(a, sh);
-      Unit w;
+      Unit w = w0;
       // Descriptors are linear in the start address (its field is addr >> 4
       // and every address here is below 256 KB), so each operand is a base
       // descriptor plus a constant offset in 16-byte units: the issue loops
@@ -568,7 +582,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       if (warp == R::kMmaWarp) {
         // S(j) = Q . KV(j)^T into S buffer j % SB as soon as tile j has
         // landed and the softmax has copied S(j - SB) out of that buffer.
-        while (ok && it.next(a, w)) {
+        for (bool more = more0; ok && more; more = it.next(a, w)) {
           if (w.n_kt == 0) continue;
           if (!SPARSE && ++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
           if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
@@ -596,7 +610,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         // O^T += V_c(j)^T . P(j)^T once the softmax has written P(j); its
         // completion frees the ring stage (QK^T(j), the stage's other
         // reader, completed before the softmax saw S(j)).
-        while (ok && it.next(a, w)) {
+        for (bool more = more0; ok && more; more = it.next(a, w)) {
           if (w.n_kt == 0) continue;
           if (!SPARSE && ++stage == kStages) stage = 0;  // the unit's Q slot
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
@@ -718,13 +732,11 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       }
       return true;
     };
-    UnitIter<NR, SPARSE> it;
-    it.init(a, sh);
-    Unit w, wn;
+    Unit w, wn = w0;
     // the split pair whose first chunk this CTA holds (its last unit), for
     // the split-merge kernel: {chunks, first global row, rows, 0}
     int4 desc = make_int4(0, 0, 0, 0);
-    bool more = it.next(a, wn);
+    bool more = more0;
     if (more && wn.n_kt > 0 && !load_q(wn)) ok = false;
     while (ok && more) {
       w = wn;
@@ -894,28 +906,36 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
       named_bar_sync(1, 128);
+      // O^T's 4 column blocks, MB per TMEM round trip (64 registers)
+      constexpr int MB = 64 / NR;
 #pragma unroll 1
-      for (int m = 0; m < 4; ++m) {
-        uint32_t o[NR];
+      for (int m0 = 0; m0 < 4; m0 += MB) {
+        uint32_t o[MB][NR];
         if (w.n_kt > 0) {
-          tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
+#pragma unroll
+          for (int mb = 0; mb < MB; ++mb) tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + (m0 + mb) * NR, o[mb]);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int n = 0; n < NR; ++n) o[n] = 0u;
-        }
-        const int dim = m * 128 + quarter * 32 + lane;
+          for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-        for (int n = 0; n < NR; ++n) {
-          if (n >= w.nrows) break;
-          const float v = __uint_as_float(o[n]) * sh.inv_l[n];
-          if (partial) {
-            const int64_t slot = chunk_slot(w.cta0, w.split, NR) + n;
-            a.part_o[slot * kNope + dim] = v;
-          } else if (a.out_f32) {
-            static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
-          } else {
-            static_cast<__nv_bfloat16*>(a.out)[grow(n) * kNope + dim] = __float2bfloat16_rn(v);
+            for (int n = 0; n < NR; ++n) o[mb][n] = 0u;
+        }
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb) {
+          const int dim = (m0 + mb) * 128 + quarter * 32 + lane;
+#pragma unroll
+          for (int n = 0; n < NR; ++n) {
+            if (n >= w.nrows) break;
+            const float v = __uint_as_float(o[mb][n]) * sh.inv_l[n];
+            if (partial) {
+              const int64_t slot = chunk_slot(w.cta0, w.split, NR) + n;
+              a.part_o[slot * kNope + dim] = v;
+            } else if (a.out_f32) {
+              static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
+            } else {
+              static_cast<__nv_bfloat16*>(a.out)[grow(n) * kNope + dim] = __float2bfloat16_rn(v);
+            }
           }
         }
       }

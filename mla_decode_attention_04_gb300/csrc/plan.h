@@ -72,10 +72,12 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   return p;
 }
 
-// Sparse decode workspace: header, token -> request map, per-token lists.
+// Sparse decode workspace: header, token -> request map, per-token key
+// counts (used when the caller does not ask for them), per-token lists of
+// cache-row addresses.
 struct SparsePlan {
   int32_t rows_per_group;
-  size_t off_tok, off_lists, total;
+  size_t off_tok, off_cnt, off_lists, total;
 };
 
 inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk) {
@@ -83,8 +85,9 @@ inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk) {
   p.rows_per_group = H <= 16 ? 16 : 32;
   const size_t nt = (size_t)(T > 0 ? T : 1);
   p.off_tok = sizeof(WorkspaceHeader);
-  p.off_lists = align_up(p.off_tok + sizeof(int32_t) * nt, 256);
-  p.total = align_up(p.off_lists + sizeof(int32_t) * nt * (size_t)(topk > 0 ? topk : 1), 256);
+  p.off_cnt = align_up(p.off_tok + sizeof(int32_t) * nt, 256);
+  p.off_lists = align_up(p.off_cnt + sizeof(int32_t) * nt, 256);
+  p.total = align_up(p.off_lists + sizeof(int64_t) * nt * (size_t)(topk > 0 ? topk : 1), 256);
   return p;
 }
 
@@ -93,7 +96,7 @@ __global__ void prep_kernel(PrepArgs a);
 // The split-merge kernel: the LSE merge of the chunks of every row group the
 // decode cut over several CTAs (entry c of the split table: {chunks, first
 // global (token, head) row, rows, 0}; chunk k's partial rows at
-// chunk_slot(c, k, NR)).  Block (c, s) merges rows [8 s, 8 s + 8) of entry c.
+// chunk_slot(c, k, NR)).  Block (c, s) merges rows [4 s, 4 s + 4) of entry c.
 struct SplitMergeArgs {
   const int4* split_desc;  // [grid]
   const float* part_lse;   // [2 grid NR]
@@ -105,7 +108,7 @@ struct SplitMergeArgs {
   float* lse;              // [T, H]
   WorkspaceHeader* hdr;
 };
-constexpr int kSplitMergeRows = 8;  // rows per split-merge block
+constexpr int kSplitMergeRows = 4;  // rows per split-merge block
 
 __global__ void split_merge_kernel(SplitMergeArgs a);
 

@@ -38,9 +38,27 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
   grid_dep_launch();
   grid_dep_wait();  // the decode's partials and table are complete and visible
   constexpr int R = kSplitMergeRows;
+  constexpr int kAhead = 4;  // chunks whose loads go out with the table entry's
   const int NR = a.rows_per_group;
   const int slices = NR / R;
   const int c = blockIdx.x / slices, n0 = (blockIdx.x % slices) * R;
+  const int d0 = threadIdx.x * 4;  // latent dims [d0, d0 + 4) of each of the block's rows
+  // The first kAhead chunks' rows are loaded before the entry is known (their
+  // slots exist whenever c + k < grid; rows of chunks the entry does not have
+  // are never used), so the entry and the data cost one memory latency.
+  float l[kAhead][R];
+  float4 v[kAhead][R];
+#pragma unroll
+  for (int k = 0; k < kAhead; ++k) {
+    const bool exists = c + k < a.grid;
+    const int64_t slot = chunk_slot(c, k, NR) + n0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      l[k][r] = exists ? __ldcg(a.part_lse + slot + r) : -INFINITY;
+      v[k][r] = exists ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (slot + r) * kNope + d0))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   const int4 d = a.split_desc[c];
   const int nsplit = d.x, nrows = d.z;
   const int64_t g0 = d.y;
@@ -49,42 +67,44 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
     if (threadIdx.x == 0 && n0 == 0) record_check(a.hdr, kCheckBadSplitEntry);
     return;
   }
-  const int d0 = threadIdx.x * 4;  // latent dims [d0, d0 + 4) of each of the block's rows
   float m[R], z[R];
   float4 acc[R];
 #pragma unroll
-  for (int k = 0; k < R; ++k) {
-    m[k] = -INFINITY;
-    z[k] = 0.f;
-    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = 0; r < R; ++r) {
+    m[r] = -INFINITY;
+    z[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // two chunks per pass: all 2 * R partial loads of a pass are in flight together
+#pragma unroll
+  for (int k = 0; k < kAhead; ++k)
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (k < nsplit && n0 + r < nrows) fold_chunk(m[r], z[r], acc[r], l[k][r], v[k][r]);
+  // longer splits: the rest, kAhead chunks per pass (all loads of a pass in flight)
 #pragma unroll 1
-  for (int sp = 0; sp < nsplit; sp += 2) {
-    float l[2][R];
-    float4 v[2][R];
+  for (int sp = kAhead; sp < nsplit; sp += kAhead) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int64_t slot = chunk_slot(c, sp + q, NR) + n0;
+    for (int k = 0; k < kAhead; ++k) {
+      const bool use = sp + k < nsplit;
+      const int64_t slot = chunk_slot(c, sp + k, NR) + n0;
 #pragma unroll
-      for (int k = 0; k < R; ++k) {
-        const bool use = sp + q < nsplit && n0 + k < nrows;
-        l[q][k] = use ? __ldg(a.part_lse + slot + k) : -INFINITY;
-        v[q][k] = use ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (slot + k) * kNope + d0))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < R; ++r) {
+        l[k][r] = use && n0 + r < nrows ? __ldcg(a.part_lse + slot + r) : -INFINITY;
+        v[k][r] = use && n0 + r < nrows ? __ldcg(reinterpret_cast<const float4*>(a.part_o + (slot + r) * kNope + d0))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int k = 0; k < kAhead; ++k)
 #pragma unroll
-      for (int k = 0; k < R; ++k) fold_chunk(m[k], z[k], acc[k], l[q][k], v[q][k]);
+      for (int r = 0; r < R; ++r) fold_chunk(m[r], z[r], acc[r], l[k][r], v[k][r]);
   }
 #pragma unroll
-  for (int k = 0; k < R; ++k) {
-    if (n0 + k >= nrows) break;
-    const int64_t g = g0 + n0 + k;
-    const float inv = z[k] > 0.f ? 1.f / z[k] : 0.f;
-    const float4 o = make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+  for (int r = 0; r < R; ++r) {
+    if (n0 + r >= nrows) break;
+    const int64_t g = g0 + n0 + r;
+    const float inv = z[r] > 0.f ? 1.f / z[r] : 0.f;
+    const float4 o = make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
     if (a.out_f32) {
       *reinterpret_cast<float4*>(static_cast<float*>(a.out) + g * kNope + d0) = o;
     } else {
@@ -93,7 +113,7 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
       *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + g * kNope + d0) =
           make_uint2(*reinterpret_cast<const uint32_t*>(&x), *reinterpret_cast<const uint32_t*>(&y));
     }
-    if (threadIdx.x == 0) a.lse[g] = z[k] > 0.f ? m[k] + __logf(z[k]) : -INFINITY;
+    if (threadIdx.x == 0) a.lse[g] = z[r] > 0.f ? m[r] + __logf(z[r]) : -INFINITY;
   }
 }
 

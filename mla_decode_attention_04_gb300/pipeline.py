@@ -12,7 +12,7 @@ from __future__ import annotations
 import torch
 
 from . import (KV_LORA_RANK, V_HEAD_DIM, decode_workspace_size, dcp_lse_merge, fused_workspace_size, mla_dcp_decode,
-               mla_dcp_decode_fused, mla_sparse_dcp_decode, sparse_workspace_size)
+               mla_dcp_decode_fused, mla_sparse_dcp_decode, mla_sparse_dcp_decode_fused, sparse_workspace_size)
 
 
 class DcpStep:
@@ -70,14 +70,16 @@ class DcpStep:
 
 
 class FusedDcpStep:
-    """The dense step in one decode launch over all D shards
-    (``mla_dcp_decode_fused``: the online softmax runs over shard 0's keys,
-    then shard 1's, ..., which is the LSE merge), followed, with W_UV, by the
-    projection (``dcp_lse_merge`` of the one merged result).  Same outputs as
-    ``DcpStep`` (``out``, ``lse``); no per-shard partials or counts."""
+    """The step in one decode call over all D shards, followed, with W_UV,
+    by the projection (``dcp_lse_merge`` of the one merged result).  Dense:
+    ``mla_dcp_decode_fused`` (the online softmax runs over shard 0's keys,
+    then shard 1's, ..., which is the LSE merge); sparse (``topk`` given):
+    ``mla_sparse_dcp_decode_fused`` (each token over every used entry of its
+    list).  Same outputs as ``DcpStep`` (``out``, ``lse``); no per-shard
+    partials or counts."""
 
     def __init__(self, q_nope, q_pe, shards, seq_lens, query_start_loc, max_query_len, max_seq_len, scale, w_uv=None,
-                 out_dtype=torch.bfloat16, num_splits=0):
+                 out_dtype=torch.bfloat16, num_splits=0, topk=None, topk_valid=None):
         self.q_nope, self.q_pe = q_nope, q_pe
         self.caches = [c for c, _ in shards]
         self.tables = [bt for _, bt in shards]
@@ -94,29 +96,41 @@ class FusedDcpStep:
         self.merged = (torch.empty((1, T, H, KV_LORA_RANK), dtype=torch.float32, device=dev)
                        if w_uv is not None else None)
         self.merged_lse = torch.empty((1, T, H), dtype=torch.float32, device=dev) if w_uv is not None else None
-        need = fused_workspace_size(seq_lens.shape[0], T, H, max_query_len, max_seq_len, num_splits)
+        self.topk, self.topk_valid = topk, topk_valid
+        if topk is not None:
+            need = sparse_workspace_size(T, H, topk.shape[1], self.D)
+        else:
+            need = fused_workspace_size(seq_lens.shape[0], T, H, max_query_len, max_seq_len, num_splits)
         self.workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=dev)
+
+    def decode(self, out, lse, stream=None):
+        """The fused decode call alone, into ``out`` / ``lse``."""
+        if self.topk is not None:
+            mla_sparse_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
+                                        self.topk, self.topk_valid, self.scale, out=out, lse=lse,
+                                        workspace=self.workspace, stream=stream)
+        else:
+            mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
+                                 self.max_query_len, self.max_seq_len, self.scale, out=out, lse=lse,
+                                 num_splits=self.num_splits, workspace=self.workspace, stream=stream)
 
     def run(self, stream=None):
         if self.w_uv is None:
-            mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
-                                 self.max_query_len, self.max_seq_len, self.scale, out=self.out, lse=self.lse,
-                                 num_splits=self.num_splits, workspace=self.workspace, stream=stream)
+            self.decode(self.out, self.lse, stream)
         else:
-            mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
-                                 self.max_query_len, self.max_seq_len, self.scale, out=self.merged[0],
-                                 lse=self.merged_lse[0], num_splits=self.num_splits, workspace=self.workspace,
-                                 stream=stream)
+            self.decode(self.merged[0], self.merged_lse[0], stream)
             dcp_lse_merge(self.merged, self.merged_lse, None, self.w_uv, out=self.out, lse_out=self.lse,
                           stream=stream)
         return self.out, self.lse
 
 
-def fused_step_for_workload(w, num_splits=0):
-    """FusedDcpStep for a dense ``workloads.Workload`` already on the GPU."""
+def fused_step_for_workload(w, num_splits=0, sparse=None):
+    """FusedDcpStep for a ``workloads.Workload`` already on the GPU."""
+    sparse = (w.topk is not None) if sparse is None else sparse
     shards = [(s.cache, s.block_table) for s in w.shards]
     return FusedDcpStep(w.q_nope, w.q_pe, shards, w.seq_lens, w.query_start_loc, w.max_query_len, w.max_seq_len,
-                        w.scale, w_uv=w.w_uv, num_splits=num_splits)
+                        w.scale, w_uv=w.w_uv, num_splits=num_splits, topk=w.topk if sparse else None,
+                        topk_valid=w.topk_valid if sparse else None)
 
 
 def step_for_workload(w, partial_dtype=None, num_splits=0, sparse=None):

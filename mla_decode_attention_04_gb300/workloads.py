@@ -156,7 +156,8 @@ def custom(seq_lens, q_lens, num_heads, dcp_world, page_size=64, seed=0, q_std=1
     flat = cache_all.view(-1, ROW)
     shards = []
     for r in range(D):
-        W = max(1, max(pages_per_req[r]) if B else 1)
+        # one row width for every shard's table (the fused calls take one stride)
+        W = max(1, max(max(p) for p in pages_per_req) if B else 1)
         bt = np.zeros((B, W), dtype=np.int32)
         perm = cpu_rng.permutation(num_pages[r]).astype(np.int64)
         off = 0

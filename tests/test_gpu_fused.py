@@ -92,3 +92,69 @@ def test_fused_matches_shard_calls_on_every_token():
     torch.cuda.synchronize()
     assert_out_close(to_np(fused_out), to_np(out).astype(np.float64), "fused vs shard calls")
     assert_lse_close(to_np(fused_lse), to_np(lse).astype(np.float64), "fused vs shard calls lse")
+
+
+# ------------------------------------------------------------------ sparse
+
+
+def _sparse_fused(w, out_dtype=torch.float32):
+    kept = torch.empty((w.num_tokens,), dtype=torch.int32, device="cuda")
+    out, lse, kept = mla.mla_sparse_dcp_decode_fused(w.q_nope, w.q_pe, [s.cache for s in w.shards],
+                                                     [s.block_table for s in w.shards], w.seq_lens,
+                                                     w.query_start_loc, w.topk, w.topk_valid, w.scale,
+                                                     out_dtype=out_dtype, kept_counts=kept)
+    torch.cuda.synchronize()
+    return out, lse, kept
+
+
+@pytest.mark.parametrize("H,D,K", [(16, 2, 64), (24, 3, 100), (64, 4, 256), (1, 1, 7), (32, 8, 300)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_sparse_fused_small(H, D, K, out_dtype):
+    # short valid counts and a row with none: the merged result over every
+    # shard's kept entries, and the kept count = the shard counts' sum
+    w = wl.custom([300, 90, 700, 45], [2, 1, 4, 3], H, D, page_size=16, seed=H + D + K, topk=K,
+                  short_valid_frac=0.3, force_zero_valid=1).to("cuda")
+    out, lse, kept = _sparse_fused(w, out_dtype)
+    ref = oracle_step(HostInputs(w), sparse=True)
+    assert kept.cpu().numpy().tolist() == ref["counts"].sum(axis=0).tolist()
+    assert_out_close(to_np(out), ref["merged"], "sparse fused output")
+    assert_lse_close(to_np(lse), ref["lse"], "sparse fused lse")
+
+
+def test_sparse_fused_matches_shard_calls_merged():
+    # the fused call against the D shard calls + merge on the GPU, every token
+    w = wl.custom([1200, 333, 2050, 64, 900], [1, 4, 2, 1, 3], 64, 4, page_size=64, seed=5, topk=512,
+                  short_valid_frac=0.2, force_zero_valid=1).to("cuda")
+    fused_out, fused_lse, _ = _sparse_fused(w)
+    parts = [mla.mla_sparse_dcp_decode(w.q_nope, w.q_pe, s.cache, s.block_table, w.seq_lens, w.query_start_loc,
+                                       w.topk, w.topk_valid, w.dcp_world, r, w.scale, out_dtype=torch.float32)
+             for r, s in enumerate(w.shards)]
+    out, lse = mla.dcp_lse_merge(torch.stack([p[0] for p in parts]), torch.stack([p[1] for p in parts]),
+                                 torch.stack([p[2] for p in parts]), None, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_out_close(to_np(fused_out), to_np(out).astype(np.float64), "sparse fused vs shard calls")
+    assert_lse_close(to_np(fused_lse), to_np(lse).astype(np.float64), "sparse fused vs shard calls lse")
+
+
+def test_sparse_fused_step_with_wuv():
+    w = wl.custom([300, 90, 700, 45], [2, 1, 4, 3], 64, 4, page_size=64, seed=11, topk=128, short_valid_frac=0.3,
+                  force_zero_valid=1).to("cuda")
+    step = pipeline.fused_step_for_workload(w)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    ref = oracle_step(HostInputs(w), sparse=True)
+    assert_out_close(to_np(out), ref["out"], "sparse fused W_UV output")
+    assert_lse_close(to_np(lse), ref["lse"], "sparse fused lse")
+
+
+def test_sparse_fused_benchmark_workload_sampled():
+    w = wl.NAMED["sparse_mixed"](device="cuda")
+    step = pipeline.fused_step_for_workload(w)
+    out, lse = step.run()
+    torch.cuda.synchronize()
+    rc, detail = mla.workspace_status(step.workspace)
+    assert rc == mla.MLA_OK, detail
+    tokens = _sample_tokens(w)
+    ref = oracle_step_threaded(HostInputs(w), tokens, sparse=True)
+    assert_out_close(to_np(out[tokens]), ref["out"], "sparse_mixed fused step")
+    assert_lse_close(to_np(lse[tokens]), ref["lse"], "sparse_mixed fused lse")
