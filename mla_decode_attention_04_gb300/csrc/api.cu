@@ -116,6 +116,25 @@ size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, i
 
 namespace {
 
+// The LSE merge of the chunks of the row groups a decode launch of `grid`
+// CTAs split (entries of its split table), right after it on the stream.
+cudaError_t launch_split_merge(const mla::DecodeArgs& da, int rows_per_group, int grid, int64_t num_rows,
+                               cudaStream_t st) {
+  mla::SplitMergeArgs sa{};
+  sa.split_desc = da.split_desc;
+  sa.part_lse = da.part_lse;
+  sa.part_o = da.part_o;
+  sa.rows_per_group = rows_per_group;
+  sa.grid = grid;
+  sa.num_rows = num_rows;
+  sa.out = da.out;
+  sa.out_f32 = da.out_f32;
+  sa.lse = da.lse;
+  sa.hdr = da.hdr;
+  const int blocks = grid * (rows_per_group / mla::kSplitMergeRows);
+  return mla::launch_pdl(mla::split_merge_kernel, dim3(blocks), dim3(128), 0, st, sa);
+}
+
 // The dense decode over nshard consecutive shards from rank shard0 (one
 // shard: mla_dcp_decode; all D: mla_dcp_decode_fused).  Arguments checked.
 int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
@@ -200,19 +219,8 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
     return cuda_fail(e, "decode launch");
   count_launch();
 
-  mla::SplitMergeArgs sa{};
-  sa.split_desc = da.split_desc;
-  sa.part_lse = da.part_lse;
-  sa.part_o = da.part_o;
-  sa.rows_per_group = plan.rows_per_group;
-  sa.grid = plan.grid;
-  sa.num_rows = (int64_t)num_tokens * num_heads;
-  sa.out = out;
-  sa.out_f32 = da.out_f32;
-  sa.lse = lse;
-  sa.hdr = hdr;
-  const int sm_blocks = plan.grid * (plan.rows_per_group / mla::kSplitMergeRows);
-  if ((e = mla::launch_pdl(mla::split_merge_kernel, dim3(sm_blocks), dim3(128), 0, st, sa)) != cudaSuccess)
+  if ((e = launch_split_merge(da, plan.rows_per_group, plan.grid, (int64_t)num_tokens * num_heads, st)) !=
+      cudaSuccess)
     return cuda_fail(e, "split_merge_kernel launch");
   count_launch();
   return ok();
@@ -231,7 +239,10 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   if (!topk_indices || !topk_valid) return fail(MLA_ERR_INVALID_ARG, "topk_indices and topk_valid are required");
   if (topk < 1 || topk > 65536) return fail(MLA_ERR_INVALID_ARG, "topk %d not in [1, 65536]", topk);
   if (num_tokens == 0) return ok();
-  const mla::SparsePlan plan = mla::make_sparse_plan(num_tokens, num_heads, topk);
+  if ((int64_t)num_tokens * num_heads > 0x7fffffff)
+    return fail(MLA_ERR_INVALID_ARG, "num_tokens * num_heads = %lld exceeds 2^31 - 1",
+                (long long)num_tokens * num_heads);
+  const mla::SparsePlan plan = mla::make_sparse_plan(num_tokens, num_heads, topk, current_sm_count());
   if (workspace_bytes < plan.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -262,6 +273,10 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   la.counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(ws + plan.off_cnt);
   la.tok_req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
   la.hdr = hdr;
+  la.num_heads = num_heads;
+  la.out = out;
+  la.out_f32 = out_dtype == MLA_DTYPE_F32;
+  la.lse = lse;
   if ((e = mla::launch_sparse_lists(la, st)) != cudaSuccess) return cuda_fail(e, "sparse list launch");
   count_launch();
 
@@ -294,9 +309,16 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.list_stride = topk;
   da.num_tokens = num_tokens;
   da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
-  const int grid = num_tokens * da.groups_per_token;
-  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, true, grid, current_sm_count(), st)) != cudaSuccess)
+  da.unit_penalty = mla::kUnitPenalty;
+  da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
+  da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
+  da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
+  if ((e = mla::launch_decode_tc(da, plan.rows_per_group, true, plan.grid, plan.grid, st)) != cudaSuccess)
     return cuda_fail(e, "sparse decode launch");
+  count_launch();
+  if ((e = launch_split_merge(da, plan.rows_per_group, plan.grid, (int64_t)num_tokens * num_heads, st)) !=
+      cudaSuccess)
+    return cuda_fail(e, "split_merge_kernel launch");
   count_launch();
   return ok();
 }
@@ -359,7 +381,7 @@ int mla_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, const vo
 
 size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t dcp_world) {
   (void)dcp_world;
-  return mla::make_sparse_plan(num_tokens, num_heads, topk).total;
+  return mla::make_sparse_plan(num_tokens, num_heads, topk, current_sm_count()).total;
 }
 
 int mla_sparse_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,

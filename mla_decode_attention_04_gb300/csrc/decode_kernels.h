@@ -33,6 +33,12 @@ struct SparseListArgs {
   int32_t* counts;    // [T] out: entries kept
   int32_t* tok_req;   // [T] out
   WorkspaceHeader* hdr;
+  // the final rows (o = 0, lse = -inf) of tokens that keep no entry (the
+  // decode has no unit for them)
+  int32_t num_heads;
+  void* out;  // [T, H, 512]
+  int32_t out_f32;
+  float* lse;  // [T, H]
 };
 cudaError_t launch_sparse_lists(const SparseListArgs& a, cudaStream_t stream);
 

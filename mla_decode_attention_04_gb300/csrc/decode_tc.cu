@@ -115,128 +115,130 @@ struct Unit {
   int token;  // sparse: the token
 };
 
-// The sequence of units of one CTA.  Dense: every (request, row group) pair
-// contributes unit_penalty work-free items (the cost of starting a unit)
-// followed by its 64-key tiles to one flattened list of W items; CTA c takes
-// items [c W / G, (c + 1) W / G), cut at pair boundaries.  The CTA found the
-// request holding its first item at start-up (plan_cta); the next request's
-// raw lengths are loaded one request ahead and turned into facts only when
-// the walk reaches it, so no step of the walk waits for a load.  Sparse: (token, head group) units
-// dealt round-robin.  Every role walks the same sequence.
+// What the split plan walks: requests (dense; a pair is a (request, row
+// group) over the request's key tiles on the call's shards) or tokens
+// (sparse; a pair is a (token, head group) over the token's key list).
 template <int NR, bool SPARSE>
-struct UnitIter {
-  int64_t i, hi, W, G, ib;  // dense: next item, range end, plan, item base of request b
-  int b;
-  ReqFacts cur;
-  int nq0, nq1, nL;  // query_start_loc[b + 1], [b + 2], seq_lens[b + 1]
-  int u, units;
-
-  // issues the loads of request b + 1's raw lengths (consumed one request later)
-  __device__ __forceinline__ void fetch_next(const DecodeArgs& a) {
-    nq0 = a.query_start_loc[b + 1];
-    nq1 = a.query_start_loc[b + 2];
-    nL = a.seq_lens[b + 1];
-  }
-
-  __device__ void init(const DecodeArgs& a, const TcShared& sh) {
+struct Source {
+  static __device__ __forceinline__ int count(const DecodeArgs& a) { return SPARSE ? a.num_tokens : a.num_requests; }
+  // the raw inputs of source i (dense: query_start_loc[i], [i + 1] and
+  // seq_lens[i]; sparse: the key count of token i)
+  static __device__ __forceinline__ void load(const DecodeArgs& a, int i, int& r0, int& r1, int& r2) {
     if constexpr (SPARSE) {
-      u = blockIdx.x;
-      units = a.num_tokens * a.groups_per_token;
+      r0 = a.list_count[i];
+      r1 = r2 = 0;
     } else {
-      if (sh.plan_b < 0) {
-        i = hi = 0;
-        return;
-      }
-      i = sh.plan_lo;
-      hi = sh.plan_hi;
-      W = sh.plan_W;
-      G = sh.plan_G;
-      b = sh.plan_b;
-      ib = sh.plan_ib;
-      cur = sh.plan_f;
-      if (b + 1 < a.num_requests) fetch_next(a);
+      r0 = a.query_start_loc[i];
+      r1 = a.query_start_loc[i + 1];
+      r2 = a.seq_lens[i];
     }
   }
-
-  __device__ bool next(const DecodeArgs& a, Unit& w) {
+  static __device__ __forceinline__ ReqFacts facts(const DecodeArgs& a, int i, int r0, int r1, int r2) {
     if constexpr (SPARSE) {
-      for (; u < units; u += gridDim.x) {
-        const int t = u / a.groups_per_token, g = u % a.groups_per_token;
-        w.token = t;
-        w.cta0 = -1;
-        w.b = a.tok_req[t];
-        w.row0 = g * NR;
-        w.nrows = min(NR, a.num_heads - w.row0);
-        w.key0 = 0;
-        w.key1 = a.list_count[t];
-        w.split = 0;
-        w.nsplit = 1;
-        w.q0 = t;
-        w.q_len = 1;
-        w.seq_len = 0;
-        w.local_len = w.key1;
-        w.n_kt = (w.key1 + kKeyTile - 1) / kKeyTile;
-        u += gridDim.x;
-        if (w.b >= 0) return true;
-        u -= gridDim.x;
-      }
-      return false;
+      ReqFacts f;
+      f.ok = true;
+      f.q0 = i;
+      f.q_len = 1;
+      f.seq_len = 0;
+      f.local_len = r0;  // keys in the token's list
+      f.groups = (a.num_heads + NR - 1) / NR;
+      f.nt = (r0 + kKeyTile - 1) / kKeyTile;
+      return f;
     } else {
-      const int64_t pen = a.unit_penalty;
-      while (true) {
-        if (i >= hi) return false;
-        const int64_t vlen = cur.nt > 0 ? (int64_t)cur.nt + pen : 0;
-        const int64_t rend = ib + (int64_t)cur.groups * vlen;  // end of request b's items
-        if (i >= rend) {
-          // request b is done (or owns no item): the next one
-          if (b + 1 >= a.num_requests) {
-            i = hi;
-            return false;
-          }
-          ib = rend;
-          ++b;
-          cur = request_facts_of(nq0, nq1, nL, a.num_tokens, a.num_heads, a.dcp_world, a.shard0, a.nshard, NR);
-          if (b + 1 < a.num_requests) fetch_next(a);
-          continue;
-        }
-        const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
-        const int64_t item0 = ib + (int64_t)g * vlen + pen;
-        // the range may start among the items that only carry the pair's
-        // start-up cost; a range holding none of its key tiles has no unit
-        if (i < item0) i = item0;
-        if (i >= hi) return false;
-        const int64_t end = min(hi, item0 + cur.nt);
-        w.token = -1;
-        w.b = b;
-        w.row0 = g * NR;
-        w.nrows = min(NR, cur.q_len * a.num_heads - g * NR);
-        w.t0 = (int)(i - item0);
-        w.key0 = w.t0 * kKeyTile;
-        w.key1 = (int)(end - item0) * kKeyTile;
-        w.n_kt = (int)(end - i);
-        w.cta0 = (int)range_owner(item0, W, G);
-        w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - w.cta0 + 1);
-        w.split = (int)blockIdx.x - w.cta0;  // the unit's items are this CTA's
-        w.q0 = cur.q0;
-        w.q_len = cur.q_len;
-        w.seq_len = cur.seq_len;
-        w.local_len = cur.local_len;
-        i = end;
-        return true;
-      }
+      return request_facts_of(r0, r1, r2, a.num_tokens, a.num_heads, a.dcp_world, a.shard0, a.nshard, NR);
     }
   }
 };
 
-// Dense split plan of this CTA, by all its threads before the roles start:
-// W = the list length (a block-wide sum over the requests), this CTA's range,
-// and the request holding the range's first item (published in sh).  Kept
+// The sequence of units of one CTA.  Every (source, row group) pair
+// contributes unit_penalty work-free items (the cost of starting a unit)
+// followed by its 64-key tiles to one flattened list of W items; CTA c takes
+// items [c W / G, (c + 1) W / G), cut at pair boundaries.  The CTA found the
+// source holding its first item at start-up (plan_cta); the next source's raw
+// inputs are loaded one source ahead and turned into facts only when the walk
+// reaches it, so no step of the walk waits for a load.  Every role walks the
+// same sequence.
+template <int NR, bool SPARSE>
+struct UnitIter {
+  int64_t i, hi, W, G, ib;  // next item, range end, plan, item base of source b
+  int b;
+  ReqFacts cur;
+  int n0, n1, n2;  // raw inputs of source b + 1
+
+  __device__ __forceinline__ void fetch_next(const DecodeArgs& a) { Source<NR, SPARSE>::load(a, b + 1, n0, n1, n2); }
+
+  __device__ void init(const DecodeArgs& a, const TcShared& sh) {
+    if (sh.plan_b < 0) {
+      i = hi = 0;
+      return;
+    }
+    i = sh.plan_lo;
+    hi = sh.plan_hi;
+    W = sh.plan_W;
+    G = sh.plan_G;
+    b = sh.plan_b;
+    ib = sh.plan_ib;
+    cur = sh.plan_f;
+    if (b + 1 < Source<NR, SPARSE>::count(a)) fetch_next(a);
+  }
+
+  __device__ bool next(const DecodeArgs& a, Unit& w) {
+    const int64_t pen = a.unit_penalty;
+    const int nsrc = Source<NR, SPARSE>::count(a);
+    while (true) {
+      if (i >= hi) return false;
+      const int64_t vlen = cur.nt > 0 ? (int64_t)cur.nt + pen : 0;
+      const int64_t rend = ib + (int64_t)cur.groups * vlen;  // end of source b's items
+      if (i >= rend) {
+        // source b is done (or owns no item): the next one
+        if (b + 1 >= nsrc) {
+          i = hi;
+          return false;
+        }
+        ib = rend;
+        ++b;
+        cur = Source<NR, SPARSE>::facts(a, b, n0, n1, n2);
+        if (b + 1 < nsrc) fetch_next(a);
+        continue;
+      }
+      const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
+      const int64_t item0 = ib + (int64_t)g * vlen + pen;
+      // the range may start among the items that only carry the pair's
+      // start-up cost; a range holding none of its key tiles has no unit
+      if (i < item0) i = item0;
+      if (i >= hi) return false;
+      const int64_t end = min(hi, item0 + cur.nt);
+      w.token = SPARSE ? b : -1;
+      w.b = b;
+      w.row0 = g * NR;
+      w.nrows = min(NR, cur.q_len * a.num_heads - g * NR);
+      w.t0 = (int)(i - item0);
+      w.key0 = w.t0 * kKeyTile;
+      w.key1 = (int)(end - item0) * kKeyTile;
+      if (SPARSE && w.key1 > cur.local_len) w.key1 = cur.local_len;  // the list's end
+      w.n_kt = (int)(end - i);
+      w.cta0 = (int)range_owner(item0, W, G);
+      w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - w.cta0 + 1);
+      w.split = (int)blockIdx.x - w.cta0;  // the unit's items are this CTA's
+      w.q0 = cur.q0;
+      w.q_len = cur.q_len;
+      w.seq_len = cur.seq_len;
+      w.local_len = cur.local_len;
+      i = end;
+      return true;
+    }
+  }
+};
+
+// Split plan of this CTA, by all its threads before the roles start: W =
+// the list length (a block-wide sum over the sources), this CTA's range, and
+// the source holding the range's first item (published in sh).  Kept
 // to one copy of the scan: the kernel's first instructions are fetched cold
 // while they run, so start-up code is kept short.
-template <int NR>
+template <int NR, bool SPARSE>
 __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int B = a.num_requests;
+  const int B = Source<NR, SPARSE>::count(a);
   const int64_t pen = a.unit_penalty;
   const bool single = B <= (int)blockDim.x;  // one chunk of requests: pass 0's facts stay in registers
   ReqFacts f1{};
@@ -249,9 +251,11 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
       const int b = base + tid;
       if (pass == 0 || !single) {
         f1 = ReqFacts{};
-        if (b < B)
-          f1 = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, a.num_heads, a.dcp_world, a.shard0,
-                             a.nshard, NR);
+        if (b < B) {
+          int r0, r1, r2;
+          Source<NR, SPARSE>::load(a, b, r0, r1, r2);
+          f1 = Source<NR, SPARSE>::facts(a, b, r0, r1, r2);
+        }
         // exclusive block scan of the requests' item counts
         const int64_t v = f1.nt > 0 ? (int64_t)f1.groups * ((int64_t)f1.nt + pen) : 0;
         int64_t x = v;
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (!SPARSE) plan_cta<NR>(a, sh);
+  plan_cta<NR, SPARSE>(a, sh);
   // Every role walks the same units; the first one is found here, in code
   // all warps share (a kernel's instructions are fetched cold as they first
   // run, so each role running its own copy of this step would pay for it
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       for (bool more = more0; ok && more; more = it.next(a, w)) {
         const int64_t* rows = a.key_rows + (int64_t)w.token * a.list_stride;
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-          const int k0 = kt * kKeyTile + pw * 16;
+          const int k0 = w.key0 + kt * kKeyTile + pw * 16;
           // lane l (< 16) fetches the row address of key k0 + l
           const int64_t my_row = (lane < 16 && k0 + lane < w.key1) ? rows[k0 + lane] : 0;
           if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
@@ -742,7 +746,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       w = wn;
       more = it.next(a, wn);
       auto grow = [&](int n) -> int64_t { return grow_of(w, n); };
-      const bool partial = !SPARSE && w.nsplit > 1;
+      const bool partial = w.nsplit > 1;
       // sparse: keys [0, kend) of the row's list; dense: the row's global
       // position P and the keys it sees on the current tile's shard (lim),
       // updated when the unit's tiles move to the next shard
@@ -774,7 +778,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
         int valid, tile_valid;  // keys of the tile this row sees / that exist
         if constexpr (SPARSE) {
-          const int kbase = kt * kKeyTile;
+          const int kbase = w.key0 + kt * kKeyTile;
           valid = max(0, min(kend - kbase, kKeyTile));
           tile_valid = min(w.key1 - kbase, kKeyTile);
         } else {
@@ -943,12 +947,10 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       if (partial && w.split == 0) desc = make_int4(w.nsplit, (int)grow(0), w.nrows, 0);
       named_bar_sync(1, 128);
     }
-    if constexpr (!SPARSE) {
-      // every CTA publishes its entry (zero chunks: no split pair starts
-      // here), after the wait that precedes every global write
-      grid_dep_wait();
-      if (st_tid == 0) a.split_desc[blockIdx.x] = desc;
-    }
+    // every CTA publishes its entry (zero chunks: no split pair starts
+    // here), after the wait that precedes every global write
+    grid_dep_wait();
+    if (st_tid == 0) a.split_desc[blockIdx.x] = desc;
   }
 
   // this kernel completes after the prep kernel, so kernels that wait for it

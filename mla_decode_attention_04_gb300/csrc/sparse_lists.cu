@@ -9,19 +9,30 @@
 // the shard-fused call, whose list is then every kept entry of the token and
 // whose attention over it is the merged result.  Each kept entry is resolved
 // here, once, to the address of its cache row (page = the shard's block
-// table at column slot div page_size).  One warp per token; order is kept
-// with a ballot.
+// table at column slot div page_size).
 #include "common.cuh"
 #include "decode_kernels.h"
 #include "pdl_launch.h"
 
 namespace mla {
 
-__global__ void __launch_bounds__(256) sparse_lists_kernel(SparseListArgs a) {
+// One block of 256 threads per token.  A pass covers 2048 entries: warp w
+// takes entries [256 w, 256 w + 256) of the pass in 8 rounds of 32; all
+// list entries of a thread are loaded first, then all their block-table
+// entries, so each pass costs two memory latencies whatever the list length.
+// Kept entries are compacted in list order (ballot within a warp, then the
+// warps' counts in order).
+constexpr int kListThreads = 256;
+constexpr int kListRounds = 8;
+constexpr int kListPass = kListThreads * kListRounds;  // entries per pass
+
+__global__ void __launch_bounds__(kListThreads) sparse_lists_kernel(SparseListArgs a) {
   grid_dep_sync();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= a.num_tokens) return;
+  __shared__ int s_warp[kListThreads / 32];
+  __shared__ int s_bad;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_bad = 0;
   // owning request: the largest b with query_start_loc[b] <= t
   int lo = 0, hi = a.num_requests - 1;
   while (lo < hi) {
@@ -34,50 +45,93 @@ __global__ void __launch_bounds__(256) sparse_lists_kernel(SparseListArgs a) {
   const int q_len = q1 - q0;
   int valid = a.topk_valid[t];
   valid = valid < 0 ? 0 : (valid > a.topk_k ? a.topk_k : valid);
-  int P = L - q_len + (t - q0);
+  const int P = L - q_len + (t - q0);
   if (q_len <= 0 || q_len > L || t >= q1) {
-    if (lane == 0) record_check(a.hdr, kCheckBadQueryLayout);
+    if (tid == 0) record_check(a.hdr, kCheckBadQueryLayout);
     valid = 0;
   }
   const int D = a.dcp_world, ps = a.page_size;
   const int32_t* src = a.topk + (int64_t)t * a.topk_k;
   int64_t* dst = a.key_rows + (int64_t)t * a.topk_k;
-  int count = 0;
-  bool bad = false;
-  for (int e0 = 0; e0 < valid; e0 += 32) {
-    const int e = e0 + lane;
-    const int idx = e < valid ? src[e] : -1;
-    const int k = idx >= 0 ? idx % D - a.shard0 : -1;  // shard index within the call
-    bool keep = idx >= 0 && idx <= P && k >= 0 && k < a.nshard;
-    int64_t row = 0;
-    if (keep) {
-      const int j = idx / D, col = j / ps;
-      const int32_t* bt = pick_shard(a.bts, k);
-      const int page = col < a.bt_stride ? bt[(int64_t)b * a.bt_stride + col] : -1;
-      if (page < 0 || page >= pick_shard(a.nblocks, k)) {
-        bad = true;  // the entry is dropped; the call reports check 1
-        keep = false;
-      } else {
-        row = (int64_t)reinterpret_cast<uintptr_t>(pick_shard(a.kvs, k)) +
-              ((int64_t)page * ps + j % ps) * (int64_t)(kRow * 2);
+  __syncthreads();
+  int count = 0;  // entries kept by earlier passes (the same in every thread)
+  for (int base = 0; base < valid; base += kListPass) {
+    int idx[kListRounds], k[kListRounds], page[kListRounds];
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      const int e = base + warp * (32 * kListRounds) + r * 32 + lane;
+      idx[r] = e < valid ? src[e] : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      k[r] = idx[r] >= 0 ? idx[r] % D - a.shard0 : -1;  // shard index within the call
+      const bool used = idx[r] >= 0 && idx[r] <= P && k[r] >= 0 && k[r] < a.nshard;
+      page[r] = -2;  // not used
+      if (used) {
+        const int col = (idx[r] / D) / ps;
+        page[r] = col < a.bt_stride ? pick_shard(a.bts, k[r])[(int64_t)b * a.bt_stride + col] : -1;
       }
     }
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    if (keep) dst[count + __popc(m & ((1u << lane) - 1u))] = row;
-    count += __popc(m);
+    int64_t row[kListRounds];
+    int pos[kListRounds];
+    int wcount = 0;
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r) {
+      bool keep = page[r] != -2;
+      row[r] = 0;
+      if (keep) {
+        if (page[r] < 0 || page[r] >= pick_shard(a.nblocks, k[r])) {
+          s_bad = 1;  // the entry is dropped; the call reports check 1
+          keep = false;
+        } else {
+          const int j = idx[r] / D;
+          row[r] = (int64_t)reinterpret_cast<uintptr_t>(pick_shard(a.kvs, k[r])) +
+                   ((int64_t)page[r] * ps + j % ps) * (int64_t)(kRow * 2);
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      pos[r] = keep ? wcount + __popc(m & ((1u << lane) - 1u)) : -1;
+      wcount += __popc(m);
+    }
+    if (lane == 0) s_warp[warp] = wcount;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kListThreads / 32; ++w) {
+      const int c = s_warp[w];
+      if (w < warp) before += c;
+      total += c;
+    }
+#pragma unroll
+    for (int r = 0; r < kListRounds; ++r)
+      if (pos[r] >= 0) dst[count + before + pos[r]] = row[r];
+    count += total;
+    __syncthreads();  // s_warp is reused by the next pass
   }
-  if (__any_sync(0xffffffffu, bad) && lane == 0) record_check(a.hdr, kCheckPageOutOfRange);
-  if (lane == 0) {
+  if (tid == 0) {
+    if (s_bad) record_check(a.hdr, kCheckPageOutOfRange);
     a.counts[t] = count;
     a.tok_req[t] = b;
+  }
+  if (count == 0) {
+    // no key: the token's final rows (the decode has no unit for them)
+    for (int h = warp; h < a.num_heads; h += kListThreads / 32) {
+      const int64_t grow = (int64_t)t * a.num_heads + h;
+      if (lane == 0) a.lse[grow] = -INFINITY;
+      if (a.out_f32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + grow * kNope);
+        for (int q = lane; q < kNope / 4; q += 32) o[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + grow * kNope);
+        for (int q = lane; q < kNope / 8; q += 32) o[q] = make_uint4(0, 0, 0, 0);
+      }
+    }
   }
 }
 
 cudaError_t launch_sparse_lists(const SparseListArgs& a, cudaStream_t stream) {
   if (a.num_tokens <= 0) return cudaSuccess;
-  const int warps = 8;
-  const int grid = (a.num_tokens + warps - 1) / warps;
-  return launch_pdl(sparse_lists_kernel, dim3(grid), dim3(warps * 32), 0, stream, a);
+  return launch_pdl(sparse_lists_kernel, dim3(a.num_tokens), dim3(kListThreads), 0, stream, a);
 }
 
 }  // namespace mla

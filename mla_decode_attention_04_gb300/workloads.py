@@ -269,6 +269,15 @@ def sparse_mixed(device="cpu", n_decode=96, n_prefill=4, prefill_len=64, lo=4096
     return custom(**args)
 
 
+def sparse_mixed_profile(device="cpu", **kw):
+    """The sparse + mixed recipe at a size an ncu capture replays quickly:
+    24 decode requests plus 1 chunked prefill, context ~ U[4096, 16384]
+    (cache ~0.3 GB, still larger than L2)."""
+    args = dict(n_decode=24, n_prefill=1, lo=4096, hi=16384, name="sparse_mixed_profile")
+    args.update(kw)
+    return sparse_mixed(device=device, **args)
+
+
 NAMED = {
     "tiny": tiny,
     "plain_decode_d1": lambda **kw: plain_decode(dcp_world=1, **kw),
@@ -276,4 +285,5 @@ NAMED = {
     "mtp": mtp,
     "long_context": long_context,
     "sparse_mixed": sparse_mixed,
+    "sparse_mixed_profile": sparse_mixed_profile,
 }
