@@ -527,9 +527,25 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       // consecutive 16-byte pieces: every instruction reads whole 128-byte
       // lines), so the memory system sees line-sized requests, not one
       // 16-byte request per thread and piece.
-      const int pw = warp;  // 0..3
+      const int pw = warp;            // 0..3
+      const int pt = threadIdx.x;     // 0..127
       Unit w = w0;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
+        if (w.n_kt > 0) {
+          // the unit's Q rows: one slot of the ring, a bulk copy per row half
+          // by thread r; all 128 threads arrive (the stage's full barrier
+          // counts the producer threads), thread 0 with the byte count
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
+          uint8_t* qdst = kv + stage * kStageBytes;
+          if (pt < w.nrows) {
+            const int64_t grow = (int64_t)w.token * a.num_heads + w.row0 + pt;
+            bulk_load(qdst + pt * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
+            bulk_load(qdst + pt * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage]);
+          }
+          if (pt == 0) mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
+          else mbar_arrive(&sh.full[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
         const int64_t* rows = a.key_rows + (int64_t)w.token * a.list_stride;
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
           const int k0 = w.key0 + kt * kKeyTile + pw * 16;
@@ -588,7 +604,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         // landed and the softmax has copied S(j - SB) out of that buffer.
         for (bool more = more0; ok && more; more = it.next(a, w)) {
           if (w.n_kt == 0) continue;
-          if (!SPARSE && ++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
+          if (++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
           if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
           q_ph ^= 1;
           tc_fence_after();
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         // reader, completed before the softmax saw S(j)).
         for (bool more = more0; ok && more; more = it.next(a, w)) {
           if (w.n_kt == 0) continue;
-          if (!SPARSE && ++stage == kStages) stage = 0;  // the unit's Q slot
+          if (++stage == kStages) stage = 0;  // the unit's Q slot
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
             if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
             tc_fence_after();
@@ -678,62 +694,29 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
       // (the TPR lanes of a row read the same addresses)
       const bool have = row < u.nrows;
-      if constexpr (!SPARSE) {
-        // dense: the rows are in this unit's Q slot of the ring
-        if (!group_wait(&sh.full[stage], sphase)) return false;
-        mbar_wait(&sh.full[stage], sphase);  // every reader observes the phase (returns at once)
-        const uint8_t* qrow = kv + stage * kStageBytes + row * kQRowBytes;
+      // the rows are in this unit's Q slot of the ring
+      if (!group_wait(&sh.full[stage], sphase)) return false;
+      mbar_wait(&sh.full[stage], sphase);  // every reader observes the phase (returns at once)
+      const uint8_t* qrow = kv + stage * kStageBytes + row * kQRowBytes;
 #pragma unroll 1
-        for (int c = 0; c < 9; ++c) {
-          uint32_t r[32];
+      for (int c = 0; c < 9; ++c) {
+        uint32_t r[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = have ? *reinterpret_cast<const uint4*>(qrow + c * 128 + v * 16) : make_uint4(0, 0, 0, 0);
-            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-          }
-          tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = have ? *reinterpret_cast<const uint4*>(qrow + c * 128 + v * 16) : make_uint4(0, 0, 0, 0);
+          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
         }
-        tmem_wait_st();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(1, 128);
-        if (st_tid == 0) {
-          mbar_arrive(&sh.empty[stage]);
-          mbar_arrive(&sh.q_ready);
-        }
-        if (++stage == kStages) { stage = 0; sphase ^= 1; }
-      } else {
-        const uint32_t* qn = have ? reinterpret_cast<const uint32_t*>(a.q_nope + grow_of(u, row) * a.q_nope_stride) : nullptr;
-        const uint32_t* qp = have ? reinterpret_cast<const uint32_t*>(a.q_pe + grow_of(u, row) * a.q_pe_stride) : nullptr;
-        // three 64-dim chunks per batch: all loads of a batch are in flight
-        // before its first store, so a unit pays three load latencies
-        constexpr int kQB = 3;
-#pragma unroll 1
-        for (int cb = 0; cb < 9; cb += kQB) {
-          uint4 x[8 * kQB];
-#pragma unroll
-          for (int q = 0; q < kQB; ++q) {
-            const int c = cb + q;
-            const uint4* src = reinterpret_cast<const uint4*>(c < 8 ? qn + c * 32 : qp);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) x[8 * q + v] = have ? src[v] : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int q = 0; q < kQB; ++q) {
-            uint32_t r[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              r[4 * v] = x[8 * q + v].x; r[4 * v + 1] = x[8 * q + v].y;
-              r[4 * v + 2] = x[8 * q + v].z; r[4 * v + 3] = x[8 * q + v].w;
-            }
-            tmem_st<32>(tmem + lane_base + kColQ + (cb + q) * 32, r);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_sync(1, 128);
-        if (st_tid == 0) mbar_arrive(&sh.q_ready);
+        tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
       }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (st_tid == 0) {
+        mbar_arrive(&sh.empty[stage]);
+        mbar_arrive(&sh.q_ready);
+      }
+      if (++stage == kStages) { stage = 0; sphase ^= 1; }
       return true;
     };
     Unit w, wn = w0;
