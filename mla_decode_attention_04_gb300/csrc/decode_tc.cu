@@ -438,17 +438,13 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
         return true;
       };
-      // The CTA's first unit finds every stage free: its first two key tiles
-      // go out before its Q slot is filled (the slot keeps its place in the
-      // ring), because the tiles are what the first score product waits for.
+      // The Q slot of the CTA's first unit (stage 0, free at the start) is
+      // filled by the softmax warps, so this warp goes straight to the key
+      // tiles and both start out at once.
       bool first = true;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
-        int q_stage = -1;  // deferred Q slot of the first unit
-        uint32_t q_phase = 0;
         if (w.n_kt > 0) {
           if (first) {
-            q_stage = stage;
-            q_phase = phase;
             first = false;
           } else if (!issue_q(w, stage, phase)) {
             ok = false;
@@ -514,10 +510,6 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
-          if (q_stage >= 0 && (kt == 1 || kt + 1 == w.n_kt)) {
-            if (ok && !issue_q(w, q_stage, q_phase)) ok = false;
-            q_stage = -1;
-          }
         }
       }
     } else {
@@ -724,6 +716,18 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     // the split-merge kernel: {chunks, first global row, rows, 0}
     int4 desc = make_int4(0, 0, 0, 0);
     bool more = more0;
+    if constexpr (!SPARSE) {
+      // dense: the first unit's Q slot (stage 0) is filled from here
+      if (more && wn.n_kt > 0) {
+        if (st_tid == 0) mbar_arrive_expect_tx(&sh.full[0], (uint32_t)wn.nrows * (kRow * 2));
+        if (st_tid < wn.nrows) {
+          const int64_t g = grow_of(wn, st_tid);
+          uint8_t* qdst = kv + st_tid * kQRowBytes;
+          bulk_load(qdst, a.q_nope + g * a.q_nope_stride, kNope * 2, &sh.full[0]);
+          bulk_load(qdst + kNope * 2, a.q_pe + g * a.q_pe_stride, kRope * 2, &sh.full[0]);
+        }
+      }
+    }
     if (more && wn.n_kt > 0 && !load_q(wn)) ok = false;
     while (ok && more) {
       w = wn;
