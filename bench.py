@@ -614,7 +614,7 @@ def run_profile_case(name, repeat, route="fused"):
     command the ncu summaries under profiles/ are captured from."""
     from mla_decode_attention_04_gb300 import pipeline, workloads as wl
     w = wl.NAMED[name](device="cuda")
-    fused = route == "fused" and w.topk is None
+    fused = route == "fused"
     step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
     for _ in range(repeat):
         step.run()
