@@ -188,9 +188,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   da.q_pe_stride = q_pe_row_stride;
   da.kv = static_cast<const __nv_bfloat16*>(kv_caches[0]);
-  da.num_blocks = num_blocks[0];
   da.page_size = page_size;
-  da.block_table = block_tables[0];
   da.bt_stride = block_table_stride;
   da.nshard = nshard;
   da.shard0 = shard0;
@@ -201,7 +199,6 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   }
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;
-  da.dcp_rank = shard0;
   da.scale = scale;
   da.out = out;
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
@@ -271,7 +268,6 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   la.bt_stride = block_table_stride;
   la.key_rows = reinterpret_cast<int64_t*>(ws + plan.off_lists);
   la.counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(ws + plan.off_cnt);
-  la.tok_req = reinterpret_cast<int32_t*>(ws + plan.off_tok);
   la.hdr = hdr;
   la.num_heads = num_heads;
   la.out = out;
@@ -286,9 +282,7 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   da.q_pe_stride = q_pe_row_stride;
   da.kv = static_cast<const __nv_bfloat16*>(kv_caches[0]);
-  da.num_blocks = num_blocks[0];
   da.page_size = page_size;
-  da.block_table = block_tables[0];
   da.nshard = 1;  // the key lists hold row addresses: the decode reads no shard table
   da.shard0 = shard0;
   da.kvs[0] = static_cast<const __nv_bfloat16*>(kv_caches[0]);
@@ -297,7 +291,6 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.bt_stride = block_table_stride;
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;
-  da.dcp_rank = shard0;
   da.scale = scale;
   da.out = out;
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
@@ -305,10 +298,8 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.hdr = hdr;
   da.key_rows = la.key_rows;
   da.list_count = la.counts;
-  da.tok_req = la.tok_req;
   da.list_stride = topk;
   da.num_tokens = num_tokens;
-  da.groups_per_token = (num_heads + plan.rows_per_group - 1) / plan.rows_per_group;
   da.unit_penalty = mla::kUnitPenalty;
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);

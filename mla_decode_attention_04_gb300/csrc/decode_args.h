@@ -10,10 +10,8 @@ struct DecodeArgs {
   int64_t q_nope_stride;  // elements between consecutive (token, head) rows
   const __nv_bfloat16* q_pe;
   int64_t q_pe_stride;
-  const __nv_bfloat16* kv;  // [num_blocks, page_size, 576] (sparse; dense: shard 0 of the call)
-  int64_t num_blocks;
+  const __nv_bfloat16* kv;  // shard 0's cache (sparse: the source of zero-length copies)
   int32_t page_size;
-  const int32_t* block_table;  // (sparse; dense: shard 0 of the call)
   int32_t bt_stride;
   // dense: the call covers shards shard0 .. shard0 + nshard - 1 (one shard,
   // or all D when fused); shard k's cache pages and block table
@@ -21,27 +19,25 @@ struct DecodeArgs {
   const __nv_bfloat16* kvs[kMaxShards];
   const int32_t* bts[kMaxShards];
   int64_t nblocks[kMaxShards];
-  int32_t num_heads, dcp_world, dcp_rank;
+  int32_t num_heads, dcp_world;
   float scale;
   void* out;  // [T, H, 512]
   int32_t out_f32;
   float* lse;  // [T, H]
   WorkspaceHeader* hdr;
-  // dense: the requests (every CTA derives the split plan from them)
+  // the requests (dense: every CTA derives the split plan from them)
   const int32_t* seq_lens;
   const int32_t* query_start_loc;
   int32_t num_requests;
   int32_t unit_penalty;
-  int4* split_desc;  // [grid] the split pair whose first chunk CTA c holds (SplitDesc layout)
+  int4* split_desc;  // [grid] the split pair whose first chunk CTA c holds: {chunks, first row, rows, 0}
   float* part_lse;   // [2 grid NR]
   float* part_o;     // [2 grid NR, 512]
-  // sparse
+  // sparse (the split plan's sources are the tokens)
   const int64_t* key_rows;    // [T, list_stride] cache-row addresses of each token's keys
   const int32_t* list_count;  // [T]
-  const int32_t* tok_req;     // [T] owning request
   int32_t list_stride;
   int32_t num_tokens;
-  int32_t groups_per_token;
 };
 
 }  // namespace mla

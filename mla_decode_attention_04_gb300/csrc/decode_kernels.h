@@ -31,7 +31,6 @@ struct SparseListArgs {
   int32_t page_size, bt_stride;
   int64_t* key_rows;  // [T, K] out: device addresses of the kept entries' cache rows, in list order
   int32_t* counts;    // [T] out: entries kept
-  int32_t* tok_req;   // [T] out
   WorkspaceHeader* hdr;
   // the final rows (o = 0, lse = -inf) of tokens that keep no entry (the
   // decode has no unit for them)

@@ -72,14 +72,14 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   return p;
 }
 
-// Sparse decode workspace: header, token -> request map, per-token key
-// counts (used when the caller does not ask for them), per-token lists of
+// Sparse decode workspace: header, per-token key counts (used when the
+// caller does not ask for them), per-token lists of
 // cache-row addresses, and the split table and partials of the (token, head
 // group) pairs the balanced plan cuts over CTAs (as in DecodePlan).
 struct SparsePlan {
   int32_t rows_per_group;
   int32_t grid;  // decode CTAs
-  size_t off_tok, off_cnt, off_lists, off_desc, off_plse, off_po, total;
+  size_t off_cnt, off_lists, off_desc, off_plse, off_po, total;
 };
 
 inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk, int32_t num_sms) {
@@ -88,8 +88,7 @@ inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk, int32_t n
   const size_t NR = (size_t)p.rows_per_group;
   p.grid = num_sms > 0 ? num_sms : 148;
   const size_t nt = (size_t)(T > 0 ? T : 1);
-  p.off_tok = sizeof(WorkspaceHeader);
-  p.off_cnt = align_up(p.off_tok + sizeof(int32_t) * nt, 256);
+  p.off_cnt = sizeof(WorkspaceHeader);
   p.off_lists = align_up(p.off_cnt + sizeof(int32_t) * nt, 256);
   p.off_desc = align_up(p.off_lists + sizeof(int64_t) * nt * (size_t)(topk > 0 ? topk : 1), 256);
   p.off_plse = align_up(p.off_desc + 16 * (size_t)p.grid, 256);

@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kListThreads) sparse_lists_kernel(SparseListAr
   if (tid == 0) {
     if (s_bad) record_check(a.hdr, kCheckPageOutOfRange);
     a.counts[t] = count;
-    a.tok_req[t] = b;
   }
   if (count == 0) {
     // no key: the token's final rows (the decode has no unit for them)
