@@ -144,3 +144,85 @@ def test_package_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text and "mla_oracle" not in text, f
     assert "oracle" not in sys.modules or True
+
+
+def _shard_arrays(D, nb=10, bad_shard=None, bad=None):
+    kvs = (ctypes.c_void_p * D)(*([A] * D))
+    nbs = (ctypes.c_int64 * D)(*([nb] * D))
+    bts = (ctypes.c_void_p * D)(*([A] * D))
+    if bad_shard is not None:
+        if bad == "kv":
+            kvs[bad_shard] = None
+        elif bad == "nb":
+            nbs[bad_shard] = 0
+        elif bad == "bt":
+            bts[bad_shard] = A + 2
+    return (ctypes.cast(kvs, ctypes.c_void_p), ctypes.cast(nbs, ctypes.c_void_p), ctypes.cast(bts, ctypes.c_void_p))
+
+
+def _fused(lib, D=2, T=2, wsb=1 << 30, arrays=None, **kw):
+    kvs, nbs, bts = arrays if arrays is not None else _shard_arrays(D)
+    a = dict(ps=64, kvdt=mla.MLA_DTYPE_BF16, ns=0, ws=A)
+    a.update(kw)
+    rc = lib.mla_dcp_decode_fused(A, 512, A, 64, kvs, nbs, a["ps"], a["kvdt"], bts, 4, A, A, 2, T, 16, 1, 100, D,
+                                  0.07, A, mla.MLA_DTYPE_BF16, A, a["ns"], a["ws"], wsb, None)
+    return rc, lib.mla_last_error().decode()
+
+
+def _sparse_fused(lib, D=4, T=2, wsb=1 << 30, arrays=None, **kw):
+    kvs, nbs, bts = arrays if arrays is not None else _shard_arrays(D)
+    a = dict(topk=A, K=2048, valid=A, ws=A, kept=None)
+    a.update(kw)
+    rc = lib.mla_sparse_dcp_decode_fused(A, 512, A, 64, kvs, nbs, 64, mla.MLA_DTYPE_BF16, bts, 4, A, A, 2, T, 16,
+                                         a["topk"], a["K"], a["valid"], D, 0.07, A, mla.MLA_DTYPE_BF16, A, a["kept"],
+                                         a["ws"], wsb, None)
+    return rc, lib.mla_last_error().decode()
+
+
+@pytest.mark.parametrize("call", ["dense", "sparse"])
+def test_fused_calls_check_every_shard(lib, call):
+    f = _fused if call == "dense" else _sparse_fused
+    D = 4
+    # one bad shard among good ones is caught on the host, whichever it is
+    for bad in ("kv", "nb", "bt"):
+        for r in (0, D - 1):
+            rc, msg = f(lib, D=D, arrays=_shard_arrays(D, bad_shard=r, bad=bad))
+            assert rc == mla.MLA_ERR_INVALID_ARG, (bad, r, msg)
+            assert msg
+    # at most 8 shards in one call
+    rc, msg = f(lib, D=9, arrays=_shard_arrays(9))
+    assert rc == mla.MLA_ERR_INVALID_ARG and "dcp_world" in msg
+    # the shard arrays themselves are required
+    rc, _ = f(lib, D=2, arrays=(None, None, None))
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    # no token: a successful no-op; too small a workspace: refused
+    assert f(lib, D=2, T=0)[0] == mla.MLA_OK
+    assert f(lib, D=2, wsb=64)[0] == mla.MLA_ERR_WORKSPACE
+
+
+def test_sparse_fused_argument_errors(lib):
+    assert _sparse_fused(lib, topk=None)[0] == mla.MLA_ERR_INVALID_ARG
+    assert _sparse_fused(lib, valid=None)[0] == mla.MLA_ERR_INVALID_ARG
+    assert _sparse_fused(lib, K=0)[0] == mla.MLA_ERR_INVALID_ARG
+    assert _sparse_fused(lib, K=70000)[0] == mla.MLA_ERR_INVALID_ARG
+
+
+def test_fused_dense_feature_gates(lib):
+    assert _fused(lib, kvdt=mla.MLA_DTYPE_FP8_E4M3)[0] == mla.MLA_ERR_UNSUPPORTED
+    assert _fused(lib, ps=12)[0] == mla.MLA_ERR_UNSUPPORTED
+    assert _fused(lib, ns=-1)[0] == mla.MLA_ERR_INVALID_ARG
+
+
+def test_sparse_workspace_holds_lists_and_split_partials(lib):
+    # per token the kept rows' addresses (8 bytes per entry), plus the split
+    # table and two partial slots of NR rows per CTA, whatever the tokens
+    T, H, K = 480, 64, 2048
+    size = lib.mla_sparse_dcp_decode_workspace_size(T, H, K, 4)
+    assert size >= T * K * 8
+    small = lib.mla_sparse_dcp_decode_workspace_size(1, H, K, 4)
+    assert small >= 2 * 32 * (512 * 4 + 4)  # at least one CTA's two slots of 32 fp32 rows
+    assert size - small >= (T - 1) * K * 8
+    # the fused dense call's workspace does not grow with the batch
+    a = lib.mla_dcp_decode_fused_workspace_size(64, 64, 16, 1, 4096, 0)
+    b = lib.mla_dcp_decode_fused_workspace_size(4096, 4096, 16, 1, 4096, 0)
+    assert a == b
