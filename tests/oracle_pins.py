@@ -380,9 +380,66 @@ def check_sparse_subset(lib):
                 np.testing.assert_allclose(lse[t], ref_lse[0], rtol=0, atol=1e-12)
 
 
+def two_stage_lists(w):
+    """Index lists of the two-stage decomposition: per query token, the
+    request's context [0, L - q_len) (every query row sees all of it) and its
+    q_len new positions [L - q_len, L) (a row keeps those <= its own
+    position, i.e. the causal part).  Returns (ctx, ctx_valid, new, new_valid)."""
+    L = w.seq_lens.numpy()
+    qsl = w.query_start_loc.numpy()
+    T = w.num_tokens
+    K = int(max(1, L.max()))
+    ctx = np.full((T, K), -1, np.int32)
+    new = np.full((T, K), -1, np.int32)
+    ctx_valid = np.zeros(T, np.int32)
+    new_valid = np.zeros(T, np.int32)
+    for b in range(len(L)):
+        ql = int(qsl[b + 1] - qsl[b])
+        c = int(L[b]) - ql
+        for t in range(qsl[b], qsl[b + 1]):
+            ctx[t, :c] = np.arange(c)
+            ctx_valid[t] = c
+            new[t, :ql] = np.arange(c, c + ql)
+            new_valid[t] = ql
+    return ctx, ctx_valid, new, new_valid
+
+
+def check_two_stage_decomposition(lib):
+    """A non-causal pass over the context keys plus a causal pass over the
+    q_len new keys, merged by LSE over both passes and every shard, is the
+    one-pass causal attention: the two-stage alternative to a custom mask
+    offered in the review thread of "[Attention] add DCP support for
+    FLASH_ATTN_MLA backend" (context keys with causal off, the query's own
+    keys with causal on)."""
+    for D in (1, 2, 3):
+        w = _dense_inputs([9, 14, 5, 3], [3, 4, 1, 3], H=2, D=D, seed=71 + D, ps=2, q_std=1.0)
+        ctx, ctx_valid, new, new_valid = two_stage_lists(w)
+        res = []
+        for r in range(D):
+            res.append(_run_sparse(w, r, lib, ctx, ctx_valid))
+            res.append(_run_sparse(w, r, lib, new, new_valid))
+        parts, lses, counts = [np.stack(x) for x in zip(*res)]
+        merged, mlse = oracle.lse_merge(parts, lses, counts, lib=lib)
+        ref, ref_lse = _run_dense(w, lib)
+        np.testing.assert_allclose(merged, ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(mlse, ref_lse, rtol=0, atol=1e-12)
+        # the passes split every row's visible keys: counts add up to P + 1
+        assert (counts.sum(axis=0) == [P + 1 for P in _positions(w)]).all()
+
+
+def _positions(w):
+    L = w.seq_lens.numpy()
+    qsl = w.query_start_loc.numpy()
+    out = []
+    for b in range(len(L)):
+        ql = int(qsl[b + 1] - qsl[b])
+        out += [int(L[b]) - ql + i for i in range(ql)]
+    return out
+
+
 ALL_CHECKS = [
     check_mask_tables, check_seqlen_example, check_count_closed_form, check_sdpa_d1, check_two_key_closed_form,
     check_zero_query_mean, check_identical_keys, check_paged_equals_logical, check_shard_merge_equals_unsharded,
     check_merge_lse_logsumexp, check_merge_ignores_empty_shards, check_empty_row, check_wuv_library,
-    check_wuv_commutes, check_sparse_full_prefix_is_dense, check_sparse_subset,
+    check_wuv_commutes, check_sparse_full_prefix_is_dense, check_sparse_subset, check_two_stage_decomposition,
 ]

@@ -279,3 +279,35 @@ def test_benchmark_workload_sampled(name):
                 P = L[b] - (qsl[b + 1] - qsl[b]) + i
                 for r in range(w.dcp_world):
                     assert allc[r, qsl[b] + i] == ((P - r) // w.dcp_world + 1 if P >= r else 0)
+
+
+# ------------------------------------------------ two-stage decomposition
+
+
+def test_two_stage_decomposition_on_the_gpu():
+    """A second GPU path: per shard, the sparse decode over each token's
+    context keys (every row sees them all) and over its request's q_len new
+    keys (the kernel keeps those up to the row's position), the 2 D results
+    merged by LSE, against the oracle and against the dense decode."""
+    from oracle_pins import two_stage_lists
+    w = wl.custom([700, 1300, 90, 4], [3, 4, 2, 4], 16, 2, page_size=64, seed=31).to("cuda")
+    ctx, ctx_valid, new, new_valid = [torch.from_numpy(x).to("cuda") for x in two_stage_lists(w.to("cpu"))]
+    parts, lses, counts = [], [], []
+    for r, s in enumerate(w.shards):
+        for idx, valid in ((ctx, ctx_valid), (new, new_valid)):
+            o, l, c = mla.mla_sparse_dcp_decode(w.q_nope, w.q_pe, s.cache, s.block_table, w.seq_lens,
+                                                w.query_start_loc, idx, valid, w.dcp_world, r, w.scale,
+                                                out_dtype=torch.float32)
+            parts.append(o), lses.append(l), counts.append(c)
+    out, lse = mla.dcp_lse_merge(torch.stack(parts), torch.stack(lses), torch.stack(counts), None,
+                                 out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle_step(HostInputs(w))
+    assert_out_close(to_np(out), ref["merged"], "two-stage merged output")
+    assert_lse_close(to_np(lse), ref["lse"], "two-stage merged lse")
+    dense_out, dense_lse = mla.mla_dcp_decode_fused(w.q_nope, w.q_pe, [s.cache for s in w.shards],
+                                                    [s.block_table for s in w.shards], w.seq_lens,
+                                                    w.query_start_loc, w.max_query_len, w.max_seq_len, w.scale,
+                                                    out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_out_close(to_np(out), to_np(dense_out).astype(np.float64), "two-stage vs one-pass on the GPU")
