@@ -158,3 +158,43 @@ def test_sparse_fused_benchmark_workload_sampled():
     ref = oracle_step_threaded(HostInputs(w), tokens, sparse=True)
     assert_out_close(to_np(out[tokens]), ref["out"], "sparse_mixed fused step")
     assert_lse_close(to_np(lse[tokens]), ref["lse"], "sparse_mixed fused lse")
+
+
+# ---------------------------------------------- graph replay with new lengths
+
+
+@pytest.mark.parametrize("sparse", [False, True])
+def test_graph_replays_new_lengths(sparse):
+    """The split plan is derived on the device from the lengths in memory, so
+    one captured step serves a later step whose lengths, query lengths and
+    lists differ (same buffers, same bounds): the replay equals an eager call
+    on the new inputs."""
+    kw = dict(topk=256, short_valid_frac=0.2, force_zero_valid=1) if sparse else {}
+    w = wl.custom([700, 1300, 90, 500], [3, 4, 2, 4], 32, 2, page_size=64, seed=41, with_w_uv=False, **kw).to("cuda")
+    step = pipeline.fused_step_for_workload(w)
+    step.run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step.run(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.run()
+    # the next step: shorter sequences, other query lengths (same token
+    # count), other queries; the block tables and caches stay valid
+    w.seq_lens.copy_(torch.tensor([400, 1300, 60, 9], dtype=torch.int32))
+    w.query_start_loc.copy_(torch.tensor([0, 4, 7, 10, 13], dtype=torch.int32))
+    w.q_nope.copy_(torch.randn_like(w.q_nope, dtype=torch.float32).to(torch.bfloat16) * 0.1)
+    if sparse:
+        w.topk_valid.copy_(torch.clamp(w.topk_valid, max=100))
+    g.replay()
+    torch.cuda.synchronize()
+    out_g, lse_g = step.out.clone(), step.lse.clone()
+    step.out.zero_()
+    step.run()
+    torch.cuda.synchronize()
+    rc, detail = mla.workspace_status(step.workspace)
+    assert rc == mla.MLA_OK, detail
+    assert torch.equal(out_g, step.out) and torch.equal(lse_g, step.lse)
