@@ -23,14 +23,17 @@
 // overlaps the softmax and the value product of tile j.
 //
 // Warp roles: producer (TMA tile loads through the block table; for sparse,
-// 4 warps of 16-byte cp.async row gathers), the QK^T warp (also owns TMEM),
-// four softmax warps (one per TMEM lane quarter) that also rescale O^T, zero
-// the value rows of keys past the chunk end and write the outputs (a chunk
-// of a split row group as a normalised partial with its LSE, merged by the
-// split-merge kernel that runs after this one), and the PV warp.  A 3-stage shared-memory ring of 64-key
-// tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM.  The
-// online softmax rescales O^T lazily: the running
-// reference max only moves when a tile's max exceeds it by more than 2^8.
+// 4 warps gathering whole rows with cp.async from the addresses the key-list
+// kernel resolved), the QK^T warp (also owns TMEM), four softmax warps (one
+// per TMEM lane quarter) that also rescale O^T, zero the value rows of keys
+// past the chunk end and write the outputs (a chunk of a split row group as a
+// normalised partial with its LSE, merged by the split-merge kernel that runs
+// after this one), and the PV warp.  A 3-stage shared-memory ring of 64-key
+// tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM; each
+// unit's Q rows take one ring slot ahead of its tiles.  Both variants cut the
+// work into balanced contiguous ranges of key tiles, one per CTA (the split
+// plan below).  The online softmax rescales O^T lazily: the running reference
+// max only moves when a tile's max exceeds it by more than 2^8.
 #include <string.h>
 
 #include "common.cuh"
@@ -67,7 +70,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // hi at offset 0 and lo = bf16(P - hi) at offset kPBytes.
 constexpr int kPBytes = 32 * 128;
 constexpr int kPChunk = 8;  // the k_pe chunk of a stage
-// Dense units: the unit's Q rows travel through the ring as one slot ahead of
+// A unit's Q rows travel through the ring as one slot ahead of
 // its key tiles (row r at r * kQRowBytes; the 16-byte pad puts consecutive
 // rows in different banks for the softmax warps' row reads).
 constexpr int kQRowBytes = kRow * 2 + 16;
@@ -82,7 +85,7 @@ struct TcShared {
   float alpha[32], inv_l[32];
   float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
   float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
-  // dense split plan of this CTA (written once at the start)
+  // split plan of this CTA (written once at the start)
   int64_t plan_lo, plan_hi, plan_W, plan_G, plan_ib;
   int32_t plan_b;  // request holding the range's first item, -1: no work
   ReqFacts plan_f;
