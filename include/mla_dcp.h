@@ -159,7 +159,14 @@ int mla_dcp_decode(const void *q_nope, int64_t q_nope_row_stride, const void *q_
  *  local_counts device int32 [num_tokens] (required: it is the merge's
  *               per-row valid count).
  *  Other arguments as in mla_dcp_decode.  workspace >=
- *  mla_sparse_dcp_decode_workspace_size() bytes.
+ *  mla_sparse_dcp_decode_workspace_size() bytes (per token, 8 bytes per
+ *  list entry for the resolved cache-row addresses, plus a part bounded by
+ *  the SM count).
+ *  Launches: three kernels on `stream` (the key lists: each kept entry
+ *  resolved to its cache row and counted, rows of tokens that keep none
+ *  written; the decode over balanced ranges of (token, head group) key
+ *  tiles; the LSE merge of the pairs it split).  The first waits for all
+ *  earlier work on the stream before it reads anything.
  * ---------------------------------------------------------------------- */
 size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk,
                                             int32_t dcp_world);
