@@ -13,7 +13,6 @@ import numpy as np
 import pytest
 
 
-
 def quot_floor(t, W):
     q = int(np.float32(t) * (np.float32(1.0) / np.float32(W)))
     while q > 0 and q * W > t:
