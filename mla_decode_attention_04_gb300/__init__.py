@@ -161,7 +161,8 @@ def mla_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_lo
     if row_counts is None and return_counts:
         row_counts = torch.empty((T,), dtype=torch.int32, device=dev)
     if workspace is None:  # (the library checks a given workspace's size itself)
-        workspace = torch.empty((decode_workspace_size(B, T, H, max_query_len, max_seq_len, dcp_world, num_splits),), dtype=torch.uint8, device=dev)
+        need = decode_workspace_size(B, T, H, max_query_len, max_seq_len, dcp_world, num_splits)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     _check(lib.mla_dcp_decode(_ptr(q_nope), sn, _ptr(q_pe), sp, _ptr(kv_cache), nb, ps, kv_dt, _ptr(block_table),
                               block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), B, T, H,
                               int(max_query_len), int(max_seq_len), int(dcp_world), int(dcp_rank), float(scale),
@@ -205,7 +206,8 @@ def mla_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_
     if lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     if workspace is None:  # (the library checks a given workspace's size itself)
-        workspace = torch.empty((fused_workspace_size(B, T, H, max_query_len, max_seq_len, num_splits),), dtype=torch.uint8, device=dev)
+        need = fused_workspace_size(B, T, H, max_query_len, max_seq_len, num_splits)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
     nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
     bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
@@ -250,7 +252,8 @@ def mla_sparse_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens,
     if lse is None:
         lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     if workspace is None:  # (the library checks a given workspace's size itself)
-        workspace = torch.empty((sparse_workspace_size(T, H, K, D),), dtype=torch.uint8, device=dev)
+        need = sparse_workspace_size(T, H, K, D)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
     nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
     bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
@@ -284,7 +287,8 @@ def mla_sparse_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_s
     if local_counts is None:
         local_counts = torch.empty((T,), dtype=torch.int32, device=dev)
     if workspace is None:  # (the library checks a given workspace's size itself)
-        workspace = torch.empty((sparse_workspace_size(T, H, K, dcp_world),), dtype=torch.uint8, device=dev)
+        need = sparse_workspace_size(T, H, K, dcp_world)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
     _check(lib.mla_sparse_dcp_decode(_ptr(q_nope), sn, _ptr(q_pe), sp, _ptr(kv_cache), nb, ps, kv_dt,
                                      _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc),
                                      B, T, H, _ptr(topk_indices), K, _ptr(topk_valid), int(dcp_world), int(dcp_rank),
