@@ -198,3 +198,26 @@ def test_graph_replays_new_lengths(sparse):
     rc, detail = mla.workspace_status(step.workspace)
     assert rc == mla.MLA_OK, detail
     assert torch.equal(out_g, step.out) and torch.equal(lse_g, step.lse)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_sparse_long_lists(fused):
+    # lists longer than one 2048-entry pass of the key-list kernel, page 32,
+    # a request whose prefix is shorter than the list, short and empty rows
+    w = wl.custom([6100, 700, 2600], [2, 1, 3], 24, 3, page_size=32, seed=13, topk=5000, short_valid_frac=0.3,
+                  force_zero_valid=1).to("cuda")
+    ref = oracle_step(HostInputs(w), sparse=True)
+    if fused:
+        out, lse, kept = _sparse_fused(w)
+        assert kept.cpu().numpy().tolist() == ref["counts"].sum(axis=0).tolist()
+    else:
+        parts = [mla.mla_sparse_dcp_decode(w.q_nope, w.q_pe, s.cache, s.block_table, w.seq_lens, w.query_start_loc,
+                                           w.topk, w.topk_valid, w.dcp_world, r, w.scale, out_dtype=torch.float32)
+                 for r, s in enumerate(w.shards)]
+        counts = torch.stack([p[2] for p in parts])
+        assert counts.cpu().numpy().tolist() == ref["counts"].tolist()
+        out, lse = mla.dcp_lse_merge(torch.stack([p[0] for p in parts]), torch.stack([p[1] for p in parts]), counts,
+                                     None, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    assert_out_close(to_np(out), ref["merged"], "long-list sparse output")
+    assert_lse_close(to_np(lse), ref["lse"], "long-list sparse lse")
