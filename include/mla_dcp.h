@@ -305,9 +305,12 @@ int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
  *
  *  - The array exists on every GPU that loads the library and stays
  *    allocated until the process exits.
- *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture on the device.
+ *  - The first call on a device looks up the array's device address, with
+ *    that device current, and keeps it for the device's current CUDA context
+ *    (a context created later, e.g. after cudaDeviceReset, gets a fresh
+ *    lookup).  Make that first call before any stream capture on the device.
+ *  - Arguments are checked first (errors as mla_dcp_decode); only a valid
+ *    problem can be refused for its size.
  *  - Problems whose scratch (mla_dcp_decode_workspace_size) exceeds the
  *    array are refused with MLA_ERR_WORKSPACE before anything runs.  The
  *    dense workspace is bounded by the GPU's SM count (at most 2 x SMs x 32

@@ -97,6 +97,30 @@ int check_decode_common(const void* q_nope, int64_t q_nope_row_stride, const voi
 namespace mla {
 // Lets other translation units of the library report through mla_last_error.
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// Every host-side check of an mla_dcp_decode call except those on the
+// workspace: MLA_OK, or the error the call would return (message set).
+int check_dense_decode_args(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                            const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                            const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens,
+                            int32_t num_heads, int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
+                            int32_t dcp_rank, float scale, void* out, int32_t out_dtype, float* lse,
+                            int32_t num_splits) {
+  static __align__(256) const uint8_t placeholder[1] = {0};  // stands for a workspace; never read
+  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
+                               kv_cache_dtype, block_table, block_table_stride, seq_lens, query_start_loc,
+                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                               const_cast<uint8_t*>(placeholder));
+  if (rc != MLA_OK) return rc;
+  (void)max_query_len;
+  if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
+    return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
+  if ((int64_t)num_tokens * num_heads > 0x7fffffff)
+    return fail(MLA_ERR_INVALID_ARG, "num_tokens * num_heads = %lld exceeds 2^31 - 1",
+                (long long)num_tokens * num_heads);
+  return MLA_OK;
+}
 }  // namespace mla
 
 extern "C" {

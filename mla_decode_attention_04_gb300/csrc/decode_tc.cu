@@ -49,42 +49,65 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
 constexpr int kChunk = 64 * 128;        // one 64-key x 64-dim bf16 tile, SW128
 constexpr int kStageBytes = 9 * kChunk;  // 576 dims
-constexpr int kColQ = 0;                 // TMEM columns: Q [0, 288)
-constexpr int kColS = 288;               //               S buffers [288, 288 + 64 SBUF)
-// S is double-buffered when TMEM has room (NR = 16: 288 + 2*64 + 4*16 = 480
-// columns), so QK^T of tile j+1 runs while the softmax reads S of tile j.
+constexpr int kColQ = 0;                 // TMEM columns: Q first
+// Where a unit's operands live, by rows per unit NR.
+//  * NR = 16, 32: Q in TMEM (9 chunks of 64 dims = 288 columns), S after it;
+//    S double-buffered when TMEM has room (NR = 16: 288 + 2*64 + 4*16 = 480
+//    columns), so QK^T of tile j+1 runs while the softmax reads S of tile j.
+//  * NR = 64: O^T takes 4*64 = 256 columns, so Q's first 3 chunks (dims
+//    0-191) are a shared-memory operand (each row twice: TMEM lanes l and
+//    l + 64 hold the same row) and only chunks 3-8 sit in TMEM (192
+//    columns); S gets the remaining 64.  Shared memory then holds 2 ring
+//    stages (not 3) next to the 48 KB of Q and a separate P lo buffer.
 template <int NR> struct TmemPlan {
+  static constexpr int kQSmemChunks = NR == 64 ? 3 : 0;
+  static constexpr int kColS = kColQ + (9 - kQSmemChunks) * 32;  // S buffers [kColS, kColS + 64 SBUF)
   static constexpr int kSBufs = NR == 16 ? 2 : 1;
   static constexpr int kColO = kColS + kSBufs * 64;  // O^T [kColO, kColO + 4 NR)
   static_assert(kColO + 4 * NR <= 512, "TMEM budget");
+};
+template <int NR> struct Pipe {
+  static constexpr int kStages = NR == 64 ? 2 : 3;
+  // a unit's Q rows travel through one ring slot, row r at r * kQRowBytes:
+  // with room to spare, a 16-byte pad puts consecutive rows in different
+  // banks for the softmax warps' row reads (64 padded rows would not fit)
+  static constexpr int kQRowBytes = NR == 64 ? kRow * 2 : kRow * 2 + 16;
+  static_assert(NR * kQRowBytes <= kStageBytes, "Q slot");
+  static constexpr int kQSmemBytes = TmemPlan<NR>::kQSmemChunks * 128 * 128;  // [chunk][128 rows][128 B]
+  static constexpr int kPBytes = NR * 128;  // P^T (NR rows x 64 keys bf16, SW128 K-major)
+  // P lo sits next to P hi in the stage's k_pe chunk when both fit (8 KB),
+  // else in a buffer of its own per stage
+  static constexpr bool kPLoInChunk = 2 * kPBytes <= kChunk;
+  static constexpr int kPLoBytes = kPLoInChunk ? 0 : kStages * kPBytes;
+  static constexpr int kOffQSmem = kStages * kStageBytes;
+  static constexpr int kOffPLo = kOffQSmem + kQSmemBytes;
+  static constexpr int kOffShared = kOffPLo + kPLoBytes;
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// P^T (up to 32 rows x 64 keys, bf16, SW128 K-major) lives in the k_pe chunk
-// of the tile's own stage, free once QK^T of the tile is done: P as bf16
-// hi at offset 0 and lo = bf16(P - hi) at offset kPBytes.
-constexpr int kPBytes = 32 * 128;
+// P^T (NR rows x 64 keys, bf16, SW128 K-major) lives in the k_pe chunk of
+// the tile's own stage, free once QK^T of the tile is done: P as bf16 hi at
+// offset 0, and for fp32 outputs lo = bf16(P - hi) at offset kPBytes (NR <=
+// 32) or in the stage's P lo buffer (NR = 64).
 constexpr int kPChunk = 8;  // the k_pe chunk of a stage
-// A unit's Q rows travel through the ring as one slot ahead of
-// its key tiles (row r at r * kQRowBytes; the 16-byte pad puts consecutive
-// rows in different banks for the softmax warps' row reads).
-constexpr int kQRowBytes = kRow * 2 + 16;
+constexpr int kMaxStages = 3;
 
 struct TcShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
-  float alpha[32], inv_l[32];
-  float red[2][8][32];  // per-tile partial row maxima [tile parity][key slice][row]
-  float lpart[8][32];   // partial row sums at the epilogue [key slice][row]
+  float alpha[64], inv_l[64];
+  // per-tile partial row maxima [tile parity][key slice * NR + row] (the
+  // 128 TMEM lanes hold 128 / NR key slices of each of the NR rows)
+  float red[2][128];
+  float lpart[128];  // partial row sums at the epilogue [key slice * NR + row]
   // split plan of this CTA (written once at the start)
   int64_t plan_lo, plan_hi, plan_W, plan_G, plan_ib;
   int32_t plan_b;  // request holding the range's first item, -1: no work

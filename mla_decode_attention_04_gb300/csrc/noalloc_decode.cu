@@ -15,6 +15,7 @@
 // on one stream, or otherwise ordered, are fine.  The array keeps the last
 // call's contents; the decode clears what must start at zero (its status word)
 // at the start of every call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -26,13 +27,45 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_static_scratch[MLA_STATIC_SCRATCH_BYTES];
 
+// The array's device address, looked up once per CUDA context.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, with the device current.  A context is identified
+// by its driver-assigned unique id, so a context created after a
+// cudaDeviceReset (which unloads the module and frees the array) gets a
+// fresh lookup instead of a dangling address.
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext*);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long*);
+
+void* driver_entry(const char* name, unsigned version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return p;
+}
+
+// Unique id of the current context (0 if there is none yet).
+unsigned long long current_context_id() {
+  static PfnCtxGetCurrent get_current = reinterpret_cast<PfnCtxGetCurrent>(driver_entry("cuCtxGetCurrent", 4000));
+  static PfnCtxGetId get_id = reinterpret_cast<PfnCtxGetId>(driver_entry("cuCtxGetId", 12000));
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the array in the current context of the current device.
 cudaError_t static_scratch_address(void** out, int* device) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -40,13 +73,17 @@ cudaError_t static_scratch_address(void** out, int* device) {
   *device = dev;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+  const unsigned long long id = current_context_id();
+  if (id != 0 && g_scratch[dev].addr != nullptr && g_scratch[dev].ctx_id == id) {
+    *out = g_scratch[dev].addr;
+    return cudaSuccess;
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);  // also makes the device's primary context current
+  if (e != cudaSuccess) return e;
+  g_scratch[dev].addr = p;
+  g_scratch[dev].ctx_id = current_context_id();
+  *out = p;
   return cudaSuccess;
 }
 
@@ -54,7 +91,14 @@ cudaError_t static_scratch_address(void** out, int* device) {
 
 namespace mla {
 int set_last_error(int code, const char* msg);
-}
+int check_dense_decode_args(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                            const void* kv_cache, int64_t num_blocks, int32_t page_size, int32_t kv_cache_dtype,
+                            const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens,
+                            int32_t num_heads, int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
+                            int32_t dcp_rank, float scale, void* out, int32_t out_dtype, float* lse,
+                            int32_t num_splits);
+}  // namespace mla
 
 extern "C" int mla_dcp_decode_static_scratch(
     const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride, const void* kv_cache,
@@ -63,6 +107,13 @@ extern "C" int mla_dcp_decode_static_scratch(
     int32_t num_tokens, int32_t num_heads, int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
     int32_t dcp_rank, float scale, void* out, int32_t out_dtype, float* lse, int32_t* row_counts,
     int32_t num_splits, void* stream) {
+  // argument errors first, reported as such (not as a scratch shortfall)
+  const int rc = mla::check_dense_decode_args(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks,
+                                              page_size, kv_cache_dtype, block_table, block_table_stride, seq_lens,
+                                              query_start_loc, num_requests, num_tokens, num_heads, max_query_len,
+                                              max_seq_len, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                                              num_splits);
+  if (rc != MLA_OK) return rc;
   const size_t need = mla_dcp_decode_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len,
                                                     dcp_world, num_splits);
   if (need > (size_t)MLA_STATIC_SCRATCH_BYTES) {

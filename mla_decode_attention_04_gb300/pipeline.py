@@ -97,6 +97,8 @@ class FusedDcpStep:
                        if w_uv is not None else None)
         self.merged_lse = torch.empty((1, T, H), dtype=torch.float32, device=dev) if w_uv is not None else None
         self.topk, self.topk_valid = topk, topk_valid
+        # sparse: an int32 [T] tensor here receives each token's used-entry count
+        self.kept_counts = None
         if topk is not None:
             need = sparse_workspace_size(T, H, topk.shape[1], self.D)
         else:
@@ -108,7 +110,7 @@ class FusedDcpStep:
         if self.topk is not None:
             mla_sparse_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
                                         self.topk, self.topk_valid, self.scale, out=out, lse=lse,
-                                        workspace=self.workspace, stream=stream)
+                                        kept_counts=self.kept_counts, workspace=self.workspace, stream=stream)
         else:
             mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
                                  self.max_query_len, self.max_seq_len, self.scale, out=out, lse=lse,

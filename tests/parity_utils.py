@@ -81,6 +81,20 @@ def oracle_step_threaded(h: HostInputs, tokens, sparse=False, threads=None):
     return out
 
 
+_WORKLOAD_REFS = {}
+
+
+def oracle_workload(name, w):
+    """The oracle on every token of a named benchmark workload: each shard's
+    (partial, lse, count) and the merged (and W_UV-projected) result.  The
+    workloads are seeded, so the result is kept per name for the tests of
+    both routes in one process."""
+    if name not in _WORKLOAD_REFS:
+        ref = oracle_step_threaded(HostInputs(w), range(w.num_tokens), sparse=w.topk is not None)
+        _WORKLOAD_REFS[name] = ref
+    return _WORKLOAD_REFS[name]
+
+
 def assert_out_close(got, ref, what=""):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

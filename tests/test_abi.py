@@ -226,3 +226,22 @@ def test_sparse_workspace_holds_lists_and_split_partials(lib):
     a = lib.mla_dcp_decode_fused_workspace_size(64, 64, 16, 1, 4096, 0)
     b = lib.mla_dcp_decode_fused_workspace_size(4096, 4096, 16, 1, 4096, 0)
     assert a == b
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=0), mla.MLA_ERR_INVALID_ARG),
+    (dict(T=-1), mla.MLA_ERR_INVALID_ARG),
+    (dict(r=2), mla.MLA_ERR_INVALID_ARG),
+    (dict(ms=-5), mla.MLA_ERR_INVALID_ARG),
+    (dict(kvdt=7), mla.MLA_ERR_UNSUPPORTED),
+])
+def test_static_scratch_reports_argument_errors_before_sizing(lib, kw, code):
+    """The allocation-free variant checks its arguments before it compares the
+    problem's scratch with its array, so a bad size is an argument error, not
+    a scratch shortfall (and nothing reaches the GPU)."""
+    a = dict(H=16, T=2, r=0, ms=100, kvdt=mla.MLA_DTYPE_BF16)
+    a.update(kw)
+    rc = lib.mla_dcp_decode_static_scratch(A, 512, A, 64, A, 10, 64, a["kvdt"], A, 4, A, A, 2, a["T"], a["H"], 1,
+                                           a["ms"], 2, a["r"], ctypes.c_float(0.07), A, mla.MLA_DTYPE_BF16, A, None, 0,
+                                           None)
+    assert rc == code, lib.mla_last_error().decode()

@@ -11,8 +11,8 @@ import torch
 import mla_decode_attention_04_gb300 as mla
 from mla_decode_attention_04_gb300 import build as mla_build
 from mla_decode_attention_04_gb300 import pipeline, workloads as wl
-from parity_utils import HostInputs, assert_lse_close, assert_out_close, oracle_step, oracle_step_threaded, to_np
-from test_gpu_parity import EDGE, _sample_tokens
+from parity_utils import HostInputs, assert_lse_close, assert_out_close, oracle_step, oracle_workload, to_np
+from test_gpu_parity import EDGE
 
 pytestmark = pytest.mark.gpu
 
@@ -70,17 +70,18 @@ def test_fused_needs_one_cache_and_table_per_shard():
 
 
 @pytest.mark.parametrize("name", ["plain_decode_d1", "plain_decode_d2", "mtp", "long_context"])
-def test_fused_benchmark_workload_sampled(name):
+def test_fused_benchmark_workload_every_token(name):
+    """The benchmarked shard-fused step at full size against the oracle's
+    merged (W_UV-projected) result on every token."""
     w = wl.NAMED[name](device="cuda")
     step = pipeline.fused_step_for_workload(w)
     out, lse = step.run()
     torch.cuda.synchronize()
     rc, detail = mla.workspace_status(step.workspace)
     assert rc == mla.MLA_OK, detail
-    tokens = _sample_tokens(w)
-    ref = oracle_step_threaded(HostInputs(w), tokens)
-    assert_out_close(to_np(out[tokens]), ref["out"], f"{name} fused step")
-    assert_lse_close(to_np(lse[tokens]), ref["lse"], f"{name} fused lse")
+    ref = oracle_workload(name, w)
+    assert_out_close(to_np(out), ref["out"], f"{name} fused step")
+    assert_lse_close(to_np(lse), ref["lse"], f"{name} fused lse")
 
 
 def test_fused_matches_shard_calls_on_every_token():
@@ -147,17 +148,21 @@ def test_sparse_fused_step_with_wuv():
     assert_lse_close(to_np(lse), ref["lse"], "sparse fused lse")
 
 
-def test_sparse_fused_benchmark_workload_sampled():
+def test_sparse_fused_benchmark_workload_every_token():
+    """The benchmarked sparse shard-fused step at full size against the
+    oracle on every token, kept counts (the shard counts' sum) bit-exact."""
     w = wl.NAMED["sparse_mixed"](device="cuda")
     step = pipeline.fused_step_for_workload(w)
+    kept = torch.empty((w.num_tokens,), dtype=torch.int32, device="cuda")
+    step.kept_counts = kept
     out, lse = step.run()
     torch.cuda.synchronize()
     rc, detail = mla.workspace_status(step.workspace)
     assert rc == mla.MLA_OK, detail
-    tokens = _sample_tokens(w)
-    ref = oracle_step_threaded(HostInputs(w), tokens, sparse=True)
-    assert_out_close(to_np(out[tokens]), ref["out"], "sparse_mixed fused step")
-    assert_lse_close(to_np(lse[tokens]), ref["lse"], "sparse_mixed fused lse")
+    ref = oracle_workload("sparse_mixed", w)
+    assert kept.cpu().numpy().tolist() == ref["counts"].sum(axis=0).tolist()
+    assert_out_close(to_np(out), ref["out"], "sparse_mixed fused step")
+    assert_lse_close(to_np(lse), ref["lse"], "sparse_mixed fused lse")
 
 
 # ---------------------------------------------- graph replay with new lengths

@@ -1,9 +1,9 @@
 """GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
 
 Counts bit-exact; outputs within 1e-2 + 2e-2*|ref| element-wise; LSE within
-1e-3 (see parity_utils).  Small cases compare every element; the benchmark
-workloads at full size compare sampled tokens computed one by one by the
-oracle, in the launch configuration the benchmark times.
+1e-3 (see parity_utils).  Every case compares every element, the benchmark
+workloads at full size included (in the launch configuration the benchmark
+times).
 """
 import math
 
@@ -16,7 +16,7 @@ from mla_decode_attention_04_gb300 import build as mla_build
 from mla_decode_attention_04_gb300 import pipeline
 from mla_decode_attention_04_gb300 import workloads as wl
 from parity_utils import (HostInputs, assert_lse_close, assert_out_close, oracle_shard, oracle_step,
-                          oracle_step_threaded, to_np)
+                          oracle_workload, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -239,46 +239,25 @@ def test_graph_replay_matches_eager():
 # ------------------------------------------------- benchmark workloads, full size
 
 
-def _sample_tokens(w, n_random=6):
-    T = w.num_tokens
-    rng = np.random.default_rng(123)
-    picks = {0, 1, T - 2, T - 1}
-    picks |= set(rng.choice(T, size=min(n_random, T), replace=False).tolist())
-    if w.topk_valid is not None:
-        v = w.topk_valid.cpu().numpy()
-        picks |= set(np.flatnonzero(v == 0)[:2].tolist())
-        picks |= set(np.flatnonzero((v > 0) & (v < w.topk.shape[1]))[:2].tolist())
-    return sorted(t for t in picks if 0 <= t < T)
-
-
 @pytest.mark.parametrize("name", ["plain_decode_d1", "plain_decode_d2", "mtp", "long_context", "sparse_mixed"])
-def test_benchmark_workload_sampled(name):
+def test_benchmark_workload_every_token(name):
+    """The D shard calls + merge of a benchmark workload at full size, in the
+    launch configuration the benchmark times, against the oracle on every
+    token: each shard's partials, LSEs and counts (bit-exact), and the merged
+    (W_UV-projected) result."""
     w = wl.NAMED[name](device="cuda")
     step = pipeline.step_for_workload(w)
     out, lse = step.run()
     torch.cuda.synchronize()
     rc, detail = mla.workspace_status(step.workspace)
     assert rc == mla.MLA_OK, detail
-    tokens = _sample_tokens(w)
-    sparse = w.topk is not None
-    ref = oracle_step_threaded(HostInputs(w), tokens, sparse=sparse)
-    got_counts = step.counts.cpu().numpy()[:, tokens]
-    assert got_counts.tolist() == ref["counts"].tolist()
+    ref = oracle_workload(name, w)
+    assert step.counts.cpu().numpy().tolist() == ref["counts"].tolist(), f"{name} counts"
     for r in range(w.dcp_world):
-        assert_out_close(to_np(step.partials[r][tokens]), ref["parts"][r], f"{name} shard {r}")
-        assert_lse_close(to_np(step.lses[r][tokens]), ref["lses"][r], f"{name} shard {r} lse")
-    assert_out_close(to_np(out[tokens]), ref["out"], f"{name} merged")
-    assert_lse_close(to_np(lse[tokens]), ref["lse"], f"{name} merged lse")
-    if not sparse:
-        # every token's counts: the closed form of the visible prefix (cheap on the host)
-        L = w.seq_lens.cpu().numpy()
-        qsl = w.query_start_loc.cpu().numpy()
-        allc = step.counts.cpu().numpy()
-        for b in range(len(L)):
-            for i in range(qsl[b + 1] - qsl[b]):
-                P = L[b] - (qsl[b + 1] - qsl[b]) + i
-                for r in range(w.dcp_world):
-                    assert allc[r, qsl[b] + i] == ((P - r) // w.dcp_world + 1 if P >= r else 0)
+        assert_out_close(to_np(step.partials[r]), ref["parts"][r], f"{name} shard {r}")
+        assert_lse_close(to_np(step.lses[r]), ref["lses"][r], f"{name} shard {r} lse")
+    assert_out_close(to_np(out), ref["out"], f"{name} merged")
+    assert_lse_close(to_np(lse), ref["lse"], f"{name} merged lse")
 
 
 # ------------------------------------------------ two-stage decomposition

@@ -4,8 +4,10 @@ mla_dcp_decode_static_scratch takes no workspace: its scratch is a fixed
 device array inside the library.  This file is collected last so that a run
 stopping at the first failure has already run every other test.  It checks,
 through the C ABI, two calls in a row against mla_dcp_decode with a caller
-workspace (same tolerance as the other parity tests), and that a problem
-whose scratch would not fit the array is refused before anything runs.
+workspace (same tolerance as the other parity tests), two calls on
+different problems issued back to back on one stream with no synchronise in
+between, and that a problem whose scratch would not fit the array is
+refused before anything runs.
 """
 import ctypes
 
@@ -64,6 +66,31 @@ def test_static_scratch_matches_workspace_entry_point(lib, name):
             assert torch.equal(cnt, ref_cnt)
             assert_out_close(to_np(out), to_np(ref_out).astype(np.float64), f"{name} shard {r}")
             assert_lse_close(to_np(lse), to_np(ref_lse).astype(np.float64), f"{name} shard {r} lse")
+
+
+def test_static_scratch_back_to_back_on_one_stream(lib):
+    """Calls on one stream are ordered, so consecutive calls may share the
+    array: two different problems, launched back to back without a
+    synchronise, each match the workspace entry point."""
+    cases = [wl.tiny().to("cuda"), wl.mtp(device="cuda", batch=16)]
+    refs, outs = [], []
+    for w in cases:
+        s = w.shards[1]
+        refs.append(mla.mla_dcp_decode(w.q_nope, w.q_pe, s.cache, s.block_table, w.seq_lens, w.query_start_loc,
+                                       w.max_query_len, w.max_seq_len, w.dcp_world, 1, w.scale,
+                                       out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    for w, (ro, rl, rc) in zip(cases, refs):
+        o = torch.full_like(ro, float("nan"))
+        l = torch.full_like(rl, float("nan"))
+        c = torch.full_like(rc, -1)
+        assert _call_static(lib, w, 1, o, l, c) == mla.MLA_OK, lib.mla_last_error().decode()
+        outs.append((o, l, c))
+    torch.cuda.synchronize()
+    for (ro, rl, rc), (o, l, c) in zip(refs, outs):
+        assert torch.equal(c, rc)
+        assert_out_close(to_np(o), to_np(ro).astype(np.float64), "back-to-back static call")
+        assert_lse_close(to_np(l), to_np(rl).astype(np.float64), "back-to-back static call lse")
 
 
 def test_static_scratch_refuses_oversized_problems(lib):
