@@ -113,7 +113,7 @@ const char *mla_last_error(void);
  *           chunks per request (fix it for CUDA-graph capture).
  *  workspace   device scratch of at least mla_dcp_decode_workspace_size()
  *           bytes, 256-byte aligned; contents need not be initialised.  Its
- *           size is bounded by the GPU's SM count (two slots of up to 32
+ *           size is bounded by the GPU's SM count (two slots of up to 64
  *           partial rows per SM), not by the batch.
  *  Stream order: every kernel of this library writes nothing before all
  *  earlier work on the stream has finished, but this call starts reading its
@@ -313,9 +313,11 @@ int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
  *    problem can be refused for its size.
  *  - Problems whose scratch (mla_dcp_decode_workspace_size) exceeds the
  *    array are refused with MLA_ERR_WORKSPACE before anything runs.  The
- *    dense workspace is bounded by the GPU's SM count (at most 2 x SMs x 32
- *    partial rows of 2 KB plus small tables), so on a 152-SM GB300 every
- *    problem fits.
+ *    dense workspace is bounded by the GPU's SM count: 2 partial slots of
+ *    16, 32 or 64 rows of 2 KB per SM (the rows per work unit grow with
+ *    max_query_len x num_heads: up to 16, 32, then 64) plus small tables.
+ *    On a 152-SM GB300, problems of up to 32 rows per request fit; those
+ *    with more (about 40 MB) are refused.
  *  - Every call shares the one array: calls that may overlap on the GPU
  *    (unordered streams) race on it.  Calls on one stream are fine.  The
  *    array keeps the last call's contents; what must start at zero (the

@@ -7,14 +7,18 @@
 // per-token key lists of sparse MLA.
 //
 // One CTA per SM walks work units (request or token, row group, KV chunk).
-// A unit's NR rows (NR = 16 or 32 (token, head) pairs) share every key, so
-// per 64-key tile:
-//   S  [128 lanes x 64]  = Q (TMEM, rows padded to 128 lanes) . KV^T   (K = 576)
+// A unit's NR rows (NR = 16, 32 or 64 (token, head) pairs) share every key,
+// so per 64-key tile:
+//   S  [128 lanes x 64]  = Q (rows repeated to 128 lanes) . KV^T       (K = 576)
 //   O^T[512 x NR]       += KV_c^T (smem, MN-major) . P^T (smem)        (K = 64)
 // The first product keeps the 64 keys on the MMA's N side, the second puts
 // the 512 latent dims on M and the few rows on N, so neither wastes the
 // tensor core on padding for the value product and O^T only needs 4*NR TMEM
-// columns next to Q (288) and S (64).  For fp32 outputs P enters the value
+// columns next to Q and S (64).  Q sits in TMEM (288 columns) for NR <= 32;
+// for NR = 64 its first 192 dims are a shared-memory operand, loaded by TMA
+// like a key tile, so that O^T (256 columns) fits.  Bigger units read each
+// key tile for more rows: a 64-row unit covers a token of 64 heads, or a
+// quarter of a 2-token, 128-head request.  For fp32 outputs P enters the value
 // product as two bf16 terms (hi + lo, both accumulated into O^T), so the
 // probabilities keep fp32-level precision; for bf16 outputs one bf16 term.
 // QK^T and PV are issued by two threads in different warps (one thread
@@ -29,8 +33,8 @@
 // past the chunk end and write the outputs (a chunk of a split row group as a
 // normalised partial with its LSE, merged by the split-merge kernel that runs
 // after this one), and the PV warp.  A 3-stage shared-memory ring of 64-key
-// tiles (72 KB each) keeps up to 216 KB of KV loads in flight per SM; each
-// unit's Q rows take one ring slot ahead of its tiles.  Both variants cut the
+// tiles (72 KB each; 2 stages for NR = 64) keeps up to 216 KB of KV loads in
+// flight per SM; each unit's Q rows take one ring slot ahead of its tiles.  Both variants cut the
 // work into balanced contiguous ranges of key tiles, one per CTA (the split
 // plan below).  The online softmax rescales O^T lazily: the running reference
 // max only moves when a tile's max exceeds it by more than 2^8.
@@ -122,9 +126,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-template <bool SPARSE>
+template <bool SPARSE, int NR>
 struct Roles {
-  static constexpr int kProducerWarps = SPARSE ? 4 : 1;
+  // sparse: warps gathering key rows (2 for 64-row units, whose softmax
+  // needs the registers a 4-warp CTA could not give it)
+  static constexpr int kProducerWarps = SPARSE ? (NR == 64 ? 2 : 4) : 1;
   static constexpr int kMmaWarp = kProducerWarps;          // issues QK^T (and owns TMEM)
   static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;  // four consecutive warps
   static constexpr int kPvWarp = kProducerWarps + 5;        // issues PV
@@ -330,20 +336,20 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   __syncthreads();
 }
 
-// The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T.  The
-// first tile of a unit overwrites O^T; the P split (hi + lo, for fp32
-// outputs) doubles the MMAs.  One rolled copy: the issue rate of a thread,
+// The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T (P^T
+// hi and lo at descriptors p_hi, p_lo).  The first tile of a unit overwrites
+// O^T; the P split (hi + lo, for fp32 outputs) doubles the MMAs.  One rolled copy: the issue rate of a thread,
 // not the loop, bounds it.
 template <int NR>
-__device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p0, uint32_t id_pv, bool first,
-                                              bool split) {
+__device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p_hi, uint64_t p_lo, uint32_t id_pv,
+                                              bool first, bool split) {
 #pragma unroll 1
   for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
-      mma_ss(o0 + m * NR, va, p0 + (uint64_t)(kk * 2), id_pv, (first && kk == 0) ? 0u : 1u);
-      if (split) mma_ss(o0 + m * NR, va, p0 + (uint64_t)((kPBytes >> 4) + kk * 2), id_pv, 1u);
+      mma_ss(o0 + m * NR, va, p_hi + (uint64_t)(kk * 2), id_pv, (first && kk == 0) ? 0u : 1u);
+      if (split) mma_ss(o0 + m * NR, va, p_lo + (uint64_t)(kk * 2), id_pv, 1u);
     }
 }
 
@@ -353,10 +359,24 @@ struct TileLoc {
   int32_t k, lt, Lr;
 };
 
-// The dense call's cache tensor maps, one per shard it covers.
+// The cache tensor maps of a dense call, one per shard it covers, and (units
+// of 64 rows) the queries' maps.
 struct KvMaps {
   CUtensorMap m[kMaxShards];
+  CUtensorMap q_nope, q_pe;  // [T H rows][512 | 64 dims] bf16, box 64 rows x 64 dims, 128-byte swizzle
 };
+
+// A 64-row unit's Q rows [grow0, grow0 + 64) as 9 TMA tiles of 64 rows x 64
+// dims (128-byte swizzle; rows past the last (token, head) read as zero)
+// into one ring slot, chunk c at c * kChunk: the layout of a key tile.
+template <int NR>
+__device__ __forceinline__ void issue_q_tma(const KvMaps& maps, uint8_t* dst, int64_t grow0, uint64_t* bar) {
+  const uint64_t pol = policy_evict_first();
+  mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) tma_load_3d(dst + c * kChunk, &maps.q_nope, c * 64, (int32_t)grow0, 0, bar, pol);
+  tma_load_3d(dst + 8 * kChunk, &maps.q_pe, 0, (int32_t)grow0, 0, bar, pol);
+}
 
 // Address of shard k's map in the kernel's parameter space (static indices).
 __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int k) {
@@ -373,13 +393,18 @@ __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int 
 }
 
 template <int NR, bool SPARSE, bool FUSED>
-__global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ KvMaps maps, const __grid_constant__ DecodeArgs a) {
-  using R = Roles<SPARSE>;
+  using R = Roles<SPARSE, NR>;
+  using PP = Pipe<NR>;
+  using TP = TmemPlan<NR>;
+  constexpr int kStages = PP::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* kv = base;                                  // [kStages][9][kChunk]
-  TcShared& sh = *reinterpret_cast<TcShared*>(base + kStages * kStageBytes);
+  uint8_t* kv = base;                           // [kStages][9][kChunk]
+  uint8_t* q_smem = base + PP::kOffQSmem;       // NR = 64: Q chunks 0-2 as the QK^T A operand [3][128 rows][128 B]
+  uint8_t* p_lo_buf = base + PP::kOffPLo;       // NR = 64: P lo per stage
+  TcShared& sh = *reinterpret_cast<TcShared*>(base + PP::kOffShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // fp32 outputs get P as bf16 hi + lo (fp32-level probabilities); bf16
@@ -411,6 +436,10 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     fence_mbar_init();
   }
   if (!SPARSE && warp == R::kMmaWarp && lane < nshard) prefetch_tmap(kv_map_of(maps, lane));
+  if (NR == 64 && warp == R::kMmaWarp && lane == 0) {
+    prefetch_tmap(&maps.q_nope);
+    prefetch_tmap(&maps.q_pe);
+  }
   // The dense decode reads only its inputs until its first global write (a
   // unit's epilogue), so it starts at once, plans its range itself and
   // streams, and waits for the kernels before it in the stream only there;
@@ -447,20 +476,24 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
       Unit w = w0;
       int cache_b = -1, cache_k = -1, cache_col = 0, my_page = -1;
-      // the unit's Q rows: one slot of the ring, a bulk copy per row half
+      // the unit's Q rows: one slot of the ring (NR <= 32: a bulk copy per
+      // row half; NR = 64: 9 TMA tiles of 64 rows x 64 dims)
       auto issue_q = [&](const Unit& u, int st, uint32_t ph) -> bool {
         bool good = true;
         if (lane == 0) {
           if (!mbar_wait(&sh.empty[st], ph ^ 1)) good = false;
+          else if (NR == 64) issue_q_tma<NR>(maps, kv + st * kStageBytes, (int64_t)u.q0 * a.num_heads + u.row0, &sh.full[st]);
           else mbar_arrive_expect_tx(&sh.full[st], (uint32_t)u.nrows * (kRow * 2));
         }
         good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
         if (!good) return false;
-        uint8_t* qdst = kv + st * kStageBytes;
-        for (int r = lane; r < u.nrows; r += 32) {
-          const int64_t grow = (int64_t)u.q0 * a.num_heads + u.row0 + r;
-          bulk_load(qdst + r * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[st]);
-          bulk_load(qdst + r * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[st]);
+        if (NR < 64) {
+          uint8_t* qdst = kv + st * kStageBytes;
+          for (int r = lane; r < u.nrows; r += 32) {
+            const int64_t grow = (int64_t)u.q0 * a.num_heads + u.row0 + r;
+            bulk_load(qdst + r * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[st]);
+            bulk_load(qdst + r * PP::kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[st]);
+          }
         }
         return true;
       };
@@ -539,41 +572,49 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
     } else {
-      // sparse: 4 warps gather 64 rows x 72 16-byte pieces per tile with
-      // cp.async; warp pw copies keys [16 pw, 16 pw + 16), one row at a time
+      // sparse: the producer warps gather 64 rows x 72 16-byte pieces per
+      // tile with cp.async; warp pw copies keys [KW pw, KW pw + KW), one row at a time
       // with all its lanes (a row's 72 pieces in 3 instructions of
       // consecutive 16-byte pieces: every instruction reads whole 128-byte
       // lines), so the memory system sees line-sized requests, not one
       // 16-byte request per thread and piece.
-      const int pw = warp;            // 0..3
-      const int pt = threadIdx.x;     // 0..127
+      constexpr int KW = kKeyTile / R::kProducerWarps;  // keys per producer warp: 16 or 32
+      const int pw = warp;            // producer warp
+      const int pt = threadIdx.x;     // producer thread
       Unit w = w0;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
         if (w.n_kt > 0) {
           // the unit's Q rows: one slot of the ring, a bulk copy per row half
-          // by thread r; all 128 threads arrive (the stage's full barrier
-          // counts the producer threads), thread 0 with the byte count
+          // by thread r (64-row units: 9 TMA tiles by thread 0); every
+          // producer thread arrives (the stage's full barrier counts them),
+          // thread 0 with the byte count
           if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
           uint8_t* qdst = kv + stage * kStageBytes;
-          if (pt < w.nrows) {
-            const int64_t grow = (int64_t)w.token * a.num_heads + w.row0 + pt;
-            bulk_load(qdst + pt * kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
-            bulk_load(qdst + pt * kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage]);
+          const int64_t grow0 = (int64_t)w.token * a.num_heads + w.row0;
+          if (NR < 64 && pt < w.nrows) {
+            const int64_t grow = grow0 + pt;
+            bulk_load(qdst + pt * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
+            bulk_load(qdst + pt * PP::kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2,
+                      &sh.full[stage]);
           }
-          if (pt == 0) mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
-          else mbar_arrive(&sh.full[stage]);
+          if (pt == 0) {
+            if (NR == 64) issue_q_tma<NR>(maps, qdst, grow0, &sh.full[stage]);
+            else mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
+          } else {
+            mbar_arrive(&sh.full[stage]);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         const int64_t* rows = a.key_rows + (int64_t)w.token * a.list_stride;
         for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-          const int k0 = w.key0 + kt * kKeyTile + pw * 16;
-          // lane l (< 16) fetches the row address of key k0 + l
-          const int64_t my_row = (lane < 16 && k0 + lane < w.key1) ? rows[k0 + lane] : 0;
+          const int k0 = w.key0 + kt * kKeyTile + pw * KW;
+          // lane l (< KW) fetches the row address of key k0 + l
+          const int64_t my_row = (lane < KW && k0 + lane < w.key1) ? rows[k0 + lane] : 0;
           if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
           uint8_t* dst = kv + stage * kStageBytes;
 #pragma unroll 4
-          for (int kk = 0; kk < 16; ++kk) {
-            const int key = pw * 16 + kk;
+          for (int kk = 0; kk < KW; ++kk) {
+            const int key = pw * KW + kk;
             const int64_t row = __shfl_sync(0xffffffffu, my_row, kk);
             // a key past the list's end copies no byte (its row is zero-filled)
             const char* src = row != 0 ? reinterpret_cast<const char*>(row) : reinterpret_cast<const char*>(a.kv);
@@ -615,7 +656,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       const uint32_t kv0 = smem_u32(kv);
       const uint64_t d_kv = smem_desc_sw128(kv0, 16, 1024);                 // K-major KV rows (QK^T B)
       const uint64_t d_v = smem_desc_sw128(kv0, 8192, 1024);                // MN-major kv_c (PV A)
-      const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T (PV B)
+      const uint64_t d_p = smem_desc_sw128(kv0 + kPChunk * kChunk, 16, 1024);  // P^T hi (PV B)
+      // P^T lo: next to hi in the k_pe chunk, or in the stage's own buffer
+      const uint64_t d_plo = PP::kPLoInChunk ? d_p + (uint64_t)(PP::kPBytes >> 4)
+                                             : smem_desc_sw128(smem_u32(p_lo_buf), 16, 1024);
+      constexpr uint64_t kPLoStageUnits = PP::kPLoInChunk ? (kStageBytes >> 4) : (PP::kPBytes >> 4);
+      const uint64_t d_q = smem_desc_sw128(smem_u32(q_smem), 16, 1024);  // Q chunks 0-2 (QK^T A, NR = 64)
       constexpr uint64_t kStageUnits = kStageBytes >> 4;
       if (warp == R::kMmaWarp) {
         // S(j) = Q . KV(j)^T into S buffer j % SB as soon as tile j has
@@ -634,12 +680,18 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             }
             tc_fence_after();
             const uint64_t b0 = d_kv + (uint64_t)stage * kStageUnits;
+            const uint32_t s_col = tmem + TP::kColS + sb * 64;
 #pragma unroll
             for (int c = 0; c < 9; ++c)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColS + sb * 64, tmem + kColQ + (c * 4 + kk) * 8,
-                       b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2), id_qk, (c | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2);
+                const uint32_t acc = (c | kk) != 0;
+                if (c < TP::kQSmemChunks)  // A = Q chunk c in shared memory (128 rows of 128 B)
+                  mma_ss(s_col, d_q + (uint64_t)(c * (16384 >> 4) + kk * 2), bd, id_qk, acc);
+                else  // A = Q chunk c in TMEM
+                  mma_ts(s_col, tmem + kColQ + ((c - TP::kQSmemChunks) * 4 + kk) * 8, bd, id_qk, acc);
+              }
             mma_commit(&sh.s_full[sb]);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
@@ -655,9 +707,10 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
             tc_fence_after();
             const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
-            const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;  // P hi; P lo at + kPBytes
-            const uint32_t o0 = tmem + TmemPlan<NR>::kColO;
-            issue_pv_tile<NR>(o0, v0, p0, id_pv, kt == 0, p_split);
+            const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;
+            const uint64_t p1 = d_plo + (uint64_t)stage * kPLoStageUnits;
+            const uint32_t o0 = tmem + TP::kColO;
+            issue_pv_tile<NR>(o0, v0, p0, p1, id_pv, kt == 0, p_split);
             mma_commit(&sh.empty[stage]);
             mma_commit(&sh.pv_done);
             if (kt + 1 == w.n_kt) mma_commit(&sh.unit_done);
@@ -674,17 +727,20 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     // Every unit row is replicated over TPR TMEM lanes (the M = 128 rows of
     // QK^T cost the same whether padded or not), so each softmax thread owns
-    // KPT of the 64 keys of one row.  Lane l of quarter q holds row l % NR and
-    // key slice q * (32 / NR) + l / NR: the slice is uniform over a warp (or
+    // KPT of the 64 keys of one row.  TMEM lane L = 32 q + l (quarter q) holds
+    // row L % NR and key slice L / NR: the slice is uniform over a warp (or
     // over each half-warp for NR = 16), so each thread reads just its own
     // columns of S.  The row max is reduced through shared memory; each thread
     // keeps a partial row sum until the unit's epilogue.
-    constexpr int TPR = 128 / NR;          // lanes per row: 8 or 4
-    constexpr int KPT = kKeyTile / TPR;    // keys per thread: 8 or 16
-    constexpr int RPW = 32 / NR;           // replicas of a row inside one warp: 2 or 1
-    const int row = lane % NR;             // unit row of this lane
-    const int kslice = quarter * RPW + lane / NR;  // keys [kslice * KPT, + KPT) of the tile
-    const bool row_lead = kslice == 0;     // writes the row's shared values
+    constexpr int TPR = 128 / NR;                 // lanes per row: 8, 4 or 2
+    constexpr int KPT = kKeyTile / TPR;           // keys per thread: 8, 16 or 32
+    constexpr int RPW = NR >= 32 ? 1 : 32 / NR;   // key slices inside one warp: 2 or 1
+    constexpr int CW = NR < 32 ? NR : 32;         // O^T columns per TMEM load (registers)
+    const int tl = quarter * 32 + lane;           // this thread's TMEM lane
+    const int row = tl % NR;                      // unit row of this lane
+    const int kslice = tl / NR;                   // keys [kslice * KPT, + KPT) of the tile
+    const int kslice0 = quarter * 32 / NR;        // the warp's first key slice
+    const bool row_lead = kslice == 0;            // writes the row's shared values
     const float scale_log2 = a.scale * kLog2e;
     const int H = a.num_heads;
     uint32_t j = 0, u_ph = 0;
@@ -709,22 +765,31 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     // Q rows of unit u into TMEM, then q_ready.  Called once every QK^T
     // issued so far is complete (the softmax has read all their S).
     auto load_q = [&](const Unit& u) -> bool {
-      // Q row of this lane -> its TMEM lane: columns [0, 288) hold 576 bf16
-      // (the TPR lanes of a row read the same addresses)
+      // Q row of this lane -> its TMEM lane: 32 columns (64 bf16) per chunk
+      // (the TPR lanes of a row read the same addresses); NR = 64: chunks 0-2
+      // into the shared-memory A operand instead, at row tl
       const bool have = row < u.nrows;
       // the rows are in this unit's Q slot of the ring
       if (!group_wait(&sh.full[stage], sphase)) return false;
       mbar_wait(&sh.full[stage], sphase);  // every reader observes the phase (returns at once)
-      const uint8_t* qrow = kv + stage * kStageBytes + row * kQRowBytes;
+      const uint8_t* slot = kv + stage * kStageBytes;
 #pragma unroll 1
       for (int c = 0; c < 9; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x = have ? *reinterpret_cast<const uint4*>(qrow + c * 128 + v * 16) : make_uint4(0, 0, 0, 0);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+          // NR <= 32: padded rows; NR = 64: TMA tiles (64 rows x 128 B per
+          // chunk, 16-byte pieces swizzled by row & 7)
+          const uint8_t* src = NR == 64 ? slot + c * kChunk + row * 128 + ((v ^ (row & 7)) << 4)
+                                        : slot + row * PP::kQRowBytes + c * 128 + v * 16;
+          const uint4 x = have ? *reinterpret_cast<const uint4*>(src) : make_uint4(0, 0, 0, 0);
+          if (c < TP::kQSmemChunks) {
+            *reinterpret_cast<uint4*>(q_smem + c * 16384 + tl * 128 + ((v ^ (tl & 7)) << 4)) = x;
+          } else {
+            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+          }
         }
-        tmem_st<32>(tmem + lane_base + kColQ + c * 32, r);
+        if (c >= TP::kQSmemChunks) tmem_st<32>(tmem + lane_base + kColQ + (c - TP::kQSmemChunks) * 32, r);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -745,12 +810,16 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
     if constexpr (!SPARSE) {
       // dense: the first unit's Q slot (stage 0) is filled from here
       if (more && wn.n_kt > 0) {
-        if (st_tid == 0) mbar_arrive_expect_tx(&sh.full[0], (uint32_t)wn.nrows * (kRow * 2));
-        if (st_tid < wn.nrows) {
-          const int64_t g = grow_of(wn, st_tid);
-          uint8_t* qdst = kv + st_tid * kQRowBytes;
-          bulk_load(qdst, a.q_nope + g * a.q_nope_stride, kNope * 2, &sh.full[0]);
-          bulk_load(qdst + kNope * 2, a.q_pe + g * a.q_pe_stride, kRope * 2, &sh.full[0]);
+        if (NR == 64) {
+          if (st_tid == 0) issue_q_tma<NR>(maps, kv, grow_of(wn, 0), &sh.full[0]);
+        } else {
+          if (st_tid == 0) mbar_arrive_expect_tx(&sh.full[0], (uint32_t)wn.nrows * (kRow * 2));
+          if (st_tid < wn.nrows) {
+            const int64_t g = grow_of(wn, st_tid);
+            uint8_t* qdst = kv + st_tid * PP::kQRowBytes;
+            bulk_load(qdst, a.q_nope + g * a.q_nope_stride, kNope * 2, &sh.full[0]);
+            bulk_load(qdst + kNope * 2, a.q_pe + g * a.q_pe_stride, kRope * 2, &sh.full[0]);
+          }
         }
       }
     }
@@ -782,9 +851,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
           uint32_t v[KPT];
-          tmem_ld<KPT>(tmem + lane_base + kColS + (j % SB) * 64 + (quarter * RPW + r) * KPT, v);
+          tmem_ld<KPT>(tmem + lane_base + TP::kColS + (j % SB) * 64 + (kslice0 + r) * KPT, v);
           tmem_wait_ld();
-          if (lane / NR == r) {
+          if (kslice - kslice0 == r) {
 #pragma unroll
             for (int e = 0; e < KPT; ++e) s[e] = __uint_as_float(v[e]);
           }
@@ -808,7 +877,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           s[e] = v;
           pmax = fmaxf(pmax, v);
         }
-        sh.red[j & 1][kslice][row] = pmax;
+        sh.red[j & 1][kslice * NR + row] = pmax;
         tc_fence_before();
         named_bar_sync(1, 128);
         if (st_tid == 0) {
@@ -818,7 +887,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         {
           float tmax = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < TPR; ++k) tmax = fmaxf(tmax, sh.red[j & 1][k][row]);
+          for (int k = 0; k < TPR; ++k) tmax = fmaxf(tmax, sh.red[j & 1][k * NR + row]);
           float alpha = 1.f;
           if (tmax > m_ref + kRescaleThreshold) {  // also the first finite max (m_ref = -inf)
             alpha = fast_exp2(m_ref - tmax);       // 0 when m_ref = -inf
@@ -830,7 +899,9 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           // P^T in the k_pe chunk of this tile's stage (QK^T of the tile, its
           // only reader, is complete).  For fp32 outputs P goes in as bf16 hi
           // and lo = bf16(P - hi), so hi + lo carries P to ~2^-17.
-          uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + (row >> 3) * 1024 + (row & 7) * 128;
+          const int roff = (row >> 3) * 1024 + (row & 7) * 128;
+          uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + roff;
+          uint8_t* prow_lo = PP::kPLoInChunk ? prow + PP::kPBytes : p_lo_buf + stage * PP::kPBytes + roff;
           float sum = 0.f;
 #pragma unroll
           for (int c8 = 0; c8 < KPT / 8; ++c8) {
@@ -851,7 +922,7 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
             const int piece = kslice * (KPT / 8) + c8;  // 16-byte piece (8 keys) of the row
             const int off = (piece ^ (row & 7)) << 4;
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            if (p_split) *reinterpret_cast<uint4*>(prow + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            if (p_split) *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
           l_sum += sum;  // this thread's part of the row sum (same alpha for every part)
         }
@@ -875,14 +946,16 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
           named_bar_sync(1, 128);
         }
         if (sh.any_rescale[j & 1]) {
+          // O^T's 4 NR columns, CW per TMEM round trip
 #pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
-            uint32_t o[NR];
-            tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
+          for (int q = 0; q < 4 * NR / CW; ++q) {
+            uint32_t o[CW];
+            tmem_ld<CW>(tmem + lane_base + TP::kColO + q * CW, o);
             tmem_wait_ld();
+            const int n0 = (q * CW) % NR;
 #pragma unroll
-            for (int n = 0; n < NR; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * sh.alpha[n]);
-            tmem_st<NR>(tmem + lane_base + TmemPlan<NR>::kColO + m * NR, o);
+            for (int n = 0; n < CW; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * sh.alpha[n0 + n]);
+            tmem_st<CW>(tmem + lane_base + TP::kColO + q * CW, o);
           }
           tmem_wait_st();
         }
@@ -908,12 +981,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
       // first global write of this kernel: everything before it in the
       // stream (the previous call's readers of these outputs) has finished
       grid_dep_wait();
-      sh.lpart[kslice][row] = l_sum;
+      sh.lpart[kslice * NR + row] = l_sum;
       named_bar_sync(1, 128);
       if (row_lead) {
         float lt = 0.f;
 #pragma unroll
-        for (int k = 0; k < TPR; ++k) lt += sh.lpart[k][row];
+        for (int k = 0; k < TPR; ++k) lt += sh.lpart[k * NR + row];
         const bool live = lt > 0.f && m_ref > -INFINITY;
         sh.inv_l[row] = live ? 1.f / lt : 0.f;
         if (row < w.nrows) {
@@ -923,28 +996,31 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
         }
       }
       named_bar_sync(1, 128);
-      // O^T's 4 column blocks, MB per TMEM round trip (64 registers)
-      constexpr int MB = 64 / NR;
+      // O^T's 4 NR columns (column m NR + n: dims of block m, row n), 64
+      // columns (registers) per TMEM round trip in loads of CW
+      constexpr int PER = 64 / CW;
 #pragma unroll 1
-      for (int m0 = 0; m0 < 4; m0 += MB) {
-        uint32_t o[MB][NR];
+      for (int q0 = 0; q0 < 4 * NR / CW; q0 += PER) {
+        uint32_t o[PER][CW];
         if (w.n_kt > 0) {
 #pragma unroll
-          for (int mb = 0; mb < MB; ++mb) tmem_ld<NR>(tmem + lane_base + TmemPlan<NR>::kColO + (m0 + mb) * NR, o[mb]);
+          for (int p = 0; p < PER; ++p) tmem_ld<CW>(tmem + lane_base + TP::kColO + (q0 + p) * CW, o[p]);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int mb = 0; mb < MB; ++mb)
+          for (int p = 0; p < PER; ++p)
 #pragma unroll
-            for (int n = 0; n < NR; ++n) o[mb][n] = 0u;
+            for (int n = 0; n < CW; ++n) o[p][n] = 0u;
         }
 #pragma unroll
-        for (int mb = 0; mb < MB; ++mb) {
-          const int dim = (m0 + mb) * 128 + quarter * 32 + lane;
+        for (int p = 0; p < PER; ++p) {
+          const int col0 = (q0 + p) * CW;
+          const int dim = (col0 / NR) * 128 + quarter * 32 + lane;
 #pragma unroll
-          for (int n = 0; n < NR; ++n) {
+          for (int e = 0; e < CW; ++e) {
+            const int n = col0 % NR + e;
             if (n >= w.nrows) break;
-            const float v = __uint_as_float(o[mb][n]) * sh.inv_l[n];
+            const float v = __uint_as_float(o[p][e]) * sh.inv_l[n];
             if (partial) {
               const int64_t slot = chunk_slot(w.cta0, w.split, NR) + n;
               a.part_o[slot * kNope + dim] = v;
@@ -980,11 +1056,12 @@ __global__ void __launch_bounds__(Roles<SPARSE>::kThreads, 1)
 
 template <int NR, bool SPARSE, bool FUSED>
 cudaError_t launch_tc(const DecodeArgs& a, const KvMaps& maps, int grid, cudaStream_t stream) {
-  const size_t smem = 1024 + kStages * kStageBytes + sizeof(TcShared);
+  const size_t smem = 1024 + Pipe<NR>::kOffShared + sizeof(TcShared);
+  static_assert(1024 + Pipe<NR>::kOffShared + sizeof(TcShared) <= 232448, "shared memory per CTA");
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<NR, SPARSE, FUSED>, dim3(grid), dim3(Roles<SPARSE>::kThreads), smem, stream,
+  return launch_pdl(decode_tc_kernel<NR, SPARSE, FUSED>, dim3(grid), dim3(Roles<SPARSE, NR>::kThreads), smem, stream,
                     maps, a);
 }
 
@@ -994,17 +1071,31 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool spars
                              cudaStream_t stream) {
   if (max_units <= 0) return cudaSuccess;
   if (a.nshard < 1 || a.nshard > kMaxShards || (sparse && a.nshard != 1)) return cudaErrorInvalidValue;
+  if (rows_per_group != 16 && rows_per_group != 32 && rows_per_group != 64) return cudaErrorInvalidValue;
   KvMaps maps;
   memset(&maps, 0, sizeof(maps));
   for (int k = 0; k < a.nshard; ++k)
     if (!make_kv_tensor_map(&maps.m[k], a.kvs[k], a.nblocks[k], a.page_size)) return cudaErrorInvalidValue;
+  if (rows_per_group == 64) {
+    const int64_t rows = (int64_t)a.num_tokens * a.num_heads;
+    if (!make_query_tensor_map(&maps.q_nope, a.q_nope, rows, kNope, a.q_nope_stride) ||
+        !make_query_tensor_map(&maps.q_pe, a.q_pe, rows, kRope, a.q_pe_stride))
+      return cudaErrorInvalidValue;
+  }
   const int grid = max_units < num_sms ? max_units : num_sms;
-  const bool nr16 = rows_per_group == 16;
-  if (sparse)
-    return nr16 ? launch_tc<16, true, false>(a, maps, grid, stream) : launch_tc<32, true, false>(a, maps, grid, stream);
-  if (a.nshard > 1)
-    return nr16 ? launch_tc<16, false, true>(a, maps, grid, stream) : launch_tc<32, false, true>(a, maps, grid, stream);
-  return nr16 ? launch_tc<16, false, false>(a, maps, grid, stream) : launch_tc<32, false, false>(a, maps, grid, stream);
+  if (sparse) {
+    if (rows_per_group == 16) return launch_tc<16, true, false>(a, maps, grid, stream);
+    if (rows_per_group == 32) return launch_tc<32, true, false>(a, maps, grid, stream);
+    return launch_tc<64, true, false>(a, maps, grid, stream);
+  }
+  if (a.nshard > 1) {
+    if (rows_per_group == 16) return launch_tc<16, false, true>(a, maps, grid, stream);
+    if (rows_per_group == 32) return launch_tc<32, false, true>(a, maps, grid, stream);
+    return launch_tc<64, false, true>(a, maps, grid, stream);
+  }
+  if (rows_per_group == 16) return launch_tc<16, false, false>(a, maps, grid, stream);
+  if (rows_per_group == 32) return launch_tc<32, false, false>(a, maps, grid, stream);
+  return launch_tc<64, false, false>(a, maps, grid, stream);
 }
 
 }  // namespace mla

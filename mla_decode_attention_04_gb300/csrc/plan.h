@@ -29,7 +29,7 @@ struct PrepArgs {
 // [(2 c + 1) NR, (2 c + 2) NR) for the chunk its last unit starts; entry c
 // of the split table describes the pair whose first chunk CTA c holds.
 struct DecodePlan {
-  int32_t rows_per_group;  // rows (token, head) per work unit: 16 or 32
+  int32_t rows_per_group;  // rows (token, head) per work unit: 16, 32 or 64
   int32_t grid;            // decode CTAs
   int32_t unit_penalty;    // balancing cost of a unit start, in 64-key tiles
   size_t off_desc, off_plse, off_po, total;
@@ -37,12 +37,18 @@ struct DecodePlan {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Rows (token, head) per decode work unit for a request (or token) of up to
+// `rows` rows: the fewest of 16, 32, 64 that hold them (64 at most; more
+// rows form several units, each of which streams the keys).  Bigger units
+// read each key tile for more rows.
+inline int32_t rows_per_unit(int64_t rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
+
 inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_query_len, int32_t max_seq_len,
                                    int32_t D, int32_t num_splits, int32_t num_sms) {
   DecodePlan p{};
   if (max_query_len < 1) max_query_len = 1;  // the backend's capture-time clamp
   if (D < 1) D = 1;
-  p.rows_per_group = (int64_t)max_query_len * H <= 16 ? 16 : 32;
+  p.rows_per_group = rows_per_unit((int64_t)max_query_len * H);
   p.unit_penalty = kUnitPenalty;
   const int64_t NR = p.rows_per_group;
   const int64_t max_local = (max_seq_len + D - 1) / D;
@@ -84,7 +90,7 @@ struct SparsePlan {
 
 inline SparsePlan make_sparse_plan(int32_t T, int32_t H, int32_t topk, int32_t num_sms) {
   SparsePlan p{};
-  p.rows_per_group = H <= 16 ? 16 : 32;
+  p.rows_per_group = rows_per_unit(H);
   const size_t NR = (size_t)p.rows_per_group;
   p.grid = num_sms > 0 ? num_sms : 148;
   const size_t nt = (size_t)(T > 0 ? T : 1);

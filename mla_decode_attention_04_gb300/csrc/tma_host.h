@@ -38,4 +38,21 @@ inline bool make_kv_tensor_map(CUtensorMap* map, const void* kv, int64_t num_blo
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a query part (q_nope or q_pe) viewed as [rows][width] bf16
+// with a row stride of `stride` elements (a multiple of 8), box of 64 rows x
+// 64 columns (128 bytes, 128-byte swizzle), with a unit outer dimension so
+// the 3-D TMA wrapper serves it.  Rows past the end read as zero.
+inline bool make_query_tensor_map(CUtensorMap* map, const void* q, int64_t rows, int32_t width, int64_t stride) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || rows < 1) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 1};
+  const cuuint64_t strides[2] = {(cuuint64_t)stride * 2, (cuuint64_t)stride * 2 * (cuuint64_t)rows};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mla

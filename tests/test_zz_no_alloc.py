@@ -94,9 +94,10 @@ def test_static_scratch_back_to_back_on_one_stream(lib):
 
 
 def test_static_scratch_refuses_oversized_problems(lib):
-    # The dense workspace is bounded by the SM count (2 x SMs x 32 partial
-    # rows), so the largest problem this GPU can be given is one with 32-row
-    # units; the refusal is only reachable on a GPU where that exceeds the array.
+    # The dense workspace is bounded by the SM count (2 partial slots of up
+    # to 64 rows per SM): a problem with 64-row units (here 2 query tokens x
+    # 128 heads per request) needs about 40 MB on a 152-SM GPU, more than the
+    # array, so it is refused before anything runs.
     B, T, H, L = 32, 64, 128, 32768
     need = lib.mla_dcp_decode_workspace_size(B, T, H, 2, L, 8, 0)
     if need <= mla.MLA_STATIC_SCRATCH_BYTES:
