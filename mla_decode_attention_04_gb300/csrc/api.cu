@@ -145,6 +145,7 @@ namespace {
 cudaError_t launch_split_merge(const mla::DecodeArgs& da, int rows_per_group, int grid, int64_t num_rows,
                                cudaStream_t st) {
   mla::SplitMergeArgs sa{};
+  sa.cta_stride = da.gang > 1 ? da.gang : 1;
   sa.split_desc = da.split_desc;
   sa.part_lse = da.part_lse;
   sa.part_o = da.part_o;
@@ -232,6 +233,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.query_start_loc = query_start_loc;
   da.num_requests = num_requests;
   da.unit_penalty = plan.unit_penalty;
+  da.gang = plan.gang;
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
@@ -325,6 +327,7 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.list_stride = topk;
   da.num_tokens = num_tokens;
   da.unit_penalty = mla::kUnitPenalty;
+  da.gang = 1;
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);

@@ -55,9 +55,11 @@ __host__ __device__ __forceinline__ int32_t visible_keys(int32_t P, int32_t D, i
 
 // First partial row of chunk k of a split row group whose first chunk decode
 // CTA cta0 holds: chunk 0 is cta0's last unit (its second slot), chunk k > 0
-// is the first unit of CTA cta0 + k (that CTA's first slot).  NR rows each.
-__host__ __device__ __forceinline__ int64_t chunk_slot(int cta0, int k, int NR) {
-  return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k)) * NR;
+// is the first unit of CTA cta0 + k * stride (that CTA's first slot); the
+// stride is 1, or the gang size when the CTAs run in gangs (the gang
+// members hold the other row groups of the same requests).  NR rows each.
+__host__ __device__ __forceinline__ int64_t chunk_slot(int cta0, int k, int NR, int stride) {
+  return (int64_t)(k == 0 ? 2 * cta0 + 1 : 2 * (cta0 + k * stride)) * NR;
 }
 
 // Most DCP shards one call can cover (the shard-fused entry points).

@@ -30,6 +30,11 @@ struct DecodeArgs {
   const int32_t* query_start_loc;
   int32_t num_requests;
   int32_t unit_penalty;
+  // CTAs per gang (1: no gangs).  With gangs of S CTAs, gang j takes a range
+  // of the requests' key tiles and its CTA g runs row group g of each
+  // request over that range, so the S row groups read each tile at about
+  // the same time (one HBM read serves them all through L2).
+  int32_t gang;
   int4* split_desc;  // [grid] the split pair whose first chunk CTA c holds: {chunks, first row, rows, 0}
   float* part_lse;   // [2 grid NR]
   float* part_o;     // [2 grid NR, 512]

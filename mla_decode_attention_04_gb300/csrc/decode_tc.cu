@@ -99,10 +99,20 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // 32) or in the stage's P lo buffer (NR = 64).
 constexpr int kPChunk = 8;  // the k_pe chunk of a stage
 constexpr int kMaxStages = 3;
+// A stage is filled and freed in 4 parts: part m holds chunks 2m and 2m + 1,
+// the dims block 128m..128m+127 that value-product block m reads, and part 3
+// also the k_pe chunk (P's home after the score product).  Each part has
+// its own full and empty barrier, so the producer refills a stage part by
+// part as the value product's blocks complete, and the score product of the
+// next tile in the stage starts on its first parts while the last ones
+// still load.
+constexpr int kParts = 4;
+__host__ __device__ constexpr int part_first_chunk(int m) { return 2 * m; }
+__host__ __device__ constexpr int part_chunks(int m) { return m == kParts - 1 ? 3 : 2; }
 
 struct TcShared {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t full[kMaxStages][kParts];
+  uint64_t empty[kMaxStages][kParts];
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
@@ -182,24 +192,39 @@ struct Source {
   }
 };
 
+// Items a source contributes to the split plan: its pairs (row groups;
+// with gangs of S > 1 CTAs the pairs share the items, so one) times its key
+// tiles plus the unit start-up cost; nothing without keys or rows.
+__device__ __forceinline__ int64_t source_items(const ReqFacts& f, int64_t pen, int S) {
+  if (f.nt <= 0 || f.groups <= 0) return 0;
+  return (S > 1 ? 1 : (int64_t)f.groups) * ((int64_t)f.nt + pen);
+}
+
 // The sequence of units of one CTA.  Every (source, row group) pair
 // contributes unit_penalty work-free items (the cost of starting a unit)
 // followed by its 64-key tiles to one flattened list of W items; CTA c takes
-// items [c W / G, (c + 1) W / G), cut at pair boundaries.  The CTA found the
-// source holding its first item at start-up (plan_cta); the next source's raw
-// inputs are loaded one source ahead and turned into facts only when the walk
-// reaches it, so no step of the walk waits for a load.  Every role walks the
-// same sequence.
+// items [c W / G, (c + 1) W / G), cut at pair boundaries.  With gangs of S
+// CTAs (dense calls whose requests have several row groups), a source
+// contributes its items once, not once per row group: gang j = c / S takes
+// items [j W / G, (j + 1) W / G) (G gangs) and its CTA g = c % S runs row
+// group g of each source over them; a pair's chunks are then on CTAs S
+// apart.  The CTA found the source holding its first item at start-up
+// (plan_cta); the next source's raw inputs are loaded one source ahead and
+// turned into facts only when the walk reaches it, so no step of the walk
+// waits for a load.  Every role walks the same sequence.
 template <int NR, bool SPARSE>
 struct UnitIter {
   int64_t i, hi, W, G, ib;  // next item, range end, plan, item base of source b
   int b;
+  int S, gg;  // gang size (1: no gangs) and this CTA's row group within its gang
   ReqFacts cur;
   int n0, n1, n2;  // raw inputs of source b + 1
 
   __device__ __forceinline__ void fetch_next(const DecodeArgs& a) { Source<NR, SPARSE>::load(a, b + 1, n0, n1, n2); }
 
   __device__ void init(const DecodeArgs& a, const TcShared& sh) {
+    S = (!SPARSE && a.gang > 1) ? a.gang : 1;
+    gg = (int)blockIdx.x % S;
     if (sh.plan_b < 0) {
       i = hi = 0;
       return;
@@ -219,8 +244,8 @@ struct UnitIter {
     const int nsrc = Source<NR, SPARSE>::count(a);
     while (true) {
       if (i >= hi) return false;
-      const int64_t vlen = cur.nt > 0 ? (int64_t)cur.nt + pen : 0;
-      const int64_t rend = ib + (int64_t)cur.groups * vlen;  // end of source b's items
+      const int64_t vlen = (int64_t)cur.nt + pen;
+      const int64_t rend = ib + source_items(cur, pen, S);  // end of source b's items
       if (i >= rend) {
         // source b is done (or owns no item): the next one
         if (b + 1 >= nsrc) {
@@ -233,13 +258,18 @@ struct UnitIter {
         if (b + 1 < nsrc) fetch_next(a);
         continue;
       }
-      const int g = (int)quot_floor(i - ib, vlen);  // row group holding item i
-      const int64_t item0 = ib + (int64_t)g * vlen + pen;
+      // row group holding item i (gangs: this CTA's group, items shared)
+      const int g = S > 1 ? gg : (int)quot_floor(i - ib, vlen);
+      const int64_t item0 = ib + (S > 1 ? 0 : (int64_t)g * vlen) + pen;
       // the range may start among the items that only carry the pair's
       // start-up cost; a range holding none of its key tiles has no unit
       if (i < item0) i = item0;
       if (i >= hi) return false;
       const int64_t end = min(hi, item0 + cur.nt);
+      if (g >= cur.groups) {  // gangs: this source has no row group g
+        i = end;
+        continue;
+      }
       w.token = SPARSE ? b : -1;
       w.b = b;
       w.row0 = g * NR;
@@ -249,9 +279,10 @@ struct UnitIter {
       w.key1 = (int)(end - item0) * kKeyTile;
       if (SPARSE && w.key1 > cur.local_len) w.key1 = cur.local_len;  // the list's end
       w.n_kt = (int)(end - i);
-      w.cta0 = (int)range_owner(item0, W, G);
-      w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - w.cta0 + 1);
-      w.split = (int)blockIdx.x - w.cta0;  // the unit's items are this CTA's
+      const int own0 = (int)range_owner(item0, W, G);  // CTA (gangs: gang) of the pair's first tile
+      w.cta0 = own0 * S + gg;
+      w.nsplit = (int)(range_owner(item0 + cur.nt - 1, W, G) - own0 + 1);
+      w.split = (int)blockIdx.x / S - own0;  // the unit's items are this CTA's
       w.q0 = cur.q0;
       w.q_len = cur.q_len;
       w.seq_len = cur.seq_len;
@@ -272,6 +303,9 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int B = Source<NR, SPARSE>::count(a);
   const int64_t pen = a.unit_penalty;
+  // gangs of S CTAs: a source's items counted once; this CTA plans as gang c / S of gridDim / S
+  const int S = (!SPARSE && a.gang > 1) ? a.gang : 1;
+  const int64_t me = (int64_t)blockIdx.x / S, nplan = (int64_t)gridDim.x / S;
   const bool single = B <= (int)blockDim.x;  // one chunk of requests: pass 0's facts stay in registers
   ReqFacts f1{};
   int64_t ex1 = 0, lo = 0;
@@ -289,7 +323,7 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
           f1 = Source<NR, SPARSE>::facts(a, b, r0, r1, r2);
         }
         // exclusive block scan of the requests' item counts
-        const int64_t v = f1.nt > 0 ? (int64_t)f1.groups * ((int64_t)f1.nt + pen) : 0;
+        const int64_t v = source_items(f1, pen, S);
         int64_t x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -309,7 +343,7 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
         run += all;
       }
       if (pass == 1) {
-        const int64_t n = f1.nt > 0 ? (int64_t)f1.groups * ((int64_t)f1.nt + pen) : 0;
+        const int64_t n = source_items(f1, pen, S);
         if (b < B && n > 0 && ex1 <= lo && lo < ex1 + n) {
           sh.plan_b = b;
           sh.plan_ib = ex1;
@@ -319,13 +353,13 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
     }
     if (pass == 0) {
       const int64_t W = run;
-      const int64_t G = (int64_t)gridDim.x < W ? (int64_t)gridDim.x : (W > 0 ? W : 1);
-      const bool has = W > 0 && (int64_t)blockIdx.x < G;
-      lo = has ? quot_floor((int64_t)blockIdx.x * W, G) : 0;
+      const int64_t G = nplan < W ? nplan : (W > 0 ? W : 1);
+      const bool has = W > 0 && me < G;
+      lo = has ? quot_floor(me * W, G) : 0;
       if (tid == 0) {
         sh.plan_b = -1;
         sh.plan_lo = lo;
-        sh.plan_hi = has ? quot_floor(((int64_t)blockIdx.x + 1) * W, G) : 0;
+        sh.plan_hi = has ? quot_floor((me + 1) * W, G) : 0;
         sh.plan_W = W;
         sh.plan_G = G;
       }
@@ -337,20 +371,26 @@ __device__ __forceinline__ void plan_cta(const DecodeArgs& a, TcShared& sh) {
 }
 
 // The 16 (32 with P as hi + lo) MMAs of one tile's O^T += V_c^T . P^T (P^T
-// hi and lo at descriptors p_hi, p_lo).  The first tile of a unit overwrites
-// O^T; the P split (hi + lo, for fp32 outputs) doubles the MMAs.  One rolled copy: the issue rate of a thread,
-// not the loop, bounds it.
+// hi and lo at descriptors p_hi, p_lo), block m (dims 128m..128m+127) after
+// block m - 1, each block's completion committed to the stage part that
+// holds its dims (empty[m]), so the producer refills the part while the
+// later blocks run.  The first tile of a unit overwrites O^T; the P split
+// (hi + lo, for fp32 outputs) doubles the MMAs (they share their A operand,
+// which makes the second nearly free).  One rolled copy: the issue rate of
+// a thread, not the loop, bounds it.
 template <int NR>
 __device__ __forceinline__ void issue_pv_tile(uint32_t o0, uint64_t v0, uint64_t p_hi, uint64_t p_lo, uint32_t id_pv,
-                                              bool first, bool split) {
+                                              bool first, bool split, uint64_t* empty) {
 #pragma unroll 1
-  for (int m = 0; m < 4; ++m)
+  for (int m = 0; m < kParts; ++m) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t va = v0 + (uint64_t)((2 * m * kChunk + kk * 2048) >> 4);
       mma_ss(o0 + m * NR, va, p_hi + (uint64_t)(kk * 2), id_pv, (first && kk == 0) ? 0u : 1u);
       if (split) mma_ss(o0 + m * NR, va, p_lo + (uint64_t)(kk * 2), id_pv, 1u);
     }
+    mma_commit(&empty[m]);
+  }
 }
 
 // A tile of a request's sequence: shard index k within the call, tile lt of
@@ -420,10 +460,11 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh.full[s], SPARSE ? 32 * R::kProducerWarps : 1);
-      mbar_init(&sh.empty[s], 1);
-    }
+    for (int s = 0; s < kStages; ++s)
+      for (int m = 0; m < kParts; ++m) {
+        mbar_init(&sh.full[s][m], SPARSE ? 32 * R::kProducerWarps : 1);
+        mbar_init(&sh.empty[s][m], 1);
+      }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
       mbar_init(&sh.s_free[b], 1);
@@ -471,7 +512,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       // table column (cache_col + l), refilled 32 columns at a time, so the
       // block-table reads of 32 pages cost one memory latency.  Lane 0 waits
       // for free stages and issues the TMA loads.
-      const uint64_t pol = policy_evict_first();
+      // a key tile read by one CTA is evicted first; gang members read each
+      // tile in turn, so then it stays in L2 at normal priority
+      const uint64_t pol = a.gang > 1 ? policy_evict_normal() : policy_evict_first();
       const int ps = a.page_size;
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
       Unit w = w0;
@@ -480,10 +523,18 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       // row half; NR = 64: 9 TMA tiles of 64 rows x 64 dims)
       auto issue_q = [&](const Unit& u, int st, uint32_t ph) -> bool {
         bool good = true;
+        // the slot's bytes all complete on part 0's full barrier; parts 1-3
+        // only see an arrival, so every part completes one phase per use
         if (lane == 0) {
-          if (!mbar_wait(&sh.empty[st], ph ^ 1)) good = false;
-          else if (NR == 64) issue_q_tma<NR>(maps, kv + st * kStageBytes, (int64_t)u.q0 * a.num_heads + u.row0, &sh.full[st]);
-          else mbar_arrive_expect_tx(&sh.full[st], (uint32_t)u.nrows * (kRow * 2));
+          for (int m = 0; m < kParts && good; ++m)
+            if (!mbar_wait(&sh.empty[st][m], ph ^ 1)) good = false;
+          if (good) {
+            if (NR == 64)
+              issue_q_tma<NR>(maps, kv + st * kStageBytes, (int64_t)u.q0 * a.num_heads + u.row0, &sh.full[st][0]);
+            else
+              mbar_arrive_expect_tx(&sh.full[st][0], (uint32_t)u.nrows * (kRow * 2));
+            for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[st][m]);
+          }
         }
         good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
         if (!good) return false;
@@ -491,8 +542,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           uint8_t* qdst = kv + st * kStageBytes;
           for (int r = lane; r < u.nrows; r += 32) {
             const int64_t grow = (int64_t)u.q0 * a.num_heads + u.row0 + r;
-            bulk_load(qdst + r * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[st]);
-            bulk_load(qdst + r * PP::kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[st]);
+            bulk_load(qdst + r * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[st][0]);
+            bulk_load(qdst + r * PP::kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2,
+                      &sh.full[st][0]);
           }
         }
         return true;
@@ -554,17 +606,21 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
             }
           }
           if (lane == 0) {
-            if (!mbar_wait(&sh.empty[stage], phase ^ 1)) {
-              ok = false;
-            } else {
-              uint8_t* dst = kv + stage * kStageBytes;
-              const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
-              mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)nvalid * rows * 128u * 9u);
-              const int off = ps >= kKeyTile ? k % ps : 0;
+            // part by part, each as soon as the value product frees it
+            uint8_t* dst = kv + stage * kStageBytes;
+            const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
+            const int off = ps >= kKeyTile ? k % ps : 0;
+            for (int m = 0; m < kParts; ++m) {
+              if (!mbar_wait(&sh.empty[stage][m], phase ^ 1)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&sh.full[stage][m], (uint32_t)(nvalid * rows * 128 * part_chunks(m)));
               for (int i = 0; i < nsub; ++i)
                 if (pages[i] >= 0)
-                  for (int c = 0; c < 9; ++c)
-                    tma_load_3d(dst + c * kChunk + i * ps * 128, map, c * 64, off, pages[i], &sh.full[stage], pol);
+                  for (int c = part_first_chunk(m); c < part_first_chunk(m) + part_chunks(m); ++c)
+                    tma_load_3d(dst + c * kChunk + i * ps * 128, map, c * 64, off, pages[i], &sh.full[stage][m],
+                                pol);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -588,21 +644,25 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           // by thread r (64-row units: 9 TMA tiles by thread 0); every
           // producer thread arrives (the stage's full barrier counts them),
           // thread 0 with the byte count
-          if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
+          bool free_ok = true;
+          for (int m = 0; m < kParts; ++m)
+            if (!mbar_wait(&sh.empty[stage][m], phase ^ 1)) free_ok = false;
+          if (!free_ok) { ok = false; break; }
           uint8_t* qdst = kv + stage * kStageBytes;
           const int64_t grow0 = (int64_t)w.token * a.num_heads + w.row0;
           if (NR < 64 && pt < w.nrows) {
             const int64_t grow = grow0 + pt;
-            bulk_load(qdst + pt * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage]);
+            bulk_load(qdst + pt * PP::kQRowBytes, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage][0]);
             bulk_load(qdst + pt * PP::kQRowBytes + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2,
-                      &sh.full[stage]);
+                      &sh.full[stage][0]);
           }
           if (pt == 0) {
-            if (NR == 64) issue_q_tma<NR>(maps, qdst, grow0, &sh.full[stage]);
-            else mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)w.nrows * (kRow * 2));
+            if (NR == 64) issue_q_tma<NR>(maps, qdst, grow0, &sh.full[stage][0]);
+            else mbar_arrive_expect_tx(&sh.full[stage][0], (uint32_t)w.nrows * (kRow * 2));
           } else {
-            mbar_arrive(&sh.full[stage]);
+            mbar_arrive(&sh.full[stage][0]);
           }
+          for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[stage][m]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         const int64_t* rows = a.key_rows + (int64_t)w.token * a.list_stride;
@@ -610,29 +670,36 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           const int k0 = w.key0 + kt * kKeyTile + pw * KW;
           // lane l (< KW) fetches the row address of key k0 + l
           const int64_t my_row = (lane < KW && k0 + lane < w.key1) ? rows[k0 + lane] : 0;
-          if (!mbar_wait(&sh.empty[stage], phase ^ 1)) { ok = false; break; }
           uint8_t* dst = kv + stage * kStageBytes;
-#pragma unroll 4
-          for (int kk = 0; kk < KW; ++kk) {
-            const int key = pw * KW + kk;
-            const int64_t row = __shfl_sync(0xffffffffu, my_row, kk);
-            // a key past the list's end copies no byte (its row is zero-filled)
-            const char* src = row != 0 ? reinterpret_cast<const char*>(row) : reinterpret_cast<const char*>(a.kv);
-            const uint32_t nbytes = row != 0 ? 16u : 0u;
+          // part by part, each as soon as the value product frees it: the
+          // part's 16 or 24 pieces of each of the warp's rows, consecutive
+          // lanes taking consecutive pieces of a row (whole 128-byte lines)
 #pragma unroll
-            for (int q0 = 0; q0 < 72; q0 += 32) {
-              const int piece = q0 + lane;  // 0..71
-              if (piece < 72) {
-                const int cc = piece >> 3, within = piece & 7;
-                const uint32_t d = smem_u32(dst + cc * kChunk + key * 128 + ((within ^ (key & 7)) << 4));
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src + piece * 16),
-                             "r"(nbytes)
-                             : "memory");
-              }
+          for (int m = 0; m < kParts; ++m) {
+            if (!ok || !mbar_wait(&sh.empty[stage][m], phase ^ 1)) {
+              ok = false;
+              break;
             }
+            constexpr int kPieces[kParts] = {16, 16, 16, 24};
+            const int np = kPieces[m], p0 = part_first_chunk(m) * 8;
+#pragma unroll 4
+            for (int idx = lane; idx < KW * np; idx += 32) {
+              const int kk = idx / np, piece = p0 + idx % np;
+              const int key = pw * KW + kk;
+              const int64_t row = __shfl_sync(0xffffffffu, my_row, kk);
+              // a key past the list's end copies no byte (its row is zero-filled)
+              const char* src = row != 0 ? reinterpret_cast<const char*>(row) : reinterpret_cast<const char*>(a.kv);
+              const uint32_t nbytes = row != 0 ? 16u : 0u;
+              const int cc = piece >> 3, within = piece & 7;
+              const uint32_t d = smem_u32(dst + cc * kChunk + key * 128 + ((within ^ (key & 7)) << 4));
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src + piece * 16),
+                           "r"(nbytes)
+                           : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[stage][m]))
+                         : "memory");
           }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[stage]))
-                       : "memory");
+          if (!ok) break;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -674,15 +741,22 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           tc_fence_after();
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
             const int sb = j % SB;
-            if (!mbar_wait(&sh.full[stage], phase) || !mbar_wait(&sh.s_free[sb], ((j / SB) & 1) ^ 1)) {
+            if (!mbar_wait(&sh.s_free[sb], ((j / SB) & 1) ^ 1)) {
               ok = false;
               break;
             }
-            tc_fence_after();
             const uint64_t b0 = d_kv + (uint64_t)stage * kStageUnits;
             const uint32_t s_col = tmem + TP::kColS + sb * 64;
+            // the tile's parts in order, each once it has landed
 #pragma unroll
-            for (int c = 0; c < 9; ++c)
+            for (int c = 0; c < 9; ++c) {
+              if (c < 8 && (c & 1) == 0) {
+                if (!mbar_wait(&sh.full[stage][c >> 1], phase)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = b0 + (uint64_t)(c * (kChunk >> 4) + kk * 2);
@@ -692,6 +766,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
                 else  // A = Q chunk c in TMEM
                   mma_ts(s_col, tmem + kColQ + ((c - TP::kQSmemChunks) * 4 + kk) * 8, bd, id_qk, acc);
               }
+            }
+            if (!ok) break;
             mma_commit(&sh.s_full[sb]);
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
@@ -710,8 +786,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
             const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;
             const uint64_t p1 = d_plo + (uint64_t)stage * kPLoStageUnits;
             const uint32_t o0 = tmem + TP::kColO;
-            issue_pv_tile<NR>(o0, v0, p0, p1, id_pv, kt == 0, p_split);
-            mma_commit(&sh.empty[stage]);
+            issue_pv_tile<NR>(o0, v0, p0, p1, id_pv, kt == 0, p_split, sh.empty[stage]);
             mma_commit(&sh.pv_done);
             if (kt + 1 == w.n_kt) mma_commit(&sh.unit_done);
             if (++stage == kStages) stage = 0;
@@ -770,8 +845,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       // into the shared-memory A operand instead, at row tl
       const bool have = row < u.nrows;
       // the rows are in this unit's Q slot of the ring
-      if (!group_wait(&sh.full[stage], sphase)) return false;
-      mbar_wait(&sh.full[stage], sphase);  // every reader observes the phase (returns at once)
+      if (!group_wait(&sh.full[stage][0], sphase)) return false;
+      mbar_wait(&sh.full[stage][0], sphase);  // every reader observes the phase (returns at once)
       const uint8_t* slot = kv + stage * kStageBytes;
 #pragma unroll 1
       for (int c = 0; c < 9; ++c) {
@@ -796,7 +871,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       tc_fence_before();
       named_bar_sync(1, 128);
       if (st_tid == 0) {
-        mbar_arrive(&sh.empty[stage]);
+        for (int m = 0; m < kParts; ++m) mbar_arrive(&sh.empty[stage][m]);
         mbar_arrive(&sh.q_ready);
       }
       if (++stage == kStages) { stage = 0; sphase ^= 1; }
@@ -811,14 +886,20 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       // dense: the first unit's Q slot (stage 0) is filled from here
       if (more && wn.n_kt > 0) {
         if (NR == 64) {
-          if (st_tid == 0) issue_q_tma<NR>(maps, kv, grow_of(wn, 0), &sh.full[0]);
+          if (st_tid == 0) {
+            issue_q_tma<NR>(maps, kv, grow_of(wn, 0), &sh.full[0][0]);
+            for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[0][m]);
+          }
         } else {
-          if (st_tid == 0) mbar_arrive_expect_tx(&sh.full[0], (uint32_t)wn.nrows * (kRow * 2));
+          if (st_tid == 0) {
+            mbar_arrive_expect_tx(&sh.full[0][0], (uint32_t)wn.nrows * (kRow * 2));
+            for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[0][m]);
+          }
           if (st_tid < wn.nrows) {
             const int64_t g = grow_of(wn, st_tid);
             uint8_t* qdst = kv + st_tid * PP::kQRowBytes;
-            bulk_load(qdst, a.q_nope + g * a.q_nope_stride, kNope * 2, &sh.full[0]);
-            bulk_load(qdst + kNope * 2, a.q_pe + g * a.q_pe_stride, kRope * 2, &sh.full[0]);
+            bulk_load(qdst, a.q_nope + g * a.q_nope_stride, kNope * 2, &sh.full[0][0]);
+            bulk_load(qdst + kNope * 2, a.q_pe + g * a.q_pe_stride, kRope * 2, &sh.full[0][0]);
           }
         }
       }
@@ -871,11 +952,19 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           tile_valid = min(cur_sh.Lr - kbase, kKeyTile);
         }
         float pmax = -INFINITY;
+        if (kslice * KPT + KPT <= valid) {  // this thread sees every key of its slice (all tiles but a row's last)
 #pragma unroll
-        for (int e = 0; e < KPT; ++e) {
-          const float v = kslice * KPT + e < valid ? s[e] * scale_log2 : -INFINITY;
-          s[e] = v;
-          pmax = fmaxf(pmax, v);
+          for (int e = 0; e < KPT; ++e) {
+            s[e] *= scale_log2;
+            pmax = fmaxf(pmax, s[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < KPT; ++e) {
+            const float v = kslice * KPT + e < valid ? s[e] * scale_log2 : -INFINITY;
+            s[e] = v;
+            pmax = fmaxf(pmax, v);
+          }
         }
         sh.red[j & 1][kslice * NR + row] = pmax;
         tc_fence_before();
@@ -898,7 +987,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           if (row_lead) sh.alpha[row] = alpha;
           // P^T in the k_pe chunk of this tile's stage (QK^T of the tile, its
           // only reader, is complete).  For fp32 outputs P goes in as bf16 hi
-          // and lo = bf16(P - hi), so hi + lo carries P to ~2^-17.
+          // and lo = bf16(P - hi), so hi + lo carries P to ~2^-16.
           const int roff = (row >> 3) * 1024 + (row & 7) * 128;
           uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + roff;
           uint8_t* prow_lo = PP::kPLoInChunk ? prow + PP::kPBytes : p_lo_buf + stage * PP::kPBytes + roff;
@@ -911,12 +1000,16 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
               const float p0 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e] - m_ref) : 0.f;
               const float p1 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e + 1] - m_ref) : 0.f;
               sum += p0 + p1;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-              hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
               if (p_split) {
-                const float2 hf = __bfloat1622float2(h2);
-                const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                // hi = P truncated to bf16 (its top 16 bits, one byte permute
+                // for the pair), lo = bf16(P - hi): hi + lo carries P to 2^-16
+                const uint32_t t0 = __float_as_uint(p0) & 0xffff0000u, t1 = __float_as_uint(p1) & 0xffff0000u;
+                hi[e] = __byte_perm(t0, t1, 0x7632);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __uint_as_float(t0), p1 - __uint_as_float(t1));
                 lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+              } else {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
               }
             }
             const int piece = kslice * (KPT / 8) + c8;  // 16-byte piece (8 keys) of the row
@@ -991,7 +1084,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
         sh.inv_l[row] = live ? 1.f / lt : 0.f;
         if (row < w.nrows) {
           const float lse = live ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
-          if (partial) a.part_lse[chunk_slot(w.cta0, w.split, NR) + row] = lse;
+          if (partial) a.part_lse[chunk_slot(w.cta0, w.split, NR, it.S) + row] = lse;
           else a.lse[grow(row)] = lse;
         }
       }
@@ -1022,7 +1115,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
             if (n >= w.nrows) break;
             const float v = __uint_as_float(o[p][e]) * sh.inv_l[n];
             if (partial) {
-              const int64_t slot = chunk_slot(w.cta0, w.split, NR) + n;
+              const int64_t slot = chunk_slot(w.cta0, w.split, NR, it.S) + n;
               a.part_o[slot * kNope + dim] = v;
             } else if (a.out_f32) {
               static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;

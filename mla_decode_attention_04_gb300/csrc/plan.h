@@ -32,6 +32,7 @@ struct DecodePlan {
   int32_t rows_per_group;  // rows (token, head) per work unit: 16, 32 or 64
   int32_t grid;            // decode CTAs
   int32_t unit_penalty;    // balancing cost of a unit start, in 64-key tiles
+  int32_t gang;            // CTAs per gang (1: none); grid is a multiple of it
   size_t off_desc, off_plse, off_po, total;
 };
 
@@ -55,18 +56,27 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   const int64_t max_key_tiles = (max_local + kKeyTile - 1) / kKeyTile;
   const int64_t groups_ub = ((int64_t)T * H + NR - 1) / NR + B;  // >= sum_b ceil(q_len_b H / NR)
   const int64_t items_ub = groups_ub * max_key_tiles;
-  int64_t g = num_sms > 0 ? num_sms : 148;
-  // num_splits > 0 caps the grid at num_splits CTAs per row group; with
-  // balanced ranges a row group of average size is then cut into about
-  // num_splits KV chunks
+  const int64_t sms = num_sms > 0 ? num_sms : 148;
+  // Gangs: when a request has 2 to 8 row groups, the grid runs in gangs of
+  // that many CTAs (one per row group) over shared tile ranges, so the row
+  // groups' reads of a key tile come close together and L2 serves all but
+  // the first.  Without gangs the groups of a request stream the same tiles
+  // at different times, each from HBM.
+  const int64_t groups_max = ((int64_t)max_query_len * H + NR - 1) / NR;
+  p.gang = (groups_max >= 2 && groups_max <= 8 && groups_max * 2 <= sms) ? (int32_t)groups_max : 1;
+  const int64_t S = p.gang;
+  int64_t g = sms / S;  // gangs (or CTAs)
+  // num_splits > 0 caps the grid at num_splits CTAs per row group (gangs:
+  // per request); with balanced ranges a row group of average size is then
+  // cut into about num_splits KV chunks
   if (num_splits > 0) {
-    const int64_t groups_lb = ((int64_t)T * H + NR - 1) / NR;
-    const int64_t cap = (int64_t)num_splits * (groups_lb > 0 ? groups_lb : 1);
+    const int64_t units_lb = S > 1 ? ((int64_t)T + max_query_len - 1) / max_query_len : ((int64_t)T * H + NR - 1) / NR;
+    const int64_t cap = (int64_t)num_splits * (units_lb > 0 ? units_lb : 1);
     if (g > cap) g = cap;
   }
   if (g > items_ub) g = items_ub;
   if (g < 1) g = 1;
-  p.grid = (int32_t)g;
+  p.grid = (int32_t)(g * S);
   size_t off = sizeof(WorkspaceHeader);
   p.off_desc = off;
   off = align_up(off + 16 * (size_t)p.grid, 256);
@@ -108,12 +118,13 @@ __global__ void prep_kernel(PrepArgs a);
 // The split-merge kernel: the LSE merge of the chunks of every row group the
 // decode cut over several CTAs (entry c of the split table: {chunks, first
 // global (token, head) row, rows, 0}; chunk k's partial rows at
-// chunk_slot(c, k, NR)).  Block (c, s) merges rows [4 s, 4 s + 4) of entry c.
+// chunk_slot(c, k, NR, cta_stride)).  Block (c, s) merges rows [4 s, 4 s + 4) of entry c.
 struct SplitMergeArgs {
   const int4* split_desc;  // [grid]
   const float* part_lse;   // [2 grid NR]
   const float* part_o;     // [2 grid NR, 512]
   int32_t rows_per_group, grid;
+  int32_t cta_stride;      // CTAs between a pair's consecutive chunks (the gang size, or 1)
   int64_t num_rows;        // T * H
   void* out;               // [T, H, 512]
   int32_t out_f32;

@@ -50,8 +50,8 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
   float4 v[kAhead][R];
 #pragma unroll
   for (int k = 0; k < kAhead; ++k) {
-    const bool exists = c + k < a.grid;
-    const int64_t slot = chunk_slot(c, k, NR) + n0;
+    const bool exists = c + k * a.cta_stride < a.grid;
+    const int64_t slot = chunk_slot(c, k, NR, a.cta_stride) + n0;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       l[k][r] = exists ? __ldcg(a.part_lse + slot + r) : -INFINITY;
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
   const int nsplit = d.x, nrows = d.z;
   const int64_t g0 = d.y;
   if (nsplit < 2 || n0 >= nrows) return;  // no split row group starts at CTA c (or no rows here)
-  if ((int64_t)c + nsplit > a.grid || nrows > NR || g0 < 0 || g0 + nrows > a.num_rows) {
+  if ((int64_t)c + (int64_t)(nsplit - 1) * a.cta_stride >= a.grid || nrows > NR || g0 < 0 ||
+      g0 + nrows > a.num_rows) {
     if (threadIdx.x == 0 && n0 == 0) record_check(a.hdr, kCheckBadSplitEntry);
     return;
   }
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
       const bool use = sp + k < nsplit;
-      const int64_t slot = chunk_slot(c, sp + k, NR) + n0;
+      const int64_t slot = chunk_slot(c, sp + k, NR, a.cta_stride) + n0;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         l[k][r] = use && n0 + r < nrows ? __ldcg(a.part_lse + slot + r) : -INFINITY;

@@ -95,6 +95,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tmap, int32_t c0, int32_t c1, int32_t c2,
                                             uint64_t* bar, uint64_t policy) {
   asm volatile(

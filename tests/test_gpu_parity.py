@@ -88,6 +88,9 @@ EDGE = {
     "heads_128": dict(seq_lens=[200, 65], q_lens=[2, 1], num_heads=128, dcp_world=8, page_size=64),
     "many_splits": dict(seq_lens=[9000], q_lens=[3], num_heads=16, dcp_world=2, page_size=64),
     "d8_ragged_shards": dict(seq_lens=[1001, 64, 7], q_lens=[2, 1, 7], num_heads=16, dcp_world=8, page_size=16),
+    # 64-row units in gangs of 3 CTAs, requests with 1, 2 or 3 row groups
+    "gangs_mixed_groups": dict(seq_lens=[900, 40, 2000, 7, 1500], q_lens=[3, 1, 2, 3, 3], num_heads=64, dcp_world=2,
+                               page_size=32),
 }
 
 

@@ -5,7 +5,11 @@ Every (source, row group) pair contributes `pen` work-free items and then its
 key tiles to one list of W items; CTA c of G takes items [c W / G, (c + 1) W /
 G).  A pair cut by range boundaries becomes chunks on consecutive CTAs; chunk
 k of a pair whose first chunk CTA c0 holds writes its partial rows at
-chunk_slot(c0, k); CTA c0 publishes the pair in its split-table entry.  The
+chunk_slot(c0, k); CTA c0 publishes the pair in its split-table entry.  With
+gangs of S CTAs a source's items are counted once (not once per row group):
+gang j = c // S takes items [j W / G, (j + 1) W / G) of G gangs and its CTA
+c % S runs that row group of every source over them, so a pair's chunks are
+on CTAs S apart (chunk k of the pair starting on CTA c0 on CTA c0 + k S).  The
 kernels compute quotients with a float estimate corrected by exact integer
 products; that estimate is emulated here in float32.
 """
@@ -26,21 +30,26 @@ def range_owner(i, W, G):
     return quot_floor((i + 1) * G - 1, W)
 
 
-def chunk_slot(c0, k):
-    return 2 * c0 + 1 if k == 0 else 2 * (c0 + k)
+def chunk_slot(c0, k, stride=1):
+    return 2 * c0 + 1 if k == 0 else 2 * (c0 + k * stride)
 
 
-def plan(pairs_per_source, tiles_per_source, pen, grid):
+def plan(pairs_per_source, tiles_per_source, pen, grid, S=1):
     """Units of every CTA: (source, group, first tile, tiles, cta0, split, nsplit)."""
-    items = [g * (nt + pen) if nt > 0 else 0 for g, nt in zip(pairs_per_source, tiles_per_source)]
+    if S > 1:
+        items = [nt + pen if nt > 0 and g > 0 else 0 for g, nt in zip(pairs_per_source, tiles_per_source)]
+    else:
+        items = [g * (nt + pen) if nt > 0 else 0 for g, nt in zip(pairs_per_source, tiles_per_source)]
     W = sum(items)
-    G = min(grid, W) if W > 0 else 1
+    nplan = grid // S
+    G = min(nplan, W) if W > 0 else 1
     base = np.concatenate([[0], np.cumsum(items)]).astype(np.int64)
     units = [[] for _ in range(grid)]
     for c in range(grid):
-        if W == 0 or c >= G:
+        me, gg = c // S, c % S
+        if W == 0 or me >= G:
             continue
-        lo, hi = quot_floor(c * W, G), quot_floor((c + 1) * W, G)
+        lo, hi = quot_floor(me * W, G), quot_floor((me + 1) * W, G)
         i = lo
         b = int(np.searchsorted(base, lo, side="right") - 1)
         while i < hi and b < len(items):
@@ -50,27 +59,32 @@ def plan(pairs_per_source, tiles_per_source, pen, grid):
                 continue
             nt = tiles_per_source[b]
             vlen = nt + pen
-            g = quot_floor(i - base[b], vlen)
-            item0 = base[b] + g * vlen + pen
+            g = gg if S > 1 else quot_floor(i - base[b], vlen)
+            item0 = base[b] + (0 if S > 1 else g * vlen) + pen
             if i < item0:
                 i = item0
             if i >= hi:
                 break
             end = min(hi, item0 + nt)
-            cta0 = range_owner(item0, W, G)
-            nsplit = range_owner(item0 + nt - 1, W, G) - cta0 + 1
-            units[c].append((b, g, i - item0, end - i, cta0, c - cta0, nsplit))
+            if g >= pairs_per_source[b]:
+                i = end
+                continue
+            own0 = range_owner(item0, W, G)
+            cta0 = own0 * S + gg
+            nsplit = range_owner(item0 + nt - 1, W, G) - own0 + 1
+            units[c].append((b, g, i - item0, end - i, cta0, me - own0, nsplit))
             i = end
     return units, W, G
 
 
-def check_plan(pairs, tiles, pen, grid):
-    units, W, G = plan(pairs, tiles, pen, grid)
+def check_plan(pairs, tiles, pen, grid, S=1):
+    units, W, G = plan(pairs, tiles, pen, grid, S)
     covered = {}
     for c, us in enumerate(units):
         for k, (b, g, t0, n, cta0, split, nsplit) in enumerate(us):
             assert n > 0
-            assert 0 <= split < nsplit and cta0 + split == c
+            assert 0 <= split < nsplit and cta0 + split * S == c
+            assert S == 1 or g == c % S
             for t in range(t0, t0 + n):
                 assert (b, g, t) not in covered, "a tile in two units"
                 covered[(b, g, t)] = c
@@ -81,18 +95,18 @@ def check_plan(pairs, tiles, pen, grid):
     # every tile of every pair exactly once
     expect = {(b, g, t) for b, (gs, nt) in enumerate(zip(pairs, tiles)) for g in range(gs) for t in range(nt)}
     assert set(covered) == expect
-    # a pair's chunks: nsplit consecutive CTAs in tile order; partial slots unique and in range
+    # a pair's chunks: nsplit CTAs S apart in tile order; partial slots unique and in range
     slots = set()
     for b, (gs, nt) in enumerate(zip(pairs, tiles)):
         for g in range(gs):
             if nt == 0:
                 continue
             ctas = [covered[(b, g, t)] for t in range(nt)]
-            assert ctas == sorted(ctas) and set(ctas) == set(range(ctas[0], ctas[-1] + 1))
-            nsplit = ctas[-1] - ctas[0] + 1
+            assert ctas == sorted(ctas) and set(ctas) == set(range(ctas[0], ctas[-1] + 1, S))
+            nsplit = (ctas[-1] - ctas[0]) // S + 1
             if nsplit > 1:
                 for k in range(nsplit):
-                    s = chunk_slot(ctas[0], k)
+                    s = chunk_slot(ctas[0], k, S)
                     assert s not in slots and 0 <= s < 2 * grid
                     slots.add(s)
     # quotient estimate = exact quotient
@@ -133,3 +147,34 @@ def test_quotient_estimate_on_large_lists():
         for i in (0, 1, W // 3, W // 2 + 17, W - 2, W - 1):
             assert range_owner(i, W, G) == -(-((i + 1) * G) // W) - 1
             assert quot_floor(i, W) == 0 or quot_floor(i * G, W) == (i * G) // W
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_gang_plans(seed):
+    # gangs of S CTAs (S = the largest request's row groups, 2..8), requests
+    # with fewer groups (mixed query lengths) and without keys included
+    rng = np.random.default_rng(1000 + seed)
+    S = int(rng.integers(2, 9))
+    B = int(rng.integers(1, 120))
+    pairs = rng.integers(1, S + 1, size=B).tolist()
+    pairs[int(rng.integers(0, B))] = S
+    tiles = rng.integers(0, 400, size=B).tolist()
+    if seed % 4 == 0:
+        tiles = [int(x) if rng.random() < 0.6 else 0 for x in tiles]
+    grid = (int(rng.choice([2 * S, 37, 148, 152])) // S) * S
+    pen = int(rng.choice([0, 4]))
+    check_plan(pairs, tiles, pen, grid, S)
+
+
+def test_long_context_gang_plan():
+    # 32 requests x 4 row groups of 64 rows (2 tokens x 128 heads), ~384
+    # tiles each over all 8 shards, 38 gangs of 4 on 152 CTAs: every CTA
+    # streams the same tiles as the 3 other members of its gang
+    rng = np.random.default_rng(3)
+    tiles = rng.integers(256, 513, size=32).tolist()
+    units = check_plan([4] * 32, tiles, 4, 152, 4)
+    for j in range(38):
+        ranges = [[(b, t0, n) for (b, g, t0, n, *_rest) in units[4 * j + gg]] for gg in range(4)]
+        assert all(r == ranges[0] for r in ranges)
+    per_cta = [sum(u[3] for u in us) for us in units]
+    assert max(per_cta) - min(per_cta) <= 12
