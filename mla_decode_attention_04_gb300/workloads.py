@@ -216,6 +216,24 @@ def custom(seq_lens, q_lens, num_heads, dcp_world, page_size=64, seed=0, q_std=1
 # --------------------------------------------------------------- named configs
 
 
+def fp8_cache(w: "Workload", kv_scale: float = 0.25):
+    """An FP8 E4M3 latent cache for workload w: the bf16 cache values divided
+    by ``kv_scale`` and rounded to E4M3 codes (torch's float8_e4m3fn cast),
+    stored as uint8 [total_pages, page_size, 576] in the same page layout (a
+    shard's slice at the same page range).  Returns (codes, per-shard views).
+    Input drawing only: the cache holds kv_scale * decode(code), a value
+    near the bf16 draw."""
+    x = w.cache_all.float() / float(kv_scale)
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    views = [codes[s.page_base:s.page_base + s.cache.shape[0]] for s in w.shards]
+    return codes, views
+
+
+def e4m3_values(codes: torch.Tensor) -> torch.Tensor:
+    """float32 values of uint8 E4M3 codes (torch's float8_e4m3fn widening)."""
+    return codes.view(torch.float8_e4m3fn).float()
+
+
 def tiny(device="cpu", **kw):
     """4 requests, lengths {6,37,130,300}, q_len {4,1,2,2} (request 0 is the
     6-key / 4-query case of the mask tables), D=2, H=16, page 16, q scaled by

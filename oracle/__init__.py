@@ -63,6 +63,11 @@ def _bind(lib):
     lib.mla_oracle_dcp_decode.argtypes = [vp, vp, vp, i64, vp, i64, vp, vp, i64, i64, i64, i64, f64, i64, i64,
                                           vp, vp, vp, vp, vp]
     lib.mla_oracle_dcp_decode.restype = None
+    lib.mla_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.mla_oracle_e4m3_to_double.restype = f64
+    lib.mla_oracle_dcp_decode_kv8.argtypes = [vp, vp, vp, f64, i64, vp, i64, vp, vp, i64, i64, i64, i64, f64, i64,
+                                              i64, vp, vp, vp, vp, vp]
+    lib.mla_oracle_dcp_decode_kv8.restype = None
     lib.mla_oracle_sparse_dcp_decode.argtypes = [vp, vp, vp, i64, vp, i64, vp, vp, i64, i64, vp, i64, vp, i64, i64,
                                                  f64, i64, i64, vp, vp, vp, vp, vp]
     lib.mla_oracle_sparse_dcp_decode.restype = None
@@ -171,6 +176,41 @@ def dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, qsl, D, r, scale, 
         lib.mla_oracle_dcp_decode(_p(q_nope), _p(q_pe), _p(kv_cache), ps, _p(block_table), block_table.shape[1],
                                   _p(seq_lens), _p(qsl), B, H, D, r, float(scale), rng[0], rng[1], _p(out[o:]),
                                   _p(lse[o:]), _p(counts[o:]), ctypes.cast(keys, ctypes.c_void_p), _p(s))
+
+    _parallel(run, _token_ranges(T, t_lo, t_hi, threads or default_threads()))
+    return out, lse, counts
+
+
+def e4m3_to_double(code: int, lib=None) -> float:
+    """Exact value of one FP8 E4M3 code (NaN for S.1111.111)."""
+    return float((lib or load()).mla_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def dcp_decode_kv8(q_nope, q_pe, kv_cache, kv_scale, block_table, seq_lens, qsl, D, r, scale, t_lo=0, t_hi=None,
+                   threads=None, lib=None):
+    """dcp_decode over an FP8 E4M3 cache: kv_cache uint8 codes [num_blocks,
+    page_size, 576], each value kv_scale * decode(code).  Returns (out [n,H,512],
+    lse [n,H], row_counts int32 [n]) for tokens [t_lo, t_hi)."""
+    lib = lib or load()
+    q_nope, q_pe, kv_cache = _c(q_nope, np.uint16), _c(q_pe, np.uint16), _c(kv_cache, np.uint8)
+    block_table, seq_lens, qsl = _c(block_table, np.int32), _c(seq_lens, np.int32), _c(qsl, np.int32)
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    ps = kv_cache.shape[1]
+    t_hi = T if t_hi is None else t_hi
+    out = np.full((t_hi - t_lo, H, KV_LORA_RANK), np.nan)
+    lse = np.full((t_hi - t_lo, H), np.nan)
+    counts = np.full((t_hi - t_lo,), -1, dtype=np.int32)
+    maxL = int(seq_lens.max()) if B else 0
+
+    def run(rng):
+        keys = (ctypes.c_void_p * max(1, maxL))()
+        s = np.empty(max(1, maxL))
+        o = rng[0] - t_lo
+        lib.mla_oracle_dcp_decode_kv8(_p(q_nope), _p(q_pe), _p(kv_cache), float(kv_scale), ps, _p(block_table),
+                                      block_table.shape[1], _p(seq_lens), _p(qsl), B, H, D, r, float(scale), rng[0],
+                                      rng[1], _p(out[o:]), _p(lse[o:]), _p(counts[o:]),
+                                      ctypes.cast(keys, ctypes.c_void_p), _p(s))
 
     _parallel(run, _token_ranges(T, t_lo, t_hi, threads or default_threads()))
     return out, lse, counts

@@ -186,6 +186,91 @@ void mla_oracle_dcp_decode(const uint16_t *q_nope, const uint16_t *q_pe,
   }
 }
 
+/* ------------------------------------- dense, one DCP shard, FP8 cache -- */
+
+/* FP8 latent cache (an extension: the [P3] backend rejects an FP8 cache).
+ * Reading taken: every value of a cache row (kv_c and k_pe) is stored as one
+ * OCP FP8 E4M3 code -- 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals at exponent 0, no infinities, S.1111.111 is NaN -- and
+ * the whole tensor shares one dequantisation scale: the value is
+ * kv_scale * decode(code).  The decode below is that definition, exact in
+ * double. */
+double mla_oracle_e4m3_to_double(uint8_t code) {
+  int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);              /* m/8 * 2^(1-7) */
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);      /* 1.m * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+/* attend_row with FP8 key rows: each value is kv_scale * decode(code). */
+static void attend_row_kv8(const uint16_t *qn, const uint16_t *qp,
+                           const uint8_t *const *keys, int64_t nkeys,
+                           double kv_scale, double scale, double *s,
+                           double *out, double *lse) {
+  for (int d = 0; d < KV_LORA_RANK; ++d) out[d] = 0.0;
+  if (nkeys == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t k = 0; k < nkeys; ++k) {
+    const uint8_t *row = keys[k];
+    double acc = 0.0;
+    for (int d = 0; d < KV_LORA_RANK; ++d)
+      acc += bf16_to_double(qn[d]) * (kv_scale * mla_oracle_e4m3_to_double(row[d]));
+    for (int e = 0; e < ROPE_DIM; ++e)
+      acc += bf16_to_double(qp[e]) *
+             (kv_scale * mla_oracle_e4m3_to_double(row[KV_LORA_RANK + e]));
+    s[k] = scale * acc;
+    if (s[k] > m) m = s[k];
+  }
+  double z = 0.0;
+  for (int64_t k = 0; k < nkeys; ++k) z += exp(s[k] - m);
+  double l = m + log(z);
+  for (int64_t k = 0; k < nkeys; ++k) {
+    double p = exp(s[k] - l);
+    const uint8_t *row = keys[k];
+    for (int d = 0; d < KV_LORA_RANK; ++d)
+      out[d] += p * (kv_scale * mla_oracle_e4m3_to_double(row[d]));
+  }
+  *lse = l;
+}
+
+/* mla_oracle_dcp_decode over an FP8 cache slice [pages][page_size][576]
+ * bytes with dequantisation scale kv_scale. */
+void mla_oracle_dcp_decode_kv8(const uint16_t *q_nope, const uint16_t *q_pe,
+                               const uint8_t *kv_cache, double kv_scale,
+                               int64_t page_size, const int32_t *block_table,
+                               int64_t bt_stride, const int32_t *seq_lens,
+                               const int32_t *qsl, int64_t B, int64_t H,
+                               int64_t D, int64_t r, double scale,
+                               int64_t t_lo, int64_t t_hi, double *out,
+                               double *lse, int32_t *row_counts,
+                               const uint8_t **key_scratch,
+                               double *s_scratch) {
+  for (int64_t t = t_lo; t < t_hi; ++t) {
+    int64_t b = request_of(qsl, B, t);
+    int64_t L = seq_lens[b], q_len = qsl[b + 1] - qsl[b];
+    int64_t P = L - q_len + (t - qsl[b]);
+    int64_t Lr = mla_oracle_local_len(L, D, r);
+    int64_t n = 0;
+    for (int64_t j = 0; j < Lr; ++j)
+      if (mla_oracle_key_visible(P, D, r, j)) {
+        int64_t page = block_table[b * bt_stride + j / page_size];
+        key_scratch[n++] = kv_cache + (page * page_size + j % page_size) * ROW_WIDTH;
+      }
+    row_counts[t - t_lo] = (int32_t)n;
+    for (int64_t h = 0; h < H; ++h)
+      attend_row_kv8(q_nope + (t * H + h) * KV_LORA_RANK,
+                     q_pe + (t * H + h) * ROPE_DIM, key_scratch, n, kv_scale,
+                     scale, s_scratch,
+                     out + ((t - t_lo) * H + h) * KV_LORA_RANK,
+                     lse + (t - t_lo) * H + h);
+  }
+}
+
 /* ------------------------------------------------ sparse, one DCP shard -- */
 
 /* [P4] sparse MLA: query token t attends to the keys listed in

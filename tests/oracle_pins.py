@@ -437,9 +437,83 @@ def _positions(w):
     return out
 
 
+# ----------------------------------------------------------- FP8 cache
+
+
+def check_e4m3_decode_library(lib):
+    """Every FP8 E4M3 code decodes to torch's float8_e4m3fn value (NaN for
+    S.1111.111, signed zero, the subnormals at exponent 0, 448 at the top)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c, lib=lib) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def _fp8_case(kv_scale, seed):
+    w = _dense_inputs([9, 70, 33], [2, 1, 3], H=3, D=2, seed=seed, ps=8)
+    codes, views = wl.fp8_cache(w, kv_scale)
+    # the bf16 cache holding exactly kv_scale * decode(code) (an E4M3 value
+    # has at most 4 significant bits, times 1 or 0.75 at most 6: exact in bf16)
+    twin = (wl.e4m3_values(codes) * kv_scale).to(torch.bfloat16)
+    return w, views, twin
+
+
+def check_kv8_reduces_to_bf16(lib):
+    """The FP8 shard decode equals the (pinned) bf16 shard decode on a bf16
+    cache holding the dequantised values, for kv_scale 1 and 0.75."""
+    for kv_scale, seed in ((1.0, 11), (0.75, 12)):
+        w, views, twin = _fp8_case(kv_scale, seed)
+        for r, sh in enumerate(w.shards):
+            tw = twin[sh.page_base:sh.page_base + sh.cache.shape[0]]
+            args = (w.seq_lens.numpy(), w.query_start_loc.numpy(), w.dcp_world, r, w.scale)
+            o8, l8, c8 = oracle.dcp_decode_kv8(_bits(w.q_nope), _bits(w.q_pe), views[r].numpy(), kv_scale,
+                                              sh.block_table.numpy(), *args, lib=lib, threads=1)
+            ob, lb, cb = oracle.dcp_decode(_bits(w.q_nope), _bits(w.q_pe), _bits(tw), sh.block_table.numpy(), *args,
+                                           lib=lib, threads=1)
+            assert np.array_equal(c8, cb)
+            assert np.array_equal(np.isneginf(l8), np.isneginf(lb))
+            np.testing.assert_allclose(o8, ob, rtol=0, atol=1e-12)
+            fin = np.isfinite(lb)
+            np.testing.assert_allclose(l8[fin], lb[fin], rtol=0, atol=1e-12)
+
+
+def check_kv8_zero_query(lib):
+    """q = 0 over an FP8 cache: LSE = ln(n visible), output = kv_scale times
+    the mean of the decoded visible kv_c rows (decoded here by torch)."""
+    kv_scale = 0.5
+    w, views, _ = _fp8_case(kv_scale, 13)
+    w.q_nope.zero_()
+    w.q_pe.zero_()
+    codes, _ = wl.fp8_cache(w, kv_scale)
+    vals = wl.e4m3_values(codes).double().numpy()
+    qsl = w.query_start_loc.numpy()
+    for r, sh in enumerate(w.shards):
+        out, lse, counts = oracle.dcp_decode_kv8(_bits(w.q_nope), _bits(w.q_pe), views[r].numpy(), kv_scale,
+                                                 sh.block_table.numpy(), w.seq_lens.numpy(), qsl, 2, r, w.scale,
+                                                 lib=lib, threads=1)
+        bt = sh.block_table.numpy()
+        for b, L in enumerate(w.seq_lens.tolist()):
+            for i in range(qsl[b + 1] - qsl[b]):
+                t = qsl[b] + i
+                P = L - (qsl[b + 1] - qsl[b]) + i
+                vis = [p // 2 for p in range(r, L, 2) if p <= P]  # local slots, brute force
+                assert counts[t] == len(vis)
+                if not vis:
+                    assert np.all(np.isneginf(lse[t])) and np.all(out[t] == 0.0)
+                    continue
+                rows = np.stack([vals[sh.page_base + bt[b, j // 8], j % 8, :512] for j in vis])
+                np.testing.assert_allclose(out[t], np.broadcast_to(kv_scale * rows.mean(0), out[t].shape), rtol=0,
+                                           atol=1e-12)
+                np.testing.assert_allclose(lse[t], math.log(len(vis)), rtol=0, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_mask_tables, check_seqlen_example, check_count_closed_form, check_sdpa_d1, check_two_key_closed_form,
     check_zero_query_mean, check_identical_keys, check_paged_equals_logical, check_shard_merge_equals_unsharded,
     check_merge_lse_logsumexp, check_merge_ignores_empty_shards, check_empty_row, check_wuv_library,
     check_wuv_commutes, check_sparse_full_prefix_is_dense, check_sparse_subset, check_two_stage_decomposition,
+    check_e4m3_decode_library, check_kv8_reduces_to_bf16, check_kv8_zero_query,
 ]

@@ -33,7 +33,8 @@ MUTANTS = [
      "for (int d = 0; d < KV_LORA_RANK - 1; ++d) out[d] += p", None),
     ("position_dense", "int64_t P = L - q_len + (t - qsl[b]);", "int64_t P = L - q_len + (t - qsl[b]) - 1;", 0),
     ("position_dcp", "int64_t P = L - q_len + (t - qsl[b]);", "int64_t P = L - q_len + (t - qsl[b]) - 1;", 1),
-    ("position_sparse", "int64_t P = L - q_len + (t - qsl[b]);", "int64_t P = L - q_len + (t - qsl[b]) + 1;", 2),
+    ("position_kv8", "int64_t P = L - q_len + (t - qsl[b]);", "int64_t P = L - q_len + (t - qsl[b]) - 1;", 2),
+    ("position_sparse", "int64_t P = L - q_len + (t - qsl[b]);", "int64_t P = L - q_len + (t - qsl[b]) + 1;", 3),
     ("page_offset", "return kv_cache + (page * page_size + j % page_size) * ROW_WIDTH;",
      "return kv_cache + (page * page_size + (j + 1) % page_size) * ROW_WIDTH;", None),
     ("sparse_future_kept", "if (p < 0 || p > P) continue;", "if (p < 0) continue;", None),
@@ -44,6 +45,16 @@ MUTANTS = [
     ("merge_weight_max", "double w = exp(lses[(r * T + t) * H + h] - L);",
      "double w = exp(lses[(r * T + t) * H + h] - m);", None),
     ("merge_lse_without_max", "double L = m + log(z);", "double L = log(z);", None),
+    ("e4m3_exponent_bias", "else v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "else v = ldexp(1.0 + (double)m / 8.0, e - 8);", None),
+    ("e4m3_subnormal_scale", "if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)m, -10);", None),
+    ("e4m3_sign_dropped", "return sign ? -v : v;", "return v;", None),
+    ("kv8_value_scale_dropped", "out[d] += p * (kv_scale * mla_oracle_e4m3_to_double(row[d]));",
+     "out[d] += p * mla_oracle_e4m3_to_double(row[d]);", None),
+    ("kv8_rope_term_dropped", "acc += bf16_to_double(qp[e]) *\n             (kv_scale", "acc += 0.0 *\n             (kv_scale",
+     None),
+    ("kv8_page_offset", "key_scratch[n++] = kv_cache + (page * page_size + j % page_size) * ROW_WIDTH;",
+     "key_scratch[n++] = kv_cache + (page * page_size + (j + 1) % page_size) * ROW_WIDTH;", None),
     ("wuv_transposed", "acc += x[d] * bf16_to_double(w[d * V + v]);",
      "acc += x[d] * bf16_to_double(w[v * KV_LORA_RANK + d]);", None),
 ]
