@@ -37,8 +37,10 @@
  *     are checked by the kernels, which record the first failure in the
  *     workspace status word and skip the offending access; read it with
  *     mla_workspace_status().
- *   - Unsupported features (FP8 cache, other head dims), as in the backend's
- *     constructor gates, return MLA_ERR_UNSUPPORTED.
+ *   - An FP8 E4M3 latent cache is served by the dense _fp8 calls (the
+ *     backend's constructor rejects one; this library adds it); the other
+ *     calls, like the backend, return MLA_ERR_UNSUPPORTED for it, as for other
+ *     head dims.
  */
 #ifndef MLA_DCP_H
 #define MLA_DCP_H
@@ -139,6 +141,43 @@ int mla_dcp_decode(const void *q_nope, int64_t q_nope_row_stride, const void *q_
                    int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
                    void *out, int32_t out_dtype, float *lse, int32_t *row_counts, int32_t num_splits,
                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * mla_dcp_decode_fp8 / mla_dcp_decode_fused_fp8 -- mla_dcp_decode and
+ * mla_dcp_decode_fused over an FP8 latent cache.  "vllm.v1.attention.
+ * backends.mla.flashattn_mla" (FlashAttnMLAImpl.__init__, _forward_decode)
+ * rejects an FP8 KV cache; these calls serve the plainest such cache: every
+ * value of a row (kv_c and k_pe) is one OCP FP8 E4M3 code (1 sign, 4 exponent
+ * bits of bias 7, 3 mantissa bits; subnormals; no infinities; S.1111.111 is
+ * NaN and must not occur) and the whole cache shares one dequantisation
+ * scale, value = kv_scale * decode(code).  Scores and outputs are those of
+ * mla_dcp_decode(_fused) on the dequantised values.
+ *
+ *  kv_cache / kv_caches  device uint8 [num_blocks, page_size, 576] of E4M3
+ *            codes (576 bytes per row), 16-byte aligned; page layout and block
+ *            tables as the bf16 calls.
+ *  kv_scale  finite and > 0.
+ *  workspace at least mla_dcp_decode_workspace_size() (resp.
+ *            mla_dcp_decode_fused_workspace_size()) bytes: those sizes cover
+ *            the bf16 and the FP8 calls.
+ *  Other arguments, launches, stream order and errors as the bf16 calls
+ *  (INVALID_ARG also for a bad kv_scale).
+ * ---------------------------------------------------------------------- */
+int mla_dcp_decode_fp8(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe, int64_t q_pe_row_stride,
+                       const void *kv_cache, int64_t num_blocks, int32_t page_size, float kv_scale,
+                       const int32_t *block_table, int32_t block_table_stride, const int32_t *seq_lens,
+                       const int32_t *query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                       int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
+                       void *out, int32_t out_dtype, float *lse, int32_t *row_counts, int32_t num_splits,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int mla_dcp_decode_fused_fp8(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe,
+                             int64_t q_pe_row_stride, const void *const *kv_caches, const int64_t *num_blocks,
+                             int32_t page_size, float kv_scale, const int32_t *const *block_tables,
+                             int32_t block_table_stride, const int32_t *seq_lens, const int32_t *query_start_loc,
+                             int32_t num_requests, int32_t num_tokens, int32_t num_heads, int32_t max_query_len,
+                             int32_t max_seq_len, int32_t dcp_world, float scale, void *out, int32_t out_dtype,
+                             float *lse, int32_t num_splits, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * mla_sparse_dcp_decode -- the same attention over per-token top-k key lists
@@ -287,6 +326,12 @@ int mla_sparse_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, c
  * query_start_loc, 3 = a pipeline wait gave up, 4 = a split-table entry
  * out of range (an internal inconsistency).  This is the one call that
  * blocks the host.
+ *
+ * A decode CTA whose wait gives up stops issuing work, waits (with a bound
+ * of its own) for every copy and MMA it already issued, frees its tensor
+ * memory and exits, so the call completes and the context stays usable; its
+ * outputs are then unspecified.  The workspace's third 32-bit word then
+ * holds the site of the first wait that gave up (a diagnostic number).
  * ---------------------------------------------------------------------- */
 int mla_workspace_status(const void *workspace, void *stream, int32_t *detail);
 
@@ -342,6 +387,15 @@ int mla_dcp_decode_static_scratch(const void *q_nope, int64_t q_nope_row_stride,
  * how many of the library's kernels ran inside a timed region.
  * ---------------------------------------------------------------------- */
 int64_t mla_kernel_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * mla_debug_set_wait_budget_ns -- test hook: the budget, in ns, of every
+ * pipeline wait inside the decode kernels launched after this call by any
+ * thread of the process (0 restores the default, 2 s).  With a budget too
+ * short for the pipeline, waits give up and the call reports check 3 through
+ * mla_workspace_status; nothing else changes.  Not for production use.
+ * ---------------------------------------------------------------------- */
+void mla_debug_set_wait_budget_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

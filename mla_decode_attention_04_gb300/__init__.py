@@ -32,7 +32,7 @@ EXPORTS = [
     "mla_last_error", "mla_dcp_decode_workspace_size", "mla_dcp_decode", "mla_sparse_dcp_decode_workspace_size",
     "mla_sparse_dcp_decode", "dcp_lse_merge", "mla_workspace_status", "mla_kernel_launch_count",
     "mla_dcp_decode_static_scratch", "mla_dcp_decode_fused_workspace_size", "mla_dcp_decode_fused",
-    "mla_sparse_dcp_decode_fused",
+    "mla_sparse_dcp_decode_fused", "mla_dcp_decode_fp8", "mla_dcp_decode_fused_fp8", "mla_debug_set_wait_budget_ns",
 ]
 
 # Size of the library's fixed device scratch array used by
@@ -78,6 +78,14 @@ def _bind(lib):
     lib.mla_sparse_dcp_decode_fused.restype = ctypes.c_int
     lib.mla_sparse_dcp_decode_fused.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32,
                                                 vp, i32, vp, i32, f32, vp, i32, vp, vp, vp, sz, vp]
+    lib.mla_dcp_decode_fp8.restype = ctypes.c_int
+    lib.mla_dcp_decode_fp8.argtypes = [vp, i64, vp, i64, vp, i64, i32, f32, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                       i32, i32, f32, vp, i32, vp, vp, i32, vp, sz, vp]
+    lib.mla_dcp_decode_fused_fp8.restype = ctypes.c_int
+    lib.mla_dcp_decode_fused_fp8.argtypes = [vp, i64, vp, i64, vp, vp, i32, f32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                             i32, i32, f32, vp, i32, vp, i32, vp, sz, vp]
+    lib.mla_debug_set_wait_budget_ns.restype = None
+    lib.mla_debug_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
     lib.mla_dcp_decode_static_scratch.restype = ctypes.c_int
     lib.mla_dcp_decode_static_scratch.argtypes = [vp, i64, vp, i64, vp, i64, i32, i32, vp, i32, vp, vp, i32, i32, i32,
                                                   i32, i32, i32, i32, f32, vp, i32, vp, vp, i32, vp]
@@ -126,6 +134,12 @@ def _i32(t, name):
     return t
 
 
+def workspace_wait_site(workspace) -> int:
+    """The workspace header's diagnostic word: the site of the first pipeline
+    wait that gave up (0 if none); read after mla_workspace_status."""
+    return int(workspace[8:12].view(torch.int32).item())
+
+
 def decode_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, dcp_world,
                           num_splits=0) -> int:
     return int(load_library().mla_dcp_decode_workspace_size(num_requests, num_tokens, num_heads, max_query_len,
@@ -169,6 +183,86 @@ def mla_dcp_decode(q_nope, q_pe, kv_cache, block_table, seq_lens, query_start_lo
                               _ptr(out), _DT[out.dtype], _ptr(lse), _ptr(row_counts), int(num_splits),
                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse, row_counts
+
+
+def _kv8(kv_cache):
+    if (kv_cache.dtype != torch.uint8 or kv_cache.dim() != 3 or kv_cache.shape[2] != KV_LORA_RANK + ROPE_DIM
+            or not kv_cache.is_contiguous()):
+        raise ValueError("an FP8 kv_cache must be a contiguous uint8 [num_blocks, page_size, 576] tensor of E4M3 codes")
+    return kv_cache.shape[0], kv_cache.shape[1]
+
+
+def mla_dcp_decode_fp8(q_nope, q_pe, kv_cache, kv_scale, block_table, seq_lens, query_start_loc, max_query_len,
+                       max_seq_len, dcp_world, dcp_rank, scale, out=None, lse=None, row_counts=None,
+                       out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None):
+    """mla_dcp_decode over an FP8 E4M3 cache (uint8 codes, value = kv_scale *
+    decode(code)).  Returns (out [T,H,512], lse [T,H], row_counts [T])."""
+    lib = load_library()
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    sn, sp = _row_stride(q_nope, KV_LORA_RANK, "q_nope"), _row_stride(q_pe, ROPE_DIM, "q_pe")
+    nb, ps = _kv8(kv_cache)
+    _i32(block_table, "block_table"), _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc")
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, KV_LORA_RANK), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if row_counts is None:
+        row_counts = torch.empty((T,), dtype=torch.int32, device=dev)
+    if workspace is None:  # (the size query covers the bf16 and FP8 calls)
+        need = decode_workspace_size(B, T, H, max_query_len, max_seq_len, dcp_world, num_splits)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    _check(lib.mla_dcp_decode_fp8(_ptr(q_nope), sn, _ptr(q_pe), sp, _ptr(kv_cache), nb, ps, float(kv_scale),
+                                  _ptr(block_table), block_table.shape[1], _ptr(seq_lens), _ptr(query_start_loc), B, T,
+                                  H, int(max_query_len), int(max_seq_len), int(dcp_world), int(dcp_rank),
+                                  float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), _ptr(row_counts),
+                                  int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+    return out, lse, row_counts
+
+
+def mla_dcp_decode_fused_fp8(q_nope, q_pe, kv_caches, kv_scale, block_tables, seq_lens, query_start_loc,
+                             max_query_len, max_seq_len, scale, out=None, lse=None, out_dtype=torch.bfloat16,
+                             num_splits=0, workspace=None, stream=None):
+    """mla_dcp_decode_fused over FP8 E4M3 shard caches (uint8 codes, value =
+    kv_scale * decode(code)).  Returns the merged (out [T,H,512], lse [T,H])."""
+    lib = load_library()
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    D = len(kv_caches)
+    if len(block_tables) != D or D < 1:
+        raise ValueError("kv_caches and block_tables need one entry per shard")
+    sn, sp = _row_stride(q_nope, KV_LORA_RANK, "q_nope"), _row_stride(q_pe, ROPE_DIM, "q_pe")
+    kv_args = [_kv8(c) for c in kv_caches]
+    ps = kv_args[0][1]
+    if any(a[1] != ps for a in kv_args):
+        raise ValueError("all shard caches need the same page size")
+    bt_stride = block_tables[0].shape[1]
+    for bt in block_tables:
+        _i32(bt, "block_table")
+        if bt.shape[1] != bt_stride:
+            raise ValueError("all block tables need the same row stride")
+    _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc")
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, KV_LORA_RANK), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        need = fused_workspace_size(B, T, H, max_query_len, max_seq_len, num_splits)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
+    nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
+    bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    _check(lib.mla_dcp_decode_fused_fp8(_ptr(q_nope), sn, _ptr(q_pe), sp, ctypes.cast(kv_ptrs, ctypes.c_void_p),
+                                        ctypes.cast(nbs, ctypes.c_void_p), ps, float(kv_scale),
+                                        ctypes.cast(bt_ptrs, ctypes.c_void_p), bt_stride, _ptr(seq_lens),
+                                        _ptr(query_start_loc), B, T, H, int(max_query_len), int(max_seq_len), D,
+                                        float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), int(num_splits),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+    return out, lse
 
 
 def fused_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, num_splits=0) -> int:

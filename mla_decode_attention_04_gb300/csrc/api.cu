@@ -15,6 +15,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<int64_t> g_launches{0};
+std::atomic<uint64_t> g_wait_budget_ns{0};  // 0: the kernels' default (2 s)
 
 void count_launch(int n = 1) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -60,9 +61,12 @@ int check_decode_common(const void* q_nope, int64_t q_nope_row_stride, const voi
                         const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
                         const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                         int32_t dcp_world, int32_t dcp_rank, float scale, void* out, int32_t out_dtype, float* lse,
-                        void* workspace) {
-  if (kv_cache_dtype != MLA_DTYPE_BF16)
-    return fail(MLA_ERR_UNSUPPORTED, "kv_cache_dtype %d: only a bf16 latent cache is served (FP8 not supported)",
+                        void* workspace, bool fp8_call = false) {
+  if (fp8_call ? kv_cache_dtype != MLA_DTYPE_FP8_E4M3 : kv_cache_dtype != MLA_DTYPE_BF16)
+    return fail(MLA_ERR_UNSUPPORTED,
+                fp8_call ? "kv_cache_dtype %d: the _fp8 calls take an FP8 E4M3 cache"
+                         : "kv_cache_dtype %d: this call takes a bf16 latent cache (an FP8 E4M3 cache goes through "
+                           "mla_dcp_decode_fp8 / mla_dcp_decode_fused_fp8)",
                 kv_cache_dtype);
   if (num_tokens < 0 || num_requests < 1 || num_heads < 1 || num_heads > mla::kMaxHeads)
     return fail(MLA_ERR_INVALID_ARG, "bad sizes: num_requests=%d num_tokens=%d num_heads=%d (heads in [1,%d])",
@@ -127,13 +131,24 @@ extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
 
+// The larger of the bf16 and FP8 plans' workspaces (their unit sizes, and so
+// their grids and partial slots, can differ), so one size serves both calls.
+static size_t dense_workspace_bytes(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                    int32_t max_query_len, int32_t max_seq_len, int32_t D, int32_t num_splits) {
+  const int sms = current_sm_count();
+  const size_t a = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, D,
+                                         num_splits, sms, false).total;
+  const size_t b = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, D,
+                                         num_splits, sms, true).total;
+  return a > b ? a : b;
+}
+
 size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                                      int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world,
                                      int32_t num_splits) {
   if (dcp_world < 1) dcp_world = 1;
-  return mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, num_splits,
-                               current_sm_count())
-      .total;
+  return dense_workspace_bytes(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, dcp_world,
+                               num_splits);
 }
 
 }  // extern "C"
@@ -168,7 +183,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
                  const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                  int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, float scale, void* out,
                  int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+                 size_t workspace_bytes, void* stream, bool kv_fp8 = false, float kv_scale = 1.f) {
   if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
     return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
   if (num_tokens == 0) return ok();
@@ -176,7 +191,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
     return fail(MLA_ERR_INVALID_ARG, "num_tokens * num_heads = %lld exceeds 2^31 - 1",
                 (long long)num_tokens * num_heads);
   const mla::DecodePlan plan = mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len,
-                                                     dcp_world / nshard, num_splits, current_sm_count());
+                                                     dcp_world / nshard, num_splits, current_sm_count(), kv_fp8);
   if (workspace_bytes < plan.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, plan.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -225,6 +240,8 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;
   da.scale = scale;
+  da.kv_fp8 = kv_fp8 ? 1 : 0;
+  da.kv_scale = kv_fp8 ? kv_scale : 1.f;
   da.out = out;
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
   da.lse = lse;
@@ -234,6 +251,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.num_requests = num_requests;
   da.unit_penalty = plan.unit_penalty;
   da.gang = plan.gang;
+  da.wait_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
@@ -318,6 +336,8 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.num_heads = num_heads;
   da.dcp_world = dcp_world;
   da.scale = scale;
+  da.kv_fp8 = 0;
+  da.kv_scale = 1.f;
   da.out = out;
   da.out_f32 = out_dtype == MLA_DTYPE_F32;
   da.lse = lse;
@@ -328,6 +348,7 @@ int sparse_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_p
   da.num_tokens = num_tokens;
   da.unit_penalty = mla::kUnitPenalty;
   da.gang = 1;
+  da.wait_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
@@ -368,9 +389,7 @@ int mla_dcp_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_
 
 size_t mla_dcp_decode_fused_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                                            int32_t max_query_len, int32_t max_seq_len, int32_t num_splits) {
-  return mla::make_decode_plan(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, 1, num_splits,
-                               current_sm_count())
-      .total;
+  return dense_workspace_bytes(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, 1, num_splits);
 }
 
 int mla_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
@@ -395,6 +414,55 @@ int mla_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, const vo
                       page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests,
                       num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, scale, out, out_dtype, lse,
                       nullptr, num_splits, workspace, workspace_bytes, stream);
+}
+
+int mla_dcp_decode_fp8(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                       const void* kv_cache, int64_t num_blocks, int32_t page_size, float kv_scale,
+                       const int32_t* block_table, int32_t block_table_stride, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                       int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, int32_t dcp_rank, float scale,
+                       void* out, int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!std::isfinite(kv_scale) || !(kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale %g: a finite positive dequantisation scale is required", kv_scale);
+  int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_cache, num_blocks, page_size,
+                               MLA_DTYPE_FP8_E4M3, block_table, block_table_stride, seq_lens, query_start_loc,
+                               num_requests, num_tokens, num_heads, dcp_world, dcp_rank, scale, out, out_dtype, lse,
+                               workspace, true);
+  if (rc != MLA_OK) return rc;
+  const void* kvs[1] = {kv_cache};
+  const int64_t nbs[1] = {num_blocks};
+  const int32_t* bts[1] = {block_table};
+  return dense_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, 1, dcp_rank, kvs, nbs, page_size, bts,
+                      block_table_stride, seq_lens, query_start_loc, num_requests, num_tokens, num_heads,
+                      max_query_len, max_seq_len, dcp_world, scale, out, out_dtype, lse, row_counts, num_splits,
+                      workspace, workspace_bytes, stream, true, kv_scale);
+}
+
+int mla_dcp_decode_fused_fp8(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe,
+                             int64_t q_pe_row_stride, const void* const* kv_caches, const int64_t* num_blocks,
+                             int32_t page_size, float kv_scale, const int32_t* const* block_tables,
+                             int32_t block_table_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                             int32_t num_requests, int32_t num_tokens, int32_t num_heads, int32_t max_query_len,
+                             int32_t max_seq_len, int32_t dcp_world, float scale, void* out, int32_t out_dtype,
+                             float* lse, int32_t num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dcp_world < 1 || dcp_world > mla::kMaxShards)
+    return fail(MLA_ERR_INVALID_ARG, "dcp_world %d not in [1, %d] for the fused call", dcp_world, mla::kMaxShards);
+  if (kv_caches == nullptr || num_blocks == nullptr || block_tables == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "kv_caches / num_blocks / block_tables arrays are NULL");
+  if (!std::isfinite(kv_scale) || !(kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale %g: a finite positive dequantisation scale is required", kv_scale);
+  for (int r = 0; r < dcp_world; ++r) {
+    int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_caches[r], num_blocks[r],
+                                 page_size, MLA_DTYPE_FP8_E4M3, block_tables[r], block_table_stride, seq_lens,
+                                 query_start_loc, num_requests, num_tokens, num_heads, dcp_world, r, scale, out,
+                                 out_dtype, lse, workspace, true);
+    if (rc != MLA_OK) return rc;
+  }
+  return dense_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, dcp_world, 0, kv_caches, num_blocks,
+                      page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests,
+                      num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, scale, out, out_dtype, lse,
+                      nullptr, num_splits, workspace, workspace_bytes, stream, true, kv_scale);
 }
 
 size_t mla_sparse_dcp_decode_workspace_size(int32_t num_tokens, int32_t num_heads, int32_t topk, int32_t dcp_world) {
@@ -480,6 +548,8 @@ int dcp_lse_merge(const void* partials, int32_t partial_dtype, const float* lses
 }
 
 int64_t mla_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void mla_debug_set_wait_budget_ns(uint64_t ns) { g_wait_budget_ns.store(ns, std::memory_order_relaxed); }
 
 int mla_workspace_status(const void* workspace, void* stream, int32_t* detail) {
   if (!workspace) return fail(MLA_ERR_INVALID_ARG, "workspace is NULL");

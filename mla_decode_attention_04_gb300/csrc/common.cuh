@@ -33,12 +33,19 @@ enum DeviceCheck : int32_t {
 struct WorkspaceHeader {
   int32_t status;  // 0 or MLA_ERR_DEVICE_CHECK
   int32_t detail;  // DeviceCheck code of the first failure
-  int32_t pad[62];  // header is 256 bytes
+  int32_t where;   // after a wait gave up (detail 3): the site of the first one (diagnostic)
+  int32_t pad[61];  // header is 256 bytes
 };
 static_assert(sizeof(WorkspaceHeader) == 256, "header size");
 
 __device__ __forceinline__ void record_check(WorkspaceHeader* hdr, int32_t code) {
   if (atomicCAS(&hdr->status, 0, (int32_t)MLA_ERR_DEVICE_CHECK) == 0) hdr->detail = code;
+}
+
+// A pipeline wait that gave up: the check, and the first give-up site.
+__device__ __forceinline__ void record_wait_timeout(WorkspaceHeader* hdr, int32_t site) {
+  record_check(hdr, kCheckWaitTimeout);
+  atomicCAS(&hdr->where, 0, site);
 }
 
 // Local length on shard r of D of a request of global length L: the number of

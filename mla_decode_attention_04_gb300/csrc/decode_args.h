@@ -21,6 +21,13 @@ struct DecodeArgs {
   int64_t nblocks[kMaxShards];
   int32_t num_heads, dcp_world;
   float scale;
+  // 1: the caches hold FP8 E4M3 codes (576 bytes per row), value =
+  // kv_scale * decode(code); 0: bf16 (kv_scale 1)
+  int32_t kv_fp8;
+  float kv_scale;
+  // budget of each pipeline wait in ns (2 s unless a test shortens it);
+  // waits for copies already in flight when a role gave up have their own
+  uint64_t wait_ns;
   void* out;  // [T, H, 512]
   int32_t out_f32;
   float* lse;  // [T, H]

@@ -72,8 +72,9 @@ template <int NR> struct TmemPlan {
   static constexpr int kColO = kColS + kSBufs * 64;  // O^T [kColO, kColO + 4 NR)
   static_assert(kColO + 4 * NR <= 512, "TMEM budget");
 };
-template <int NR> struct Pipe {
-  static constexpr int kStages = NR == 64 ? 2 : 3;
+template <int NR, bool KV8 = false> struct Pipe {
+  // FP8 caches: 2 bf16 stages, next to 2 staging buffers of raw FP8 tiles
+  static constexpr int kStages = (NR == 64 || KV8) ? 2 : 3;
   // a unit's Q rows travel through one ring slot, row r at r * kQRowBytes:
   // with room to spare, a 16-byte pad puts consecutive rows in different
   // banks for the softmax warps' row reads (64 padded rows would not fit)
@@ -87,11 +88,27 @@ template <int NR> struct Pipe {
   static constexpr int kPLoBytes = kPLoInChunk ? 0 : kStages * kPBytes;
   static constexpr int kOffQSmem = kStages * kStageBytes;
   static constexpr int kOffPLo = kOffQSmem + kQSmemBytes;
-  static constexpr int kOffShared = kOffPLo + kPLoBytes;
+  // FP8 staging buffer: the tile's 576 code bytes per row as 4 boxes of 128
+  // columns (64 rows x 128 B, 128-byte swizzle, 8 KB each) and one of the
+  // last 64 columns (64 rows x 64 B, no swizzle)
+  static constexpr int kStgBufs = KV8 ? 2 : 0;
+  static constexpr int kStgBytes = 4 * 8192 + 4096;
+  static constexpr int kOffStg = kOffPLo + kPLoBytes;
+  static constexpr int kOffShared = kOffStg + kStgBufs * kStgBytes;
+  static_assert(!KV8 || NR <= 32, "FP8 caches use units of up to 32 rows");
 };
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Where a pipeline wait gave up (the workspace header's diagnostic word).
+enum WaitSite : int32_t {
+  kSiteProducerQ = 1, kSiteProducerStaging, kSiteProducerStage, kSiteSparseQ, kSiteSparsePart, kSiteQkQ,
+  kSiteQkSFree, kSiteQkFull, kSitePvReady, kSiteConvert, kSiteSoftmaxQ, kSiteSoftmaxS, kSiteSoftmaxPv,
+  kSiteSoftmaxUnit, kSiteConvertQ
+};
+// Budget of a wait for copies or MMAs already issued when a role gave up
+// (they complete by themselves; the bound only keeps the kernel finite).
+constexpr uint64_t kDrainNs = 1000000000ull;
 
 // P^T (NR rows x 64 keys, bf16, SW128 K-major) lives in the k_pe chunk of
 // the tile's own stage, free once QK^T of the tile is done: P as bf16 hi at
@@ -113,10 +130,15 @@ __host__ __device__ constexpr int part_chunks(int m) { return m == kParts - 1 ? 
 struct TcShared {
   uint64_t full[kMaxStages][kParts];
   uint64_t empty[kMaxStages][kParts];
+  uint64_t stg_full[2][kParts], stg_empty[2][kParts];  // FP8 staging (parts as the stages')
+  uint64_t drain[2];  // completion of every MMA of the QK^T / PV thread, at exit
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
+  int32_t conv_ok;  // result of the FP8 converters' last waits for a staged part
+  int32_t conv_q_ok;  // result of the FP8 converters' last waits for a Q slot
+  int32_t prod_ok;  // result of the sparse producer group's last wait
   float alpha[64], inv_l[64];
   // per-tile partial row maxima [tile parity][key slice * NR + row] (the
   // 128 TMEM lanes hold 128 / NR key slices of each of the NR rows)
@@ -136,7 +158,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-template <bool SPARSE, int NR>
+template <bool SPARSE, int NR, bool KV8 = false>
 struct Roles {
   // sparse: warps gathering key rows (2 for 64-row units, whose softmax
   // needs the registers a 4-warp CTA could not give it)
@@ -144,7 +166,11 @@ struct Roles {
   static constexpr int kMmaWarp = kProducerWarps;          // issues QK^T (and owns TMEM)
   static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;  // four consecutive warps
   static constexpr int kPvWarp = kProducerWarps + 5;        // issues PV
-  static constexpr int kThreads = (kProducerWarps + 6) * 32;
+  // FP8 caches: warps widening each staged FP8 tile to bf16 in its stage
+  // (and filling the units' Q slots)
+  static constexpr int kConvWarps = KV8 ? 4 : 0;
+  static constexpr int kConvWarp0 = kProducerWarps + 6;
+  static constexpr int kThreads = (kProducerWarps + 6 + kConvWarps) * 32;
 };
 
 // Work unit description, identical for every role.
@@ -402,9 +428,40 @@ struct TileLoc {
 // The cache tensor maps of a dense call, one per shard it covers, and (units
 // of 64 rows) the queries' maps.
 struct KvMaps {
-  CUtensorMap m[kMaxShards];
+  CUtensorMap m[kMaxShards];   // bf16 caches; FP8 caches: the 128-column maps
+  CUtensorMap m8t[kMaxShards];  // FP8 caches: the maps of the last 64 columns
   CUtensorMap q_nope, q_pe;  // [T H rows][512 | 64 dims] bf16, box 64 rows x 64 dims, 128-byte swizzle
 };
+
+__device__ __forceinline__ const CUtensorMap* kv8_tail_map_of(const KvMaps& maps, int k) {
+  switch (k) {
+    case 0: return &maps.m8t[0];
+    case 1: return &maps.m8t[1];
+    case 2: return &maps.m8t[2];
+    case 3: return &maps.m8t[3];
+    case 4: return &maps.m8t[4];
+    case 5: return &maps.m8t[5];
+    case 6: return &maps.m8t[6];
+    default: return &maps.m8t[7];
+  }
+}
+
+// 4 FP8 E4M3 codes (bytes of x, lowest first) -> 2 bf16x2 words (codes 0,1
+// and 2,3), exactly: a code's magnitude bits eeeemmm placed at bits 4-10 of a
+// bf16 read as the bf16 2^(e-127) * 1.mmm (or its subnormal 0.mmm * 2^-126 for
+// e = 0), so one multiply by 2^120 gives the code's value 2^(e-7) * 1.mmm (or
+// m * 2^-9); the sign bit moves to bit 15.  Exact: the products have at most
+// 4 significant bits and bf16 arithmetic keeps subnormal operands.
+__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const __nv_bfloat162 k = __floats2bfloat162_rn(0x1p120f, 0x1p120f);
+  const uint32_t w0 = __byte_perm(x, 0u, 0x4140), w1 = __byte_perm(x, 0u, 0x4342);
+  const uint32_t b0 = ((w0 & 0x00800080u) << 8) | ((w0 & 0x007F007Fu) << 4);
+  const uint32_t b1 = ((w1 & 0x00800080u) << 8) | ((w1 & 0x007F007Fu) << 4);
+  const __nv_bfloat162 r0 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b0), k);
+  const __nv_bfloat162 r1 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&b1), k);
+  lo = *reinterpret_cast<const uint32_t*>(&r0);
+  hi = *reinterpret_cast<const uint32_t*>(&r1);
+}
 
 // A 64-row unit's Q rows [grow0, grow0 + 64) as 9 TMA tiles of 64 rows x 64
 // dims (128-byte swizzle; rows past the last (token, head) read as zero)
@@ -432,11 +489,11 @@ __device__ __forceinline__ const CUtensorMap* kv_map_of(const KvMaps& maps, int 
   }
 }
 
-template <int NR, bool SPARSE, bool FUSED>
-__global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
+template <int NR, bool SPARSE, bool FUSED, bool KV8>
+__global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ KvMaps maps, const __grid_constant__ DecodeArgs a) {
-  using R = Roles<SPARSE, NR>;
-  using PP = Pipe<NR>;
+  using R = Roles<SPARSE, NR, KV8>;
+  using PP = Pipe<NR, KV8>;
   using TP = TmemPlan<NR>;
   constexpr int kStages = PP::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -444,6 +501,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
   uint8_t* kv = base;                           // [kStages][9][kChunk]
   uint8_t* q_smem = base + PP::kOffQSmem;       // NR = 64: Q chunks 0-2 as the QK^T A operand [3][128 rows][128 B]
   uint8_t* p_lo_buf = base + PP::kOffPLo;       // NR = 64: P lo per stage
+  uint8_t* stg = base + PP::kOffStg;            // FP8: [2][kStgBytes] raw tiles
   TcShared& sh = *reinterpret_cast<TcShared*>(base + PP::kOffShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -465,6 +523,14 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
         mbar_init(&sh.full[s][m], SPARSE ? 32 * R::kProducerWarps : 1);
         mbar_init(&sh.empty[s][m], 1);
       }
+    if (KV8)
+      for (int b = 0; b < 2; ++b)
+        for (int m = 0; m < kParts; ++m) {
+          mbar_init(&sh.stg_full[b][m], 1);
+          mbar_init(&sh.stg_empty[b][m], 1);
+        }
+    mbar_init(&sh.drain[0], 1);
+    mbar_init(&sh.drain[1], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
       mbar_init(&sh.s_free[b], 1);
@@ -477,6 +543,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     fence_mbar_init();
   }
   if (!SPARSE && warp == R::kMmaWarp && lane < nshard) prefetch_tmap(kv_map_of(maps, lane));
+  if (KV8 && warp == R::kMmaWarp && lane < nshard) prefetch_tmap(kv8_tail_map_of(maps, lane));
   if (NR == 64 && warp == R::kMmaWarp && lane == 0) {
     prefetch_tmap(&maps.q_nope);
     prefetch_tmap(&maps.q_pe);
@@ -502,6 +569,28 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
   bool ok = true;
   bool bad_page = false;
+  int32_t site = 0;  // where this thread's first wait gave up
+  const uint64_t budget = a.wait_ns ? a.wait_ns : 2000000000ull;
+  // a pipeline wait: false (and the site noted) once it gave up
+  auto wait = [&](uint64_t* bar, uint32_t parity, int32_t where) -> bool {
+    if (mbar_wait(bar, parity, budget)) return true;
+    if (site == 0) site = where;
+    return false;
+  };
+  // The last phase parity of each ring barrier this thread armed (bit
+  // 2 * part + 1: armed, bit 2 * part: parity): at exit the thread waits for
+  // those phases, so no copy it issued lands after the CTA is gone.  Only the
+  // last arming of a part can be outstanding: re-arming waits for the part's
+  // release, which follows its consumption.
+  uint32_t armed[kMaxStages] = {0, 0, 0}, armed_stg[2] = {0, 0};
+  auto note_armed = [](uint32_t& word, int m, uint32_t parity) {
+    word = (word & ~(3u << (2 * m))) | ((2u | (parity & 1u)) << (2 * m));
+  };
+  auto drain_armed = [&](uint64_t (*bars)[kParts], const uint32_t* words, int n) {
+    for (int s = 0; s < n; ++s)
+      for (int m = 0; m < kParts; ++m)
+        if ((words[s] >> (2 * m)) & 2u) mbar_wait(&bars[s][m], (words[s] >> (2 * m)) & 1u, kDrainNs);
+  };
 
   if (warp < R::kProducerWarps) {
     // ------------------------------------------------------------ producer
@@ -519,6 +608,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
       Unit w = w0;
       int cache_b = -1, cache_k = -1, cache_col = 0, my_page = -1;
+      int stg_b = 0;         // FP8 staging buffer of the next tile
+      uint32_t stg_ph = 0;   // its round parity
       // the unit's Q rows: one slot of the ring (NR <= 32: a bulk copy per
       // row half; NR = 64: 9 TMA tiles of 64 rows x 64 dims)
       auto issue_q = [&](const Unit& u, int st, uint32_t ph) -> bool {
@@ -527,12 +618,13 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
         // only see an arrival, so every part completes one phase per use
         if (lane == 0) {
           for (int m = 0; m < kParts && good; ++m)
-            if (!mbar_wait(&sh.empty[st][m], ph ^ 1)) good = false;
+            if (!wait(&sh.empty[st][m], ph ^ 1, kSiteProducerQ)) good = false;
           if (good) {
             if (NR == 64)
               issue_q_tma<NR>(maps, kv + st * kStageBytes, (int64_t)u.q0 * a.num_heads + u.row0, &sh.full[st][0]);
             else
               mbar_arrive_expect_tx(&sh.full[st][0], (uint32_t)u.nrows * (kRow * 2));
+            note_armed(armed[st], 0, ph);
             for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[st][m]);
           }
         }
@@ -551,13 +643,17 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       };
       // The Q slot of the CTA's first unit (stage 0, free at the start) is
       // filled by the softmax warps, so this warp goes straight to the key
-      // tiles and both start out at once.
+      // tiles and both start out at once.  FP8 caches: the converter warps
+      // fill every later Q slot.  This warp waits only for the staging
+      // buffers there, so it may run more than one ring round ahead of the
+      // stages' releases, where a parity wait on a stage's empty barrier
+      // could not tell the round it needs from the one before.
       bool first = true;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
         if (w.n_kt > 0) {
           if (first) {
             first = false;
-          } else if (!issue_q(w, stage, phase)) {
+          } else if (!KV8 && !issue_q(w, stage, phase)) {
             ok = false;
             break;
           }
@@ -605,17 +701,43 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
               }
             }
           }
-          if (lane == 0) {
+          if (KV8) {
+            // FP8: the tile's codes into a staging buffer, part by part (the
+            // converter warps widen part m into the stage's part m)
+            if (lane == 0) {
+              uint8_t* dst = stg + stg_b * PP::kStgBytes;
+              const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
+              const int off = ps >= kKeyTile ? k % ps : 0;
+              const CUtensorMap* tmap = kv8_tail_map_of(maps, loc.k);
+              for (int m = 0; m < kParts; ++m) {
+                if (!wait(&sh.stg_empty[stg_b][m], stg_ph ^ 1, kSiteProducerStaging)) {
+                  ok = false;
+                  break;
+                }
+                mbar_arrive_expect_tx(&sh.stg_full[stg_b][m],
+                                      (uint32_t)(nvalid * rows * (m == kParts - 1 ? 128 + 64 : 128)));
+                note_armed(armed_stg[stg_b], m, stg_ph);
+                for (int i = 0; i < nsub; ++i) {
+                  if (pages[i] < 0) continue;
+                  tma_load_3d(dst + m * 8192 + i * ps * 128, map, m * 128, off, pages[i], &sh.stg_full[stg_b][m], pol);
+                  if (m == kParts - 1)
+                    tma_load_3d(dst + 4 * 8192 + i * ps * 64, tmap, 512, off, pages[i], &sh.stg_full[stg_b][m], pol);
+                }
+              }
+            }
+            if (++stg_b == 2) { stg_b = 0; stg_ph ^= 1; }
+          } else if (lane == 0) {
             // part by part, each as soon as the value product frees it
             uint8_t* dst = kv + stage * kStageBytes;
             const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
             const int off = ps >= kKeyTile ? k % ps : 0;
             for (int m = 0; m < kParts; ++m) {
-              if (!mbar_wait(&sh.empty[stage][m], phase ^ 1)) {
+              if (!wait(&sh.empty[stage][m], phase ^ 1, kSiteProducerStage)) {
                 ok = false;
                 break;
               }
               mbar_arrive_expect_tx(&sh.full[stage][m], (uint32_t)(nvalid * rows * 128 * part_chunks(m)));
+              note_armed(armed[stage], m, phase);
               for (int i = 0; i < nsub; ++i)
                 if (pages[i] >= 0)
                   for (int c = part_first_chunk(m); c < part_first_chunk(m) + part_chunks(m); ++c)
@@ -637,6 +759,17 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       constexpr int KW = kKeyTile / R::kProducerWarps;  // keys per producer warp: 16 or 32
       const int pw = warp;            // producer warp
       const int pt = threadIdx.x;     // producer thread
+      // one thread waits, a named barrier hands the verdict to every producer
+      // thread, so all of them take the same path (and the count-based full
+      // barriers see every arrival or none)
+      auto prod_wait = [&](uint64_t* bar, uint32_t parity, int32_t where) -> bool {
+        if (pt == 0) sh.prod_ok = wait(bar, parity, where) ? 1 : 0;
+        named_bar_sync(3, 32 * R::kProducerWarps);
+        const bool r = sh.prod_ok != 0;
+        named_bar_sync(3, 32 * R::kProducerWarps);
+        if (r) mbar_wait(bar, parity, kDrainNs);  // every thread observes the phase (returns at once)
+        return r;
+      };
       Unit w = w0;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
         if (w.n_kt > 0) {
@@ -646,7 +779,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           // thread 0 with the byte count
           bool free_ok = true;
           for (int m = 0; m < kParts; ++m)
-            if (!mbar_wait(&sh.empty[stage][m], phase ^ 1)) free_ok = false;
+            if (!prod_wait(&sh.empty[stage][m], phase ^ 1, kSiteSparseQ)) free_ok = false;
           if (!free_ok) { ok = false; break; }
           uint8_t* qdst = kv + stage * kStageBytes;
           const int64_t grow0 = (int64_t)w.token * a.num_heads + w.row0;
@@ -662,6 +795,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           } else {
             mbar_arrive(&sh.full[stage][0]);
           }
+          if (pt < w.nrows || pt == 0) note_armed(armed[stage], 0, phase);  // its bulk copies or TMA
           for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[stage][m]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -676,7 +810,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           // lanes taking consecutive pieces of a row (whole 128-byte lines)
 #pragma unroll
           for (int m = 0; m < kParts; ++m) {
-            if (!ok || !mbar_wait(&sh.empty[stage][m], phase ^ 1)) {
+            if (!ok || !prod_wait(&sh.empty[stage][m], phase ^ 1, kSiteSparsePart)) {
               ok = false;
               break;
             }
@@ -698,6 +832,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
             }
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[stage][m]))
                          : "memory");
+            note_armed(armed[stage], m, phase);
           }
           if (!ok) break;
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -705,6 +840,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
+    // exit: every copy this thread issued has landed (its armed phases done)
+    drain_armed(sh.full, armed, kStages);
+    if (KV8) drain_armed(sh.stg_full, armed_stg, 2);
   } else if (warp == R::kMmaWarp || warp == R::kPvWarp) {
     // --------------------------------------------------------------- MMA
     // One thread cannot issue tcgen05.mma fast enough to keep the tensor
@@ -736,12 +874,12 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
         for (bool more = more0; ok && more; more = it.next(a, w)) {
           if (w.n_kt == 0) continue;
           if (++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
-          if (!mbar_wait(&sh.q_ready, q_ph)) { ok = false; break; }
+          if (!wait(&sh.q_ready, q_ph, kSiteQkQ)) { ok = false; break; }
           q_ph ^= 1;
           tc_fence_after();
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
             const int sb = j % SB;
-            if (!mbar_wait(&sh.s_free[sb], ((j / SB) & 1) ^ 1)) {
+            if (!wait(&sh.s_free[sb], ((j / SB) & 1) ^ 1, kSiteQkSFree)) {
               ok = false;
               break;
             }
@@ -751,7 +889,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 9; ++c) {
               if (c < 8 && (c & 1) == 0) {
-                if (!mbar_wait(&sh.full[stage][c >> 1], phase)) {
+                if (!wait(&sh.full[stage][c >> 1], phase, kSiteQkFull)) {
                   ok = false;
                   break;
                 }
@@ -780,7 +918,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           if (w.n_kt == 0) continue;
           if (++stage == kStages) stage = 0;  // the unit's Q slot
           for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-            if (!mbar_wait(&sh.p_ready, j & 1)) { ok = false; break; }
+            if (!wait(&sh.p_ready, j & 1, kSitePvReady)) { ok = false; break; }
             tc_fence_after();
             const uint64_t v0 = d_v + (uint64_t)stage * kStageUnits;
             const uint64_t p0 = d_p + (uint64_t)stage * kStageUnits;
@@ -793,7 +931,124 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
           }
         }
       }
+      // exit: every MMA this thread issued has completed (TMEM is freed and
+      // the stages' memory is reused only after that)
+      mma_commit(&sh.drain[warp == R::kMmaWarp ? 0 : 1]);
+      mbar_wait(&sh.drain[warp == R::kMmaWarp ? 0 : 1], 0, kDrainNs);
     }
+  } else if (KV8 && warp >= R::kConvWarp0) {
+    // ---------------------------------------------------------- FP8 widen
+    // Each staged FP8 part becomes the same part of its bf16 stage, in the
+    // stage's 128-byte-swizzled chunk layout.  Thread ct of the 128 takes row
+    // ct / 2 and half ct & 1 of the part's 128 code columns (4 pieces of 16
+    // codes -> 8 bf16 pieces), and of the last part's 64 tail columns (2
+    // pieces -> 4 bf16 pieces).  One thread waits, a named barrier hands the
+    // verdict to the others, each of which then observes the completed phase.
+    const int ct = (int)threadIdx.x - R::kConvWarp0 * 32;
+    const int r = ct >> 1, h = ct & 1;
+    int stage = 0, stg_b = 0;
+    uint32_t phase = 0, stg_ph = 0;
+    // These warps fill the ring in its order, so a stage's empty barrier
+    // is at most one round behind the wait.  The Q slot of every unit but
+    // the first goes in here too: a bulk copy per row half, on the slot's
+    // part-0 full barrier (parts 1-3 get a plain arrival).  Thread 0 keeps
+    // the last such slot until a later round of its stage is released
+    // (its copies have landed then): at exit it waits for that phase.
+    bool first = true;
+    int q_st = -1;
+    uint32_t q_ph = 0;
+    Unit w = w0;
+    for (bool more = more0; ok && more; more = it.next(a, w)) {
+      if (w.n_kt == 0) continue;
+      if (!first) {
+        if (ct == 0) {
+          bool g = true;
+          for (int m = 0; m < kParts && g; ++m) g = wait(&sh.empty[stage][m], phase ^ 1, kSiteConvertQ);
+          if (g) {
+            mbar_arrive_expect_tx(&sh.full[stage][0], (uint32_t)w.nrows * (kRow * 2));
+            for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[stage][m]);
+            q_st = stage;
+            q_ph = phase;
+          }
+          sh.conv_q_ok = g ? 1 : 0;
+        }
+        named_bar_sync(2, 128);
+        if (!sh.conv_q_ok) {
+          ok = false;
+          break;
+        }
+        if (ct < w.nrows) {
+          const int64_t grow = (int64_t)w.q0 * a.num_heads + w.row0 + ct;
+          uint8_t* qdst = kv + stage * kStageBytes + ct * PP::kQRowBytes;
+          bulk_load(qdst, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage][0]);
+          bulk_load(qdst + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage][0]);
+        }
+      }
+      first = false;
+      if (++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
+      for (int kt = 0; kt < w.n_kt && ok; ++kt) {
+        const uint8_t* src = stg + stg_b * PP::kStgBytes;
+        uint8_t* dst = kv + stage * kStageBytes;
+        for (int m = 0; m < kParts; ++m) {
+          if (ct == 0) {
+            sh.conv_ok = (wait(&sh.stg_full[stg_b][m], stg_ph, kSiteConvert) &&
+                          wait(&sh.empty[stage][m], phase ^ 1, kSiteConvert))
+                             ? 1
+                             : 0;
+            if (sh.conv_ok && stage == q_st) q_st = -1;  // the Q slot was read: its copies are in
+          }
+          named_bar_sync(2, 128);
+          if (!sh.conv_ok) {
+            ok = false;
+            break;
+          }
+          mbar_wait(&sh.stg_full[stg_b][m], stg_ph);  // returns at once
+          // columns [128 m, 128 m + 128): code piece v (codes 16v..16v+15)
+          // -> bf16 chunk 2m + v / 4, pieces 2 (v % 4) and 2 (v % 4) + 1
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int v = 4 * h + v4;
+            const uint4 x = *reinterpret_cast<const uint4*>(src + m * 8192 + r * 128 + ((v ^ (r & 7)) << 4));
+            uint32_t o[8];
+            e4m3x4_to_bf16x2(x.x, o[0], o[1]);
+            e4m3x4_to_bf16x2(x.y, o[2], o[3]);
+            e4m3x4_to_bf16x2(x.z, o[4], o[5]);
+            e4m3x4_to_bf16x2(x.w, o[6], o[7]);
+            uint8_t* drow = dst + (2 * m + (v >> 2)) * kChunk + r * 128;
+            const int w0 = 2 * (v & 3);
+            *reinterpret_cast<uint4*>(drow + ((w0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(drow + (((w0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          if (m == kParts - 1) {
+            // columns [512, 576): tail piece v -> bf16 chunk 8, pieces 2v, 2v + 1
+#pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2) {
+              const int v = 2 * h + v2;
+              const uint4 x = *reinterpret_cast<const uint4*>(src + 4 * 8192 + r * 64 + v * 16);
+              uint32_t o[8];
+              e4m3x4_to_bf16x2(x.x, o[0], o[1]);
+              e4m3x4_to_bf16x2(x.y, o[2], o[3]);
+              e4m3x4_to_bf16x2(x.z, o[4], o[5]);
+              e4m3x4_to_bf16x2(x.w, o[6], o[7]);
+              uint8_t* drow = dst + 8 * kChunk + r * 128;
+              *reinterpret_cast<uint4*>(drow + (((2 * v) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(drow + (((2 * v + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(2, 128);
+          if (ct == 0) {
+            mbar_arrive(&sh.full[stage][m]);
+            mbar_arrive(&sh.stg_empty[stg_b][m]);
+          }
+        }
+        if (++stg_b == 2) { stg_b = 0; stg_ph ^= 1; }
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    // exit: the last Q slot's copies have landed, read or not (no round of
+    // its stage after it was filled, so the phase is the barrier's own)
+    if (ct == 0 && q_st >= 0) mbar_wait(&sh.full[q_st][0], q_ph, kDrainNs);
   } else {
     // ----------------------------------------------------------- softmax
     const int sw = warp - R::kSoftmaxWarp0;   // 0..3
@@ -816,7 +1071,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     const int kslice = tl / NR;                   // keys [kslice * KPT, + KPT) of the tile
     const int kslice0 = quarter * 32 / NR;        // the warp's first key slice
     const bool row_lead = kslice == 0;            // writes the row's shared values
-    const float scale_log2 = a.scale * kLog2e;
+    // scores in log2 units; an FP8 cache's dequantisation scale multiplies
+    // every score (and, in the epilogue, every output)
+    const float scale_log2 = a.scale * a.kv_scale * kLog2e;
     const int H = a.num_heads;
     uint32_t j = 0, u_ph = 0;
     int stage = 0;          // ring slot of the next tile (dense: or of the next unit's Q)
@@ -825,8 +1082,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     // the 128 threads always take the same branch (no thread is left at a
     // barrier the others skipped).  Consecutive calls are separated by at
     // least one more group barrier, so the flag is not overwritten early.
-    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      if (st_tid == 0) sh.wait_ok = mbar_wait(bar, parity) ? 1 : 0;
+    auto group_wait = [&](uint64_t* bar, uint32_t parity, int32_t where) -> bool {
+      if (st_tid == 0) sh.wait_ok = wait(bar, parity, where) ? 1 : 0;
       named_bar_sync(1, 128);
       const bool r = sh.wait_ok != 0;
       tc_fence_after();
@@ -837,6 +1094,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       if constexpr (SPARSE) return (int64_t)u.token * H + u.row0 + n;
       else return (int64_t)u.q0 * H + u.row0 + n;
     };
+    // the first unit's Q slot (stage 0, first round), filled from here when
+    // dense: drained at exit if no load_q consumed it
+    bool q0_armed = false, q0_consumed = false;
     // Q rows of unit u into TMEM, then q_ready.  Called once every QK^T
     // issued so far is complete (the softmax has read all their S).
     auto load_q = [&](const Unit& u) -> bool {
@@ -845,7 +1105,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       // into the shared-memory A operand instead, at row tl
       const bool have = row < u.nrows;
       // the rows are in this unit's Q slot of the ring
-      if (!group_wait(&sh.full[stage][0], sphase)) return false;
+      if (!group_wait(&sh.full[stage][0], sphase, kSiteSoftmaxQ)) return false;
+      if (stage == 0 && sphase == 0) q0_consumed = true;
       mbar_wait(&sh.full[stage][0], sphase);  // every reader observes the phase (returns at once)
       const uint8_t* slot = kv + stage * kStageBytes;
 #pragma unroll 1
@@ -885,6 +1146,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     if constexpr (!SPARSE) {
       // dense: the first unit's Q slot (stage 0) is filled from here
       if (more && wn.n_kt > 0) {
+        q0_armed = true;
         if (NR == 64) {
           if (st_tid == 0) {
             issue_q_tma<NR>(maps, kv, grow_of(wn, 0), &sh.full[0][0]);
@@ -926,7 +1188,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
       float m_ref = -INFINITY, l_sum = 0.f;
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
-        if (!group_wait(&sh.s_full[j % SB], (j / SB) & 1)) { ok = false; break; }
+        if (!group_wait(&sh.s_full[j % SB], (j / SB) & 1, kSiteSoftmaxS)) { ok = false; break; }
         // this thread's KPT columns of its lane's row of S
         float s[KPT];
 #pragma unroll
@@ -1034,7 +1296,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
         // before this tile's P is released (waited every tile, in order); the
         // barrier inside group_wait also publishes any_rescale
         if (j > 0) {
-          if (!group_wait(&sh.pv_done, (j - 1) & 1)) { ok = false; break; }
+          if (!group_wait(&sh.pv_done, (j - 1) & 1, kSiteSoftmaxPv)) { ok = false; break; }
         } else {
           named_bar_sync(1, 128);
         }
@@ -1068,7 +1330,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
 
       // ---- epilogue of the unit
       if (w.n_kt > 0) {
-        if (!group_wait(&sh.unit_done, u_ph)) { ok = false; break; }
+        if (!group_wait(&sh.unit_done, u_ph, kSiteSoftmaxUnit)) { ok = false; break; }
         u_ph ^= 1;
       }
       // first global write of this kernel: everything before it in the
@@ -1081,7 +1343,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < TPR; ++k) lt += sh.lpart[k * NR + row];
         const bool live = lt > 0.f && m_ref > -INFINITY;
-        sh.inv_l[row] = live ? 1.f / lt : 0.f;
+        sh.inv_l[row] = live ? a.kv_scale / lt : 0.f;
         if (row < w.nrows) {
           const float lse = live ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
           if (partial) a.part_lse[chunk_slot(w.cta0, w.split, NR, it.S) + row] = lse;
@@ -1133,13 +1395,15 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
     // here), after the wait that precedes every global write
     grid_dep_wait();
     if (st_tid == 0) a.split_desc[blockIdx.x] = desc;
+    // exit: the first unit's Q copies have landed, consumed or not
+    if (q0_armed && !q0_consumed) mbar_wait(&sh.full[0][0], 0, kDrainNs);
   }
 
   // this kernel completes after the prep kernel, so kernels that wait for it
   // also see the prep kernel's outputs (rows without keys, per-token counts);
   // checks are recorded after it reset the status word
   grid_dep_wait();
-  if (!ok) record_check(a.hdr, kCheckWaitTimeout);
+  if (!ok) record_wait_timeout(a.hdr, site ? site : 99);
   if (bad_page) record_check(a.hdr, kCheckPageOutOfRange);
   tc_fence_before();
   __syncthreads();
@@ -1147,15 +1411,15 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR>::kThreads, 1)
   if (warp == R::kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int NR, bool SPARSE, bool FUSED>
+template <int NR, bool SPARSE, bool FUSED, bool KV8 = false>
 cudaError_t launch_tc(const DecodeArgs& a, const KvMaps& maps, int grid, cudaStream_t stream) {
-  const size_t smem = 1024 + Pipe<NR>::kOffShared + sizeof(TcShared);
-  static_assert(1024 + Pipe<NR>::kOffShared + sizeof(TcShared) <= 232448, "shared memory per CTA");
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE, FUSED>,
+  const size_t smem = 1024 + Pipe<NR, KV8>::kOffShared + sizeof(TcShared);
+  static_assert(1024 + Pipe<NR, KV8>::kOffShared + sizeof(TcShared) <= 232448, "shared memory per CTA");
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<NR, SPARSE, FUSED, KV8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc_kernel<NR, SPARSE, FUSED>, dim3(grid), dim3(Roles<SPARSE, NR>::kThreads), smem, stream,
-                    maps, a);
+  return launch_pdl(decode_tc_kernel<NR, SPARSE, FUSED, KV8>, dim3(grid), dim3(Roles<SPARSE, NR, KV8>::kThreads), smem,
+                    stream, maps, a);
 }
 
 }  // namespace
@@ -1167,8 +1431,12 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool spars
   if (rows_per_group != 16 && rows_per_group != 32 && rows_per_group != 64) return cudaErrorInvalidValue;
   KvMaps maps;
   memset(&maps, 0, sizeof(maps));
-  for (int k = 0; k < a.nshard; ++k)
-    if (!make_kv_tensor_map(&maps.m[k], a.kvs[k], a.nblocks[k], a.page_size)) return cudaErrorInvalidValue;
+  if (a.kv_fp8 && (sparse || rows_per_group > 32)) return cudaErrorInvalidValue;
+  for (int k = 0; k < a.nshard; ++k) {
+    const bool made = a.kv_fp8 ? make_kv8_tensor_maps(&maps.m[k], &maps.m8t[k], a.kvs[k], a.nblocks[k], a.page_size)
+                               : make_kv_tensor_map(&maps.m[k], a.kvs[k], a.nblocks[k], a.page_size);
+    if (!made) return cudaErrorInvalidValue;
+  }
   if (rows_per_group == 64) {
     const int64_t rows = (int64_t)a.num_tokens * a.num_heads;
     if (!make_query_tensor_map(&maps.q_nope, a.q_nope, rows, kNope, a.q_nope_stride) ||
@@ -1180,6 +1448,13 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, int rows_per_group, bool spars
     if (rows_per_group == 16) return launch_tc<16, true, false>(a, maps, grid, stream);
     if (rows_per_group == 32) return launch_tc<32, true, false>(a, maps, grid, stream);
     return launch_tc<64, true, false>(a, maps, grid, stream);
+  }
+  if (a.kv_fp8) {
+    if (a.nshard > 1)
+      return rows_per_group == 16 ? launch_tc<16, false, true, true>(a, maps, grid, stream)
+                                  : launch_tc<32, false, true, true>(a, maps, grid, stream);
+    return rows_per_group == 16 ? launch_tc<16, false, false, true>(a, maps, grid, stream)
+                                : launch_tc<32, false, false, true>(a, maps, grid, stream);
   }
   if (a.nshard > 1) {
     if (rows_per_group == 16) return launch_tc<16, false, true>(a, maps, grid, stream);

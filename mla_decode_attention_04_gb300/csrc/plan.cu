@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     a.hdr->status = 0;  // this call's checks start clean
     a.hdr->detail = 0;
+    a.hdr->where = 0;
   }
   const int H = a.num_heads;
   const int nthreads = gridDim.x * blockDim.x, tid = blockIdx.x * blockDim.x + threadIdx.x;

@@ -45,11 +45,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int32_t rows_per_unit(int64_t rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
 
 inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_query_len, int32_t max_seq_len,
-                                   int32_t D, int32_t num_splits, int32_t num_sms) {
+                                   int32_t D, int32_t num_splits, int32_t num_sms, bool kv_fp8 = false) {
   DecodePlan p{};
   if (max_query_len < 1) max_query_len = 1;  // the backend's capture-time clamp
   if (D < 1) D = 1;
   p.rows_per_group = rows_per_unit((int64_t)max_query_len * H);
+  // an FP8 cache's staging buffers leave room for units of up to 32 rows
+  if (kv_fp8 && p.rows_per_group > 32) p.rows_per_group = 32;
   p.unit_penalty = kUnitPenalty;
   const int64_t NR = p.rows_per_group;
   const int64_t max_local = (max_seq_len + D - 1) / D;

@@ -122,3 +122,35 @@ def assert_lse_close(got, ref, what=""):
 
 def to_np(t):
     return t.detach().float().cpu().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()
+
+
+def oracle_step_kv8(h: HostInputs, caches8, kv_scale, tokens=None):
+    """oracle_step over FP8 shard caches (uint8 E4M3 codes, value = kv_scale *
+    decode(code)), parallel over tokens."""
+    from concurrent.futures import ThreadPoolExecutor
+    T = h.q_nope.shape[0]
+    tokens = list(range(T)) if tokens is None else list(tokens)
+    n = oracle.default_threads()
+    chunks = [tokens[i::n] for i in range(n) if tokens[i::n]]
+
+    def run(chunk):
+        parts, lses, counts = [], [], []
+        for r in range(h.D):
+            ps, ls, cs = [], [], []
+            for t in chunk:
+                o, l, c = oracle.dcp_decode_kv8(h.q_nope, h.q_pe, caches8[r], kv_scale, h.tables[r], h.seq_lens, h.qsl,
+                                                h.D, r, h.scale, t_lo=t, t_hi=t + 1, threads=1)
+                ps.append(o[0]), ls.append(l[0]), cs.append(c[0])
+            parts.append(np.stack(ps)), lses.append(np.stack(ls)), counts.append(np.array(cs, np.int32))
+        return np.stack(parts), np.stack(lses), np.stack(counts)
+
+    with ThreadPoolExecutor(max_workers=len(chunks)) as ex:
+        res = list(ex.map(run, chunks))
+    order = np.concatenate([np.asarray(c) for c in chunks])
+    inv = np.argsort(order)
+    parts = np.concatenate([r[0] for r in res], axis=1)[:, inv]
+    lses = np.concatenate([r[1] for r in res], axis=1)[:, inv]
+    counts = np.concatenate([r[2] for r in res], axis=1)[:, inv]
+    merged, mlse = oracle.lse_merge(parts, lses, counts)
+    out = oracle.wuv_project(merged, h.w_uv) if h.w_uv is not None else merged
+    return dict(parts=parts, lses=lses, counts=counts, merged=merged, lse=mlse, out=out)

@@ -25,7 +25,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^(?:int|int64_t|size_t|const char \*)\s*(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^(?:int|int64_t|size_t|void|const char \*)\s*(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_three_operations():
@@ -245,3 +245,25 @@ def test_static_scratch_reports_argument_errors_before_sizing(lib, kw, code):
                                            a["ms"], 2, a["r"], ctypes.c_float(0.07), A, mla.MLA_DTYPE_BF16, A, None, 0,
                                            None)
     assert rc == code, lib.mla_last_error().decode()
+
+
+def test_fp8_calls_check_their_arguments(lib):
+    def call(**kw):
+        a = dict(kvs=0.25, H=16, ps=64, kv=A)
+        a.update(kw)
+        return lib.mla_dcp_decode_fp8(A, 512, A, 64, a["kv"], 10, a["ps"], ctypes.c_float(a["kvs"]), A, 4, A, A, 2, 2,
+                                      a["H"], 1, 100, 2, 0, ctypes.c_float(0.07), A, mla.MLA_DTYPE_BF16, A, None, 0, A,
+                                      1 << 30, None)
+    assert call(kvs=0.0) == mla.MLA_ERR_INVALID_ARG
+    assert call(kvs=float("inf")) == mla.MLA_ERR_INVALID_ARG
+    assert call(kvs=-1.0) == mla.MLA_ERR_INVALID_ARG
+    assert call(H=0) == mla.MLA_ERR_INVALID_ARG
+    assert call(ps=12) == mla.MLA_ERR_UNSUPPORTED
+    assert call(kv=None) == mla.MLA_ERR_INVALID_ARG
+    kvs, nbs, bts = _shard_arrays(2)
+    rc = lib.mla_dcp_decode_fused_fp8(A, 512, A, 64, kvs, nbs, 64, ctypes.c_float(0.0), bts, 4, A, A, 2, 2, 16, 1,
+                                      100, 2, ctypes.c_float(0.07), A, mla.MLA_DTYPE_BF16, A, 0, A, 1 << 30, None)
+    assert rc == mla.MLA_ERR_INVALID_ARG
+    # the bf16 calls still refuse an FP8 cache, pointing to these calls
+    rc, msg = _decode(lib, kvdt=mla.MLA_DTYPE_FP8_E4M3)
+    assert rc == mla.MLA_ERR_UNSUPPORTED and "_fp8" in msg
