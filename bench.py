@@ -3,13 +3,16 @@
 
 One step = the whole hot path on one batch: the D shard decodes (split-KV
 schedule, paged gathers, QK^T + online softmax + PV, split-chunk merge) and the
-LSE merge.  The headline workload is plain decode: 64 requests, q_len 1,
-16 heads, context 4096, DCP D=2 (the D shards are D slices of one HBM).  The
-other benchmark workloads (plain decode D=1, MTP, long context, sparse +
-mixed) are measured the same way and reported under "configs".
+LSE merge (with the W_UV projection where the workload has one).  The
+headline workload is the heaviest one: long context, 32 requests, q_len 2,
+128 heads, context U[16384, 32768], DCP D=8 (the D shards are D slices of one
+HBM), run as one shard-fused decode launch plus the W_UV projection.  Every
+benchmark workload (plain decode D=1 / D=2, MTP, sparse + mixed, long
+context; plain decode D=2 and MTP also over an FP8 cache) is measured on both
+routes and reported under "configs", each with its own roofline object.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle instead, on a bounded sample of the same workload.
+oracle instead, on a bounded sample of the headline workload.
 """
 from __future__ import annotations
 
@@ -31,9 +34,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA DCP decode query tok/s; KV GB/s & TFLOP/s as % of GB300 roofline"
 UNIT = "query tok/s"
-ROW_BYTES = 576 * 2
 FLOPS_PER_KEY_ROW = 2 * (576 + 512)
-HEADLINE = "plain_decode_d2"
+HEADLINE = "long_context"
+CONFIG_NAMES = ("plain_decode_d1", "plain_decode_d2", "mtp", "sparse_mixed", "long_context")
+FP8_NAMES = ("plain_decode_d2", "mtp")  # dense workloads also run over an FP8 E4M3 cache
+FP8_SCALE = 0.25
 DESCR = {
     "tiny": "tiny: 4 requests, context {6,37,130,300}, q_len {4,1,2,2}, H=16, D=2, page 16, merge+W_UV",
     "plain_decode_d1": "plain decode: batch 64, q_len 1, H=16, context 4096, D=1, page 64, merge to 512-wide",
@@ -43,6 +48,14 @@ DESCR = {
     "sparse_mixed": "sparse+mixed: 96 requests q_len {1,2,4} + 4x64 prefill, H=64, context U[4096,65536], "
                     "top-k 2048, D=4, page 64, merge+W_UV",
 }
+
+
+_T0 = time.perf_counter()
+
+
+def log(msg):
+    """Progress on stderr (the bench line alone goes to stdout)."""
+    print(f"[bench {time.perf_counter() - _T0:8.1f}s] {msg}", file=sys.stderr, flush=True)
 
 
 def peaks():
@@ -59,10 +72,12 @@ def peaks():
 # ------------------------------------------------------------ algorithmic work
 
 
-def work_of(w, partial_bytes=4, fused=False):
+def work_of(w, partial_bytes=4, fused=False, kv_elem_bytes=2):
     """Algorithmic KV bytes, FLOPs and merge bytes of one step of workload w
     (fused: the merge is inside the decode; only the W_UV projection of the
-    one merged fp32 result remains)."""
+    one merged fp32 result remains).  Each key row the step reads is read
+    once: 576 elements of ``kv_elem_bytes`` (2: bf16 cache, 1: FP8 codes)."""
+    row_bytes = 576 * kv_elem_bytes
     L = w.seq_lens.cpu().numpy().astype(np.int64)
     qsl = w.query_start_loc.cpu().numpy().astype(np.int64)
     D, H = w.dcp_world, w.num_heads
@@ -72,7 +87,7 @@ def work_of(w, partial_bytes=4, fused=False):
     if w.topk is None:
         for r in range(D):
             local = np.where(L > r, (L - r - 1) // D + 1, 0)
-            kv_bytes_shard.append(int(local.sum()) * ROW_BYTES)
+            kv_bytes_shard.append(int(local.sum()) * row_bytes)
         # every token sees its visible prefix, over all shards together
         vis = 0
         for b in range(len(L)):
@@ -89,7 +104,7 @@ def work_of(w, partial_bytes=4, fused=False):
         used = (np.arange(K)[None, :] < valid[:, None]) & (topk >= 0) & (topk <= pos[:, None])
         for r in range(D):
             kept = used & (topk % D == r)
-            kv_bytes_shard.append(int(kept.sum()) * ROW_BYTES)
+            kv_bytes_shard.append(int(kept.sum()) * row_bytes)
         flops = int(used.sum()) * H * FLOPS_PER_KEY_ROW
     T = w.num_tokens
     out_w = 128 if w.w_uv is not None else 512
@@ -201,25 +216,35 @@ def flush_l2(flush):
     flush()
 
 
-def time_workload(name, steps, warmup, with_e2e=False, l2_flush=False, fused=False, clock=None, sustain_s=1.5):
-    """Time one workload's decode step.  ``fused``: the dense step as one
+def time_workload(name, steps, warmup, with_e2e=False, l2_flush=False, fused=False, clock=None, sustain_s=1.5,
+                  fp8=False):
+    """Time one workload's decode step.  ``fused``: the step as one
     shard-fused decode launch (all D shards, merge built in; + the W_UV
     projection when the workload has one) instead of D shard calls + the
-    merge call."""
+    merge call.  ``fp8``: the fused step over an FP8 E4M3 copy of the
+    workload's cache (codes of cache / FP8_SCALE)."""
     import mla_decode_attention_04_gb300 as mla
     from mla_decode_attention_04_gb300 import pipeline, workloads as wl
 
+    log(f"{name}: building the workload (fused={fused}, fp8={fp8})")
     w = wl.NAMED[name](device="cuda")
-    step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
-    work = work_of(w, 4 if fused else step.partials.element_size(), fused=fused)
+    if fp8:
+        _, views = wl.fp8_cache(w, FP8_SCALE)
+        step = pipeline.fused_step_for_workload(w, fp8_caches=views, kv_scale=FP8_SCALE)
+        fused = True
+    else:
+        step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
+    work = work_of(w, 4 if fused else step.partials.element_size(), fused=fused, kv_elem_bytes=1 if fp8 else 2)
     flush = L2Flush() if l2_flush else None
     stream = torch.cuda.current_stream()
+    log(f"{name}: warm-up")
     for _ in range(warmup):
         step.run()
     torch.cuda.synchronize()
     rc, detail = mla.workspace_status(step.workspace)
     if rc != mla.MLA_OK:
         raise RuntimeError(f"device check {detail} in {name}")
+    log(f"{name}: capturing graphs")
 
     # The step runs as a CUDA graph (how a serving engine replays its decode
     # step): the library launches nothing per replay from the host, so the
@@ -257,6 +282,7 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=False, fused=Fal
             step_merge(step)
     torch.cuda.synchronize()
 
+    log(f"{name}: timing")
     if clock is not None:
         # the clock window: a sustained run of the same replays (untimed),
         # then the K timed steps right after it
@@ -298,9 +324,11 @@ def time_workload(name, steps, warmup, with_e2e=False, l2_flush=False, fused=Fal
     if rc != mla.MLA_OK:
         raise RuntimeError(f"device check {detail} in {name} (graph replays)")
     res = dict(name=name, w=w, step=step, work=work, step_ms=step_ms, decode_ms=decode_ms, merge_ms=merge_ms,
-               launches=launches, fused=fused)
+               launches=launches, fused=fused, fp8=fp8)
     if with_e2e:
+        log(f"{name}: end-to-end timing")
         res["e2e"] = time_e2e(w, step, steps, flush)
+    log(f"{name}: done, step {statistics.median(step_ms):.4f} ms")
     return res
 
 
@@ -363,28 +391,66 @@ def time_e2e(w, step, steps, flush):
                 d2h_bytes_per_step=int(d2h))
 
 
+def route_tag(res):
+    """Key of a timed route in profiles/traffic.json."""
+    return ("decode_fused_" if res["fused"] else "decode_shards_") + res["name"] + ("_fp8" if res.get("fp8") else "")
+
+
+def roofline_of(work, dec_ms_total, launches, pk, tag):
+    """The decode's roofline object: bound by whichever of its KV bytes at
+    HBM bandwidth or its FLOPs at bf16 tensor peak takes longer; achieved =
+    that quantity over the decode calls' measured time; per launch of the
+    decode kernel (``launches`` per step)."""
+    t_hbm = work["kv_bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = work["flops"] / (pk["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        bound, unit, peak = "hbm", "GB/s", pk["hbm_gbs"]
+        achieved = work["kv_bytes"] / (dec_ms_total * 1e-3) / 1e9
+    else:
+        bound, unit, peak = "tensor", "TFLOP/s", pk["bf16_tflops"]
+        achieved = work["flops"] / (dec_ms_total * 1e-3) / 1e12
+    tr = profile_traffic(tag)
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": tr, "algorithmic_bytes": work["kv_bytes"] / launches,
+            "algorithmic_flops": work["flops"] / launches, "launches_per_step": launches,
+            "roofline_ms": max(t_hbm, t_tc) * 1e3}
+
+
 def summarize(res, pk):
     work = res["work"]
     step_ms = statistics.median(res["step_ms"])
     dec_ms = [statistics.median([d[r] for d in res["decode_ms"]]) for r in range(len(res["decode_ms"][0]))]
     merge_ms = statistics.median(res["merge_ms"])
-    t_roof = max(work["kv_bytes"] / (pk["hbm_gbs"] * 1e9), work["flops"] / (pk["bf16_tflops"] * 1e12))
-    bound = "hbm" if work["kv_bytes"] / pk["hbm_gbs"] >= work["flops"] / (pk["bf16_tflops"] * 1e3) else "tensor"
     dec_total = sum(dec_ms)
+    roof = roofline_of(work, dec_total, len(dec_ms), pk, route_tag(res))
+    merge_gbs = work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 else None
     return dict(
         ms_per_step=step_ms,
         query_tok_s=work["tokens"] / (step_ms * 1e-3),
         decode_ms=dec_ms, merge_ms=merge_ms,
         kv_gbs=work["kv_bytes"] / (dec_total * 1e-3) / 1e9,
         tflops=work["flops"] / (dec_total * 1e-3) / 1e12,
-        roofline_bound=bound,
-        roofline_ms=t_roof * 1e3,
-        step_roofline_frac=t_roof * 1e3 / step_ms,
-        decode_roofline_frac=t_roof * 1e3 / dec_total,
-        merge_gbs=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 if merge_ms > 0 else None,
-        merge_hbm_frac=work["merge_bytes"] / (merge_ms * 1e-3) / 1e9 / pk["hbm_gbs"] if merge_ms > 0 else None,
+        roofline_bound=roof["bound"],
+        roofline_ms=roof["roofline_ms"],
+        step_roofline_frac=roof["roofline_ms"] / step_ms,
+        decode_roofline_frac=roof["frac"],
+        roofline=roof,
+        merge_gbs=merge_gbs,
+        merge_hbm_frac=merge_gbs / pk["hbm_gbs"] if merge_gbs is not None else None,
+        merge_bytes=work["merge_bytes"],
+        merge_traffic=profile_traffic(("merge_fused_" if res["fused"] else "merge_shards_") + res["name"]),
         kv_bytes=work["kv_bytes"], flops=work["flops"],
     )
+
+
+def rounded(d):
+    if isinstance(d, dict):
+        return {k: rounded(v) for k, v in d.items()}
+    if isinstance(d, list):
+        return [rounded(v) for v in d]
+    if isinstance(d, float):
+        return float(f"{d:.6g}")
+    return d
 
 
 def profile_traffic(kernel_tag):
@@ -447,37 +513,35 @@ def run_ours(args):
         head = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True, fused=True, clock=clk)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-        shards_route = time_workload(HEADLINE, args.steps, args.warmup, with_e2e=True)
-        # the same step with L2 emptied before each replay: the kernels' code
-        # then also comes from HBM, unlike in a serving loop
-        cold = time_workload(HEADLINE, args.steps, args.warmup, fused=True, l2_flush=True)
     clocks = clk.summary()
-    s_cold = summarize(cold, pk)
     s = summarize(head, pk)
-    s_shards = summarize(shards_route, pk)
     step_ms = replica_max_ms(s["ms_per_step"], "cuda")
     tokens = head["work"]["tokens"]
     value = whole_job_value(tokens, world, step_ms)
+    head_line = {k: head[k] for k in ("e2e", "launches")}
+    del head
+    torch.cuda.empty_cache()
 
+    # every workload on both routes (the headline's fused route is the line
+    # itself), and the dense fused route over FP8 caches
     configs = {}
     if args.configs != "headline" and rank == 0:
-        names = [n for n in ("plain_decode_d1", "mtp", "long_context", "sparse_mixed")
-                 if args.configs == "all" or n in args.configs.split(",")]
-        for n in names:
-            for fused in (False, True):
-                r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)), fused=fused)
-                cs = summarize(r, pk)
-                key = n + ("_fused" if fused else "")
-                configs[key] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cs.items()}
-                configs[key]["workload"] = DESCR[n] + ("; one shard-fused decode launch" if fused else
-                                                      "; D shard calls + merge call")
-                del r
-                torch.cuda.empty_cache()
+        names = [n for n in CONFIG_NAMES if args.configs == "all" or n in args.configs.split(",")]
+        runs = [(n, False, False) for n in names] + [(n, True, False) for n in names if n != HEADLINE]
+        runs += [(n, True, True) for n in FP8_NAMES if args.configs == "all" or n in args.configs.split(",")]
+        for n, fused, fp8 in runs:
+            r = time_workload(n, max(3, min(args.steps, 10)), max(3, min(args.warmup, 3)), fused=fused, fp8=fp8)
+            cs = summarize(r, pk)
+            key = n + ("_fp8" if fp8 else "") + ("_fused" if fused else "")
+            configs[key] = rounded(cs)
+            configs[key]["workload"] = DESCR[n] + (
+                "; FP8 E4M3 cache (codes of cache / 0.25, scale 0.25)" if fp8 else "") + (
+                "; one shard-fused decode launch" if fused else "; D shard calls + merge call")
+            del r
+            torch.cuda.empty_cache()
+        configs[HEADLINE + "_fused"] = dict(rounded(s), workload=DESCR[HEADLINE] + "; one shard-fused decode launch "
+                                                                                 "(the headline line)")
 
-    # dominant kernel: the shard-fused decode call (prep + one decode launch
-    # over every shard), timed as its own CUDA graph
-    dec_ms = statistics.median(d[0] for d in head["decode_ms"])
-    achieved = head["work"]["kv_bytes"] / (dec_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -492,36 +556,25 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded torch/numpy draws; no dataset)",
         "config": {"workload": DESCR[HEADLINE],
-                   "route": "one shard-fused decode launch over both DCP shards (the online softmax runs over "
-                            "shard 0's keys, then shard 1's: the LSE merge), plus its prep kernel",
-                   "l2": "inputs larger than L2, no flush: every step streams 302 MB of KV (> 129 MB L2) "
-                         "with an evict-first policy, so no step finds the previous one's KV in L2 "
-                         "(l2_flushed_step: the same step after a 256 MB write + 256 MB read flush)",
+                   "route": "one shard-fused decode launch over the 8 DCP shards (the online softmax runs over "
+                            "each shard's keys in turn: the LSE merge), plus its prep and split-merge kernels, then "
+                            "the W_UV projection of the merged rows",
+                   "l2": "inputs larger than L2, no flush: every step streams 0.9 GB of KV (> 129 MB L2)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "kv_gbs": s["kv_gbs"],
         "tflops": s["tflops"],
         "step_roofline_frac": s["step_roofline_frac"],
         "decode_roofline_frac": s["decode_roofline_frac"],
         "merge_hbm_frac": s["merge_hbm_frac"],
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm_gbs"], "traffic": profile_traffic("decode_fused_" + HEADLINE),
-                     "kernel": "shard-fused decode call (prep + one decode launch over both shards) as a CUDA "
-                               "graph, CUDA events around each replay on the launching stream",
-                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
-        "e2e": head["e2e"],
-        "shard_calls_route": {
-            "what": "the same step as D mla_dcp_decode calls + dcp_lse_merge (bf16 partials)",
-            "value": whole_job_value(tokens, world, s_shards["ms_per_step"]), "unit": UNIT,
-            "ms_per_step": s_shards["ms_per_step"], "decode_ms": s_shards["decode_ms"],
-            "merge_ms": s_shards["merge_ms"], "decode_roofline_frac": s_shards["decode_roofline_frac"],
-            "e2e": shards_route["e2e"]},
-        "l2_flushed_step": {
-            "what": "the headline step with L2 emptied before every replay (256 MB written, another 256 MB "
-                    "read); the kernels' instructions then come from HBM as well",
-            "ms_per_step": s_cold["ms_per_step"], "value": whole_job_value(tokens, world, s_cold["ms_per_step"]),
-            "unit": UNIT},
+        "roofline": dict(s["roofline"],
+                         kernel="shard-fused decode call (prep + decode + split-merge launches) as a CUDA graph, CUDA "
+                                "events around each replay on the launching stream",
+                         peak_source=pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS GEMM)",
+                         frac_of_sustained=s["roofline"]["achieved"] / pk["bf16_tflops_sustained"]
+                         if s["roofline"]["unit"] == "TFLOP/s" else None),
+        "e2e": head_line["e2e"],
         "clocks": clocks,
-        "gpu_launches": head["launches"],
+        "gpu_launches": head_line["launches"],
         "wall_s": wall,
         "configs": configs,
     }
@@ -553,29 +606,55 @@ def oracle_sample_step(w, h, threads):
 
 
 def oracle_sample(batch):
+    """``batch`` requests drawn as the headline workload draws its 32
+    (lengths U[16384, 32768], q_len 2, 128 heads, D=8, W_UV), on the host."""
     from mla_decode_attention_04_gb300 import workloads as wl
-    w = wl.plain_decode(dcp_world=2, batch=batch, device="cpu")
+    w = wl.NAMED[HEADLINE](device="cpu", batch=batch)
     h = dict(q_nope=wl.bf16_bits(w.q_nope), q_pe=wl.bf16_bits(w.q_pe), seq_lens=w.seq_lens.numpy(),
              qsl=w.query_start_loc.numpy(), caches=[wl.bf16_bits(s.cache) for s in w.shards],
-             tables=[s.block_table.numpy() for s in w.shards], w_uv=None)
+             tables=[s.block_table.numpy() for s in w.shards],
+             w_uv=None if w.w_uv is None else wl.bf16_bits(w.w_uv))
     return w, h
 
 
-def cpu_baseline(args, batch=16):
-    import oracle
-    threads = oracle.default_threads()
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def time_oracle(batch, threads, budget_s, max_reps):
     w, h = oracle_sample(batch)
     oracle_sample_step(w, h, threads)  # warm (loads the library)
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle_sample_step(w, h, threads)
         reps += 1
-        if time.perf_counter() - t0 > 10.0 or reps >= 50:
+        if time.perf_counter() - t0 > budget_s or reps >= max_reps:
             break
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": w.num_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{batch} of the 64 requests of the headline workload (context 4096, H=16, D=2: both shards "
-                      f"+ merge), fp64 C oracle, {reps} repetitions"}
+    return w.num_tokens / ((time.perf_counter() - t0) / reps), reps
+
+
+def cpu_baseline(args, batch=2):
+    import oracle
+    threads = oracle.default_threads()
+    log(f"cpu baseline: {batch} requests on {threads} threads")
+    v_all, reps = time_oracle(batch, threads, 10.0, 20)
+    log("cpu baseline: 1 request on 1 thread")
+    v_one, reps1 = time_oracle(1, 1, 1.0, 1)
+    log("cpu baseline: done")
+    return {"value": v_all, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{batch} requests drawn as the headline workload draws its 32 (q_len 2, H=128, context "
+                      f"U[16384,32768], all 8 shards + merge + W_UV), fp64 C oracle on {threads} threads, "
+                      f"{reps} repetitions",
+            "one_thread": {"value": v_one, "unit": UNIT, "cores": 1,
+                           "sample": f"1 request drawn the same way, 1 thread, {reps1} repetition"},
+            "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def run_reference(args):
@@ -585,7 +664,7 @@ def run_reference(args):
         return
     import oracle
     threads = oracle.default_threads()
-    w, h = oracle_sample(8)
+    w, h = oracle_sample(2)
     for _ in range(args.warmup):
         oracle_sample_step(w, h, threads)
     times = []
@@ -595,15 +674,16 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     ms = statistics.median(times) * 1e3
     value = w.num_tokens / (ms * 1e-3)
+    sample = ("2 requests per step, drawn as the headline workload draws its 32 (q_len 2, H=128, context "
+              "U[16384,32768], all 8 shards + merge + W_UV), fp64 C oracle")
     line = {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": DESCR[HEADLINE], "sample": "8 of the 64 requests per step"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "8 of the 64 requests of the headline workload per step (both shards + merge), "
-                                   "fp64 C oracle"},
+        "config": {"workload": DESCR[HEADLINE], "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+                         "nproc": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

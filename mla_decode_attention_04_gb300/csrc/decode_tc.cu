@@ -581,7 +581,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
   // 2 * part + 1: armed, bit 2 * part: parity): at exit the thread waits for
   // those phases, so no copy it issued lands after the CTA is gone.  Only the
   // last arming of a part can be outstanding: re-arming waits for the part's
-  // release, which follows its consumption.
+  // release, which follows its consumption.  Every arming of a part is
+  // recorded, a plain arrival too: a parity wait on an older round would
+  // alias once the barrier has completed two more.
   uint32_t armed[kMaxStages] = {0, 0, 0}, armed_stg[2] = {0, 0};
   auto note_armed = [](uint32_t& word, int m, uint32_t parity) {
     word = (word & ~(3u << (2 * m))) | ((2u | (parity & 1u)) << (2 * m));
@@ -624,7 +626,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
               issue_q_tma<NR>(maps, kv + st * kStageBytes, (int64_t)u.q0 * a.num_heads + u.row0, &sh.full[st][0]);
             else
               mbar_arrive_expect_tx(&sh.full[st][0], (uint32_t)u.nrows * (kRow * 2));
-            note_armed(armed[st], 0, ph);
+            // every part's record moves to this round, so none keeps an
+            // older round's parity that the barrier has since passed twice
+            for (int m = 0; m < kParts; ++m) note_armed(armed[st], m, ph);
             for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[st][m]);
           }
         }
@@ -795,7 +799,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
           } else {
             mbar_arrive(&sh.full[stage][0]);
           }
-          if (pt < w.nrows || pt == 0) note_armed(armed[stage], 0, phase);  // its bulk copies or TMA
+          // every part's record moves to this round (parts 1-3: a plain
+          // arrival), so none keeps an older round's parity
+          for (int m = 0; m < kParts; ++m) note_armed(armed[stage], m, phase);
           for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[stage][m]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }

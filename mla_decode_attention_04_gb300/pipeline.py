@@ -12,7 +12,8 @@ from __future__ import annotations
 import torch
 
 from . import (KV_LORA_RANK, V_HEAD_DIM, decode_workspace_size, dcp_lse_merge, fused_workspace_size, mla_dcp_decode,
-               mla_dcp_decode_fused, mla_sparse_dcp_decode, mla_sparse_dcp_decode_fused, sparse_workspace_size)
+               mla_dcp_decode_fused, mla_dcp_decode_fused_fp8, mla_sparse_dcp_decode, mla_sparse_dcp_decode_fused,
+               sparse_workspace_size)
 
 
 class DcpStep:
@@ -76,16 +77,20 @@ class FusedDcpStep:
     then shard 1's, ..., which is the LSE merge); sparse (``topk`` given):
     ``mla_sparse_dcp_decode_fused`` (each token over every used entry of its
     list).  Same outputs as ``DcpStep`` (``out``, ``lse``); no per-shard
-    partials or counts."""
+    partials or counts.  ``kv_scale`` given: the shard caches hold FP8 E4M3
+    codes (uint8) with that dequantisation scale (``mla_dcp_decode_fused_fp8``)."""
 
     def __init__(self, q_nope, q_pe, shards, seq_lens, query_start_loc, max_query_len, max_seq_len, scale, w_uv=None,
-                 out_dtype=torch.bfloat16, num_splits=0, topk=None, topk_valid=None):
+                 out_dtype=torch.bfloat16, num_splits=0, topk=None, topk_valid=None, kv_scale=None):
         self.q_nope, self.q_pe = q_nope, q_pe
         self.caches = [c for c, _ in shards]
         self.tables = [bt for _, bt in shards]
         self.seq_lens, self.qsl = seq_lens, query_start_loc
         self.max_query_len, self.max_seq_len, self.scale = int(max_query_len), int(max_seq_len), float(scale)
         self.w_uv, self.num_splits = w_uv, num_splits
+        self.kv_scale = None if kv_scale is None else float(kv_scale)
+        if self.kv_scale is not None and topk is not None:
+            raise ValueError("FP8 caches are served by the dense decode only")
         T, H = q_nope.shape[0], q_nope.shape[1]
         dev = q_nope.device
         self.D, self.T, self.H = len(shards), T, H
@@ -111,6 +116,10 @@ class FusedDcpStep:
             mla_sparse_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
                                         self.topk, self.topk_valid, self.scale, out=out, lse=lse,
                                         kept_counts=self.kept_counts, workspace=self.workspace, stream=stream)
+        elif self.kv_scale is not None:
+            mla_dcp_decode_fused_fp8(self.q_nope, self.q_pe, self.caches, self.kv_scale, self.tables, self.seq_lens,
+                                     self.qsl, self.max_query_len, self.max_seq_len, self.scale, out=out, lse=lse,
+                                     num_splits=self.num_splits, workspace=self.workspace, stream=stream)
         else:
             mla_dcp_decode_fused(self.q_nope, self.q_pe, self.caches, self.tables, self.seq_lens, self.qsl,
                                  self.max_query_len, self.max_seq_len, self.scale, out=out, lse=lse,
@@ -126,13 +135,17 @@ class FusedDcpStep:
         return self.out, self.lse
 
 
-def fused_step_for_workload(w, num_splits=0, sparse=None):
-    """FusedDcpStep for a ``workloads.Workload`` already on the GPU."""
+def fused_step_for_workload(w, num_splits=0, sparse=None, fp8_caches=None, kv_scale=None):
+    """FusedDcpStep for a ``workloads.Workload`` already on the GPU
+    (``fp8_caches`` + ``kv_scale``: per-shard FP8 code caches in the
+    workload's page layout, in place of its bf16 caches)."""
     sparse = (w.topk is not None) if sparse is None else sparse
-    shards = [(s.cache, s.block_table) for s in w.shards]
+    caches = fp8_caches if fp8_caches is not None else [s.cache for s in w.shards]
+    shards = [(c, s.block_table) for c, s in zip(caches, w.shards)]
     return FusedDcpStep(w.q_nope, w.q_pe, shards, w.seq_lens, w.query_start_loc, w.max_query_len, w.max_seq_len,
                         w.scale, w_uv=w.w_uv, num_splits=num_splits, topk=w.topk if sparse else None,
-                        topk_valid=w.topk_valid if sparse else None)
+                        topk_valid=w.topk_valid if sparse else None,
+                        kv_scale=kv_scale if fp8_caches is not None else None)
 
 
 def step_for_workload(w, partial_dtype=None, num_splits=0, sparse=None):
