@@ -541,6 +541,7 @@ int dcp_lse_merge(const void* partials, int32_t partial_dtype, const float* lses
   ma.out = out;
   ma.out_f32 = out_dtype == MLA_DTYPE_F32;
   ma.lse_out = lse_out;
+  ma.num_sms = current_sm_count();
   cudaError_t e = mla::launch_merge(ma, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   count_launch();

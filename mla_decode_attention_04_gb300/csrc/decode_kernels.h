@@ -51,9 +51,10 @@ struct MergeArgs {
   void* out;
   int32_t out_f32;
   float* lse_out;  // or NULL
+  int32_t num_sms;  // SMs of the device (grid sizing)
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
-// W_UV-fused merge on tensor cores (one CTA per head and 32 tokens).
+// W_UV-fused merge on tensor cores (CTAs per head, each over blocks of 32 tokens).
 cudaError_t launch_merge_wuv_tc(const MergeArgs& a, cudaStream_t stream);
 
 }  // namespace mla

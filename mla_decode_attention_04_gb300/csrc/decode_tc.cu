@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
     mbar_init(&sh.drain[1], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
-      mbar_init(&sh.s_free[b], 1);
+      mbar_init(&sh.s_free[b], 4);  // one arrival per softmax warp
     }
     mbar_init(&sh.p_ready, 1);
     mbar_init(&sh.pv_done, 1);
@@ -1207,6 +1207,12 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
             for (int e = 0; e < KPT; ++e) s[e] = __uint_as_float(v[e]);
           }
         }
+        // this warp's part of S is in registers: its lane quarter of the
+        // buffer is free for the score product of tile j + SB (each warp
+        // arrives once; the row max is exchanged after)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_free[j % SB]);
         int valid, tile_valid;  // keys of the tile this row sees / that exist
         if constexpr (SPARSE) {
           const int kbase = w.key0 + kt * kKeyTile;
@@ -1237,10 +1243,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
         sh.red[j & 1][kslice * NR + row] = pmax;
         tc_fence_before();
         named_bar_sync(1, 128);
-        if (st_tid == 0) {
-          mbar_arrive(&sh.s_free[j % SB]);
-          sh.any_rescale[(j + 1) & 1] = 0;
-        }
+        if (st_tid == 0) sh.any_rescale[(j + 1) & 1] = 0;
         {
           float tmax = -INFINITY;
 #pragma unroll

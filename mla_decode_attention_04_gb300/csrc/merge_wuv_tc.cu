@@ -26,10 +26,17 @@ using namespace tc;
 constexpr int kNT = 32;         // tokens per CTA (MMA N)
 constexpr int kThreads = 256;
 constexpr int kMaxShards = 64;
+constexpr int kWChunk = 16384;            // W_UV[h] rows of one 64-dim chunk: 64 dims x 128 outputs
+constexpr int kWBufs = 2;                 // W_UV chunk ring
+constexpr int kBChunk = kNT * 128;        // merged rows of one 64-dim chunk: 32 tokens x 128 B
+constexpr int kOffBHi = kWBufs * kWChunk;
+constexpr int kOffBLo = kOffBHi + 8 * kBChunk;
+constexpr int kOffShared = kOffBLo + 8 * kBChunk;
 
 struct MergeShared {
-  uint64_t w_full, mma_done;
+  uint64_t w_full[kWBufs], w_empty[kWBufs], mma_done;
   uint32_t tmem_base;
+  int32_t w_ok;  // every W_UV chunk landed and its MMAs were issued
   float wgt[kNT][kMaxShards];
 };
 
@@ -38,17 +45,35 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads) merge_wuv_tc_kernel(const __grid_constant__ CUtensorMap w_map,
-                                                                 MergeArgs a) {
+__device__ __forceinline__ void load_w_chunk(const CUtensorMap* w_map, uint8_t* dst, int h, int c, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, kWChunk);
+  const uint64_t pol = policy_evict_normal();  // every CTA of head h reads it
+  tma_load_3d(dst, w_map, 0, h * kNope + c * 64, 0, bar, pol);
+  tma_load_3d(dst + 8192, w_map, 64, h * kNope + c * 64, 0, bar, pol);
+}
+
+// One CTA per head h and 32 tokens (two CTAs fit on an SM; heads vary
+// fastest over the grid).  W_UV[h] streams
+// through a 2-chunk TMA ring; its first two chunks are requested before the
+// wait for the kernel that wrote the partials (W_UV is an input of the
+// call, not of that kernel).  Each thread merges one 8-dim piece of one
+// chunk for 8 of the tokens, all its partial loads in flight at once, and
+// writes the merged values as bf16 hi + lo; one thread then issues the
+// projection chunk by chunk as W_UV lands; four warps store the 128 x 32
+// result.
+__global__ void __launch_bounds__(kThreads, 2) merge_wuv_tc_kernel(const __grid_constant__ CUtensorMap w_map,
+                                                                    MergeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* w_s = base;                  // [2 atoms of 64 out][64 dims][128 B]  16 KB
-  uint8_t* b_hi = base + 16384;         // [32 tokens][64 dims] K-major SW128    4 KB
-  uint8_t* b_lo = base + 16384 + 4096;  //                                        4 KB
-  MergeShared& sh = *reinterpret_cast<MergeShared*>(base + 16384 + 8192);
+  uint8_t* w_s = base;              // [2][2 atoms of 64 outputs][64 dims][128 B]
+  uint8_t* b_hi = base + kOffBHi;   // [8 chunks][32 tokens][64 dims] K-major SW128
+  uint8_t* b_lo = base + kOffBLo;
+  MergeShared& sh = *reinterpret_cast<MergeShared*>(base + kOffShared);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, t0 = blockIdx.x * kNT;
+  // heads vary fastest over the grid, so the CTAs resident together read
+  // different heads' W_UV (not one head's lines from 15 SMs at once)
+  const int h = blockIdx.x, t0 = blockIdx.y * kNT;
   const int T = a.num_tokens, H = a.num_heads, D = a.dcp_world;
 
   if (warp == 0) {
@@ -56,33 +81,30 @@ __global__ void __launch_bounds__(kThreads) merge_wuv_tc_kernel(const __grid_con
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&sh.w_full, 1);
+    for (int b = 0; b < kWBufs; ++b) {
+      mbar_init(&sh.w_full[b], 1);
+      mbar_init(&sh.w_empty[b], 1);
+    }
     mbar_init(&sh.mma_done, 1);
     fence_mbar_init();
     prefetch_tmap(&w_map);
+    for (int b = 0; b < kWBufs; ++b) load_w_chunk(&w_map, w_s + b * kWChunk, h, b, &sh.w_full[b]);
   }
   grid_dep_sync();
   // merge weights: warp per token, lanes over shards
   for (int n = warp; n < kNT; n += kThreads / 32) {
     const int t = t0 + n;
-    for (int r0 = 0; r0 < D; r0 += 32) {
-      const int r = r0 + lane;
+    float m = -INFINITY;
+    for (int r = lane; r < D; r += 32) {
       float l = -INFINITY;
-      if (t < T && r < D) {
+      if (t < T) {
         const bool part = a.valid_counts ? a.valid_counts[(int64_t)r * T + t] > 0 : true;
         if (part) l = a.lses[((int64_t)r * T + t) * H + h];
         if (!(l > -INFINITY)) l = -INFINITY;  // NaN from a non-participating shard never enters
       }
-      if (r < kMaxShards) sh.wgt[n][r] = l;
+      sh.wgt[n][r] = l;
+      m = fmaxf(m, l);
     }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sh.tmem_base;
-  for (int n = warp; n < kNT; n += kThreads / 32) {
-    float m = -INFINITY;
-    for (int r = lane; r < D; r += 32) m = fmaxf(m, sh.wgt[n][r]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float z = 0.f;
@@ -90,88 +112,135 @@ __global__ void __launch_bounds__(kThreads) merge_wuv_tc_kernel(const __grid_con
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
     const float L = m > -INFINITY ? m + __logf(z) : -INFINITY;
-    __syncwarp();
     for (int r = lane; r < D; r += 32) sh.wgt[n][r] = L > -INFINITY ? __expf(sh.wgt[n][r] - L) : 0.f;
-    if (lane == 0 && a.lse_out && t0 + n < T) a.lse_out[(int64_t)(t0 + n) * H + h] = L;
+    if (lane == 0 && a.lse_out && t < T) a.lse_out[(int64_t)t * H + h] = L;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
 
-  const uint32_t idesc = idesc_bf16_f32(128, kNT, 1, 0);
-  const int n = tid >> 3;        // token of this thread in the merge
-  const int piece = tid & 7;     // 8 dims (16 bytes of bf16) of the 64-dim chunk
-  const int t = t0 + n;
-  bool ok = true;
-  for (int c = 0; c < 8; ++c) {
-    if (tid == 0) {
-      // previous chunk's MMAs must be done before W / B buffers are reused
-      if (c > 0 && !mbar_wait(&sh.mma_done, (c - 1) & 1)) ok = false;
-      mbar_arrive_expect_tx(&sh.w_full, 16384);
-      const uint64_t pol = policy_evict_first();
-      tma_load_3d(w_s, &w_map, 0, h * kNope + c * 64, 0, &sh.w_full, pol);
-      tma_load_3d(w_s + 8192, &w_map, 64, h * kNope + c * 64, 0, &sh.w_full, pol);
-    }
-    __syncthreads();  // buffers free (thread 0 waited for the previous MMAs)
-    float acc[8];
+  // this thread's piece: dims c * 64 + 8 piece .. + 7 of tokens n0 + 4 i, i < 8
+  const int c = (tid >> 3) & 7, piece = tid & 7, n0 = tid >> 6;
+  float acc[8][8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-    if (t < T) {
-      for (int r = 0; r < D; ++r) {
-        const float wr = sh.wgt[n][r];
-        if (wr == 0.f) continue;
-        const int64_t prow = ((int64_t)r * T + t) * H + h;
-        if (a.partial_f32) {
-          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.partials) + prow * kNope +
-                                                            c * 64 + piece * 8);
-          const float4 x = p[0], y = p[1];
-          acc[0] += wr * x.x; acc[1] += wr * x.y; acc[2] += wr * x.z; acc[3] += wr * x.w;
-          acc[4] += wr * y.x; acc[5] += wr * y.y; acc[6] += wr * y.z; acc[7] += wr * y.w;
-        } else {
-          const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.partials) +
-                                                          prow * kNope + c * 64 + piece * 8);
-          acc[0] += wr * bf16_lo(x.x); acc[1] += wr * bf16_hi(x.x);
-          acc[2] += wr * bf16_lo(x.y); acc[3] += wr * bf16_hi(x.y);
-          acc[4] += wr * bf16_lo(x.z); acc[5] += wr * bf16_hi(x.z);
-          acc[6] += wr * bf16_lo(x.w); acc[7] += wr * bf16_hi(x.w);
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+  for (int r = 0; r < D; ++r) {
+    float wr[8];
+    int64_t prow[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int n = n0 + 4 * i, t = t0 + n;
+      wr[i] = t < T ? sh.wgt[n][r] : 0.f;
+      prow[i] = ((int64_t)r * T + (t < T ? t : 0)) * H + h;
+    }
+    if (a.partial_f32) {
+      float4 x[8], y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[i] = y[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (wr[i] != 0.f) {
+          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.partials) +
+                                                            prow[i] * kNope + c * 64 + piece * 8);
+          x[i] = p[0];
+          y[i] = p[1];
         }
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i][0] += wr[i] * x[i].x; acc[i][1] += wr[i] * x[i].y; acc[i][2] += wr[i] * x[i].z;
+        acc[i][3] += wr[i] * x[i].w; acc[i][4] += wr[i] * y[i].x; acc[i][5] += wr[i] * y[i].y;
+        acc[i][6] += wr[i] * y[i].z; acc[i][7] += wr[i] * y[i].w;
+      }
+    } else {
+      uint4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (wr[i] != 0.f)
+          x[i] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.partials) + prow[i] * kNope +
+                                                 c * 64 + piece * 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i][0] += wr[i] * bf16_lo(x[i].x); acc[i][1] += wr[i] * bf16_hi(x[i].x);
+        acc[i][2] += wr[i] * bf16_lo(x[i].y); acc[i][3] += wr[i] * bf16_hi(x[i].y);
+        acc[i][4] += wr[i] * bf16_lo(x[i].z); acc[i][5] += wr[i] * bf16_hi(x[i].z);
+        acc[i][6] += wr[i] * bf16_lo(x[i].w); acc[i][7] += wr[i] * bf16_hi(x[i].w);
+      }
     }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = n0 + 4 * i;
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float a0 = acc[2 * k], a1 = acc[2 * k + 1];
+      const float a0 = acc[i][2 * k], a1 = acc[i][2 * k + 1];
       const float h0 = __bfloat162float(__float2bfloat16_rn(a0));
       const float h1 = __bfloat162float(__float2bfloat16_rn(a1));
       hi[k] = pack_bf16(h0, h1);
       lo[k] = pack_bf16(a0 - h0, a1 - h1);
     }
-    const int off = (n >> 3) * 1024 + (n & 7) * 128 + ((piece ^ (n & 7)) << 4);
+    const int off = c * kBChunk + (n >> 3) * 1024 + (n & 7) * 128 + ((piece ^ (n & 7)) << 4);
     *reinterpret_cast<uint4*>(b_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
     *reinterpret_cast<uint4*>(b_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      if (!mbar_wait(&sh.w_full, c & 1)) ok = false;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    // Y^T [128 x 32] = W_UV[h]^T . O^T over 8 chunks of 64 dims (hi and lo
+    // terms); chunk cc + 2 is requested once chunk cc's MMAs are done
+    const uint32_t idesc = idesc_bf16_f32(128, kNT, 1, 0);
+    const uint32_t bh = smem_u32(b_hi), bl = smem_u32(b_lo);
+    bool ok = true;
+    uint32_t armed = 0x3u;  // W buffers with a load in flight (landing on phase armed_ph[b])
+    uint32_t armed_ph[kWBufs] = {0, 0};
+    for (int cc = 0; cc < 8 && ok; ++cc) {
+      const int b = cc & (kWBufs - 1);
+      if (!mbar_wait(&sh.w_full[b], (cc >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      armed &= ~(1u << b);
       tc_fence_after();
-      const uint32_t wa = smem_u32(w_s), bh = smem_u32(b_hi), bl = smem_u32(b_lo);
+      const uint32_t wa = smem_u32(w_s + b * kWChunk);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ad = smem_desc_sw128(wa + kk * 2048, 8192, 1024);
-        mma_ss(tmem, ad, smem_desc_sw128(bh + kk * 32, 16, 1024), idesc, (c | kk) != 0);
-        mma_ss(tmem, ad, smem_desc_sw128(bl + kk * 32, 16, 1024), idesc, 1);
+        mma_ss(tmem, ad, smem_desc_sw128(bh + cc * kBChunk + kk * 32, 16, 1024), idesc, (cc | kk) != 0);
+        mma_ss(tmem, ad, smem_desc_sw128(bl + cc * kBChunk + kk * 32, 16, 1024), idesc, 1);
       }
-      mma_commit(&sh.mma_done);
+      mma_commit(&sh.w_empty[b]);
+      if (cc + kWBufs < 8) {
+        if (!mbar_wait(&sh.w_empty[b], (cc >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        load_w_chunk(&w_map, w_s + b * kWChunk, h, cc + kWBufs, &sh.w_full[b]);
+        armed |= 1u << b;
+        armed_ph[b] = ((cc + kWBufs) >> 1) & 1;
+      }
     }
+    mma_commit(&sh.mma_done);  // every MMA issued above (none: arrives at once)
+    sh.w_ok = ok ? 1 : 0;
+    // a give-up leaves copies in flight: they land before the CTA exits
+    for (int b = 0; b < kWBufs; ++b)
+      if ((armed >> b) & 1u) mbar_wait(&sh.w_full[b], armed_ph[b]);
   }
+  __syncthreads();
   // epilogue: warps 0-3 read the 128 output dims (lanes) x 32 tokens (columns)
   if (warp < 4) {
-    if (!mbar_wait(&sh.mma_done, 7 & 1)) ok = false;
+    const bool done = mbar_wait(&sh.mma_done, 0) && sh.w_ok;
     tc_fence_after();
     uint32_t y[32];
     tmem_ld<32>(tmem + ((uint32_t)(warp * 32) << 16), y);
     tmem_wait_ld();
     const int v = warp * 32 + lane;
-    for (int k = 0; k < kNT; ++k) {
+    for (int k = 0; k < kNT && done; ++k) {
       const int tt = t0 + k;
       if (tt >= T) break;
       const int64_t idx = ((int64_t)tt * H + h) * kVHead + v;
@@ -180,7 +249,6 @@ __global__ void __launch_bounds__(kThreads) merge_wuv_tc_kernel(const __grid_con
       else static_cast<__nv_bfloat16*>(a.out)[idx] = __float2bfloat16_rn(val);
     }
   }
-  (void)ok;  // a give-up leaves this block's output unspecified; waits are bounded so the kernel returns
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -208,10 +276,10 @@ cudaError_t launch_merge_wuv_tc(const MergeArgs& a, cudaStream_t stream) {
   if (a.num_tokens <= 0) return cudaSuccess;
   CUtensorMap map;
   if (!make_wuv_tensor_map(&map, a.w_uv, (int64_t)a.num_heads * kNope)) return cudaErrorInvalidValue;
-  const size_t smem = 1024 + 16384 + 8192 + sizeof(MergeShared);
+  const size_t smem = 1024 + kOffShared + sizeof(MergeShared);
   cudaError_t e = cudaFuncSetAttribute(merge_wuv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.num_tokens + kNT - 1) / kNT, a.num_heads);
+  dim3 grid(a.num_heads, (a.num_tokens + kNT - 1) / kNT);
   return launch_pdl(merge_wuv_tc_kernel, grid, dim3(kThreads), smem, stream, map, a);
 }
 
