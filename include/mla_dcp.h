@@ -319,6 +319,47 @@ int mla_sparse_dcp_decode_fused(const void *q_nope, int64_t q_nope_row_stride, c
                                 int32_t *kept_counts, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * mla_dcp_decode_two_stage -- the two-stage decomposition of a DCP decode
+ * step with q_len >= 1, for one GPU that holds all D shard slices: the
+ * alternative to a custom mask offered in the review thread of
+ * "[Attention] add DCP support for FLASH_ATTN_MLA backend" (context keys with
+ * the causal mask off, the query's own keys with it on, results merged).
+ * For request b with L keys and q_len queries:
+ *   stage 1  every query row over the context positions [0, L - q_len), no
+ *            mask: a shard-fused dense decode whose sequence lengths are the
+ *            context lengths (derived on the device);
+ *   stage 2  query i over the new positions L - q_len .. L - q_len + i: the
+ *            shard-fused sparse decode over per-token position lists built on
+ *            the device (list width max_query_len);
+ *   merge    the two (out, lse) results by LSE (dcp_lse_merge with the two
+ *            stages as its two partials).
+ * The result equals mla_dcp_decode_fused's (the causal DCP attention over
+ * all L keys), up to rounding; a row's stage-1 result is empty (lse -inf)
+ * when its request has no context.  Launches: the prep kernel, stage 1's
+ * three, stage 2's two, a status fold and the merge; no host copy.
+ *
+ *  Arguments as mla_dcp_decode_fused (kv_cache_dtype BF16 only); num_splits
+ *  is not taken.
+ *  max_query_len  >= every request's q_len (the list width), 1..65536 when
+ *               num_tokens > 0.
+ *  workspace    device scratch of at least
+ *               mla_dcp_decode_two_stage_workspace_size() bytes, 256-byte
+ *               aligned; its status word (mla_workspace_status) reports the
+ *               first failing check of either stage.
+ *  Errors as mla_dcp_decode_fused.
+ * ---------------------------------------------------------------------- */
+size_t mla_dcp_decode_two_stage_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                               int32_t max_query_len, int32_t max_seq_len);
+
+int mla_dcp_decode_two_stage(const void *q_nope, int64_t q_nope_row_stride, const void *q_pe,
+                             int64_t q_pe_row_stride, const void *const *kv_caches, const int64_t *num_blocks,
+                             int32_t page_size, int32_t kv_cache_dtype, const int32_t *const *block_tables,
+                             int32_t block_table_stride, const int32_t *seq_lens, const int32_t *query_start_loc,
+                             int32_t num_requests, int32_t num_tokens, int32_t num_heads, int32_t max_query_len,
+                             int32_t max_seq_len, int32_t dcp_world, float scale, void *out, int32_t out_dtype,
+                             float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * mla_workspace_status -- synchronises `stream`, then reads the status word
  * the kernels keep in a decode workspace: MLA_OK, or MLA_ERR_DEVICE_CHECK
  * with *detail set to the first failing check's code: 1 = a page id (or its

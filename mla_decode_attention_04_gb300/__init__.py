@@ -33,6 +33,7 @@ EXPORTS = [
     "mla_sparse_dcp_decode", "dcp_lse_merge", "mla_workspace_status", "mla_kernel_launch_count",
     "mla_dcp_decode_static_scratch", "mla_dcp_decode_fused_workspace_size", "mla_dcp_decode_fused",
     "mla_sparse_dcp_decode_fused", "mla_dcp_decode_fp8", "mla_dcp_decode_fused_fp8", "mla_debug_set_wait_budget_ns",
+    "mla_dcp_decode_two_stage_workspace_size", "mla_dcp_decode_two_stage",
 ]
 
 # Size of the library's fixed device scratch array used by
@@ -84,6 +85,11 @@ def _bind(lib):
     lib.mla_dcp_decode_fused_fp8.restype = ctypes.c_int
     lib.mla_dcp_decode_fused_fp8.argtypes = [vp, i64, vp, i64, vp, vp, i32, f32, vp, i32, vp, vp, i32, i32, i32, i32,
                                              i32, i32, f32, vp, i32, vp, i32, vp, sz, vp]
+    lib.mla_dcp_decode_two_stage_workspace_size.restype = sz
+    lib.mla_dcp_decode_two_stage_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.mla_dcp_decode_two_stage.restype = ctypes.c_int
+    lib.mla_dcp_decode_two_stage.argtypes = [vp, i64, vp, i64, vp, vp, i32, i32, vp, i32, vp, vp, i32, i32, i32, i32,
+                                             i32, i32, f32, vp, i32, vp, vp, sz, vp]
     lib.mla_debug_set_wait_budget_ns.restype = None
     lib.mla_debug_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
     lib.mla_dcp_decode_static_scratch.restype = ctypes.c_int
@@ -268,6 +274,56 @@ def mla_dcp_decode_fused_fp8(q_nope, q_pe, kv_caches, kv_scale, block_tables, se
 def fused_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, num_splits=0) -> int:
     return int(load_library().mla_dcp_decode_fused_workspace_size(num_requests, num_tokens, num_heads, max_query_len,
                                                                    max_seq_len, num_splits))
+
+
+def two_stage_workspace_size(num_requests, num_tokens, num_heads, max_query_len, max_seq_len) -> int:
+    return int(load_library().mla_dcp_decode_two_stage_workspace_size(num_requests, num_tokens, num_heads,
+                                                                       max_query_len, max_seq_len))
+
+
+def mla_dcp_decode_two_stage(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_start_loc, max_query_len,
+                             max_seq_len, scale, out=None, lse=None, out_dtype=torch.bfloat16, workspace=None,
+                             stream=None):
+    """The two-stage decomposition of the step over all D shards: each
+    query row over its request's context without a mask, then over the new
+    keys up to its own position, the two merged by LSE.  Returns the merged
+    (out [T,H,512], lse [T,H]); equals ``mla_dcp_decode_fused`` up to
+    rounding."""
+    lib = load_library()
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    B = seq_lens.shape[0]
+    D = len(kv_caches)
+    if len(block_tables) != D or D < 1:
+        raise ValueError("kv_caches and block_tables need one entry per shard")
+    sn, sp = _row_stride(q_nope, KV_LORA_RANK, "q_nope"), _row_stride(q_pe, ROPE_DIM, "q_pe")
+    kv_args = [_kv_args(c) for c in kv_caches]
+    ps, kv_dt = kv_args[0][1], kv_args[0][2]
+    if any(a[1] != ps or a[2] != kv_dt for a in kv_args):
+        raise ValueError("all shard caches need the same page size and dtype")
+    bt_stride = block_tables[0].shape[1]
+    for bt in block_tables:
+        _i32(bt, "block_table")
+        if bt.shape[1] != bt_stride:
+            raise ValueError("all block tables need the same row stride")
+    _i32(seq_lens, "seq_lens"), _i32(query_start_loc, "query_start_loc")
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty((T, H, KV_LORA_RANK), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if workspace is None:  # (the library checks a given workspace's size itself)
+        need = two_stage_workspace_size(B, T, H, max_query_len, max_seq_len)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    kv_ptrs = (ctypes.c_void_p * D)(*[c.data_ptr() for c in kv_caches])
+    nbs = (ctypes.c_int64 * D)(*[a[0] for a in kv_args])
+    bt_ptrs = (ctypes.c_void_p * D)(*[bt.data_ptr() for bt in block_tables])
+    _check(lib.mla_dcp_decode_two_stage(_ptr(q_nope), sn, _ptr(q_pe), sp, ctypes.cast(kv_ptrs, ctypes.c_void_p),
+                                        ctypes.cast(nbs, ctypes.c_void_p), ps, kv_dt,
+                                        ctypes.cast(bt_ptrs, ctypes.c_void_p), bt_stride, _ptr(seq_lens),
+                                        _ptr(query_start_loc), B, T, H, int(max_query_len), int(max_seq_len), D,
+                                        float(scale), _ptr(out), _DT[out.dtype], _ptr(lse), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
 
 
 def mla_dcp_decode_fused(q_nope, q_pe, kv_caches, block_tables, seq_lens, query_start_loc, max_query_len,

@@ -183,7 +183,8 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
                  const int32_t* query_start_loc, int32_t num_requests, int32_t num_tokens, int32_t num_heads,
                  int32_t max_query_len, int32_t max_seq_len, int32_t dcp_world, float scale, void* out,
                  int32_t out_dtype, float* lse, int32_t* row_counts, int32_t num_splits, void* workspace,
-                 size_t workspace_bytes, void* stream, bool kv_fp8 = false, float kv_scale = 1.f) {
+                 size_t workspace_bytes, void* stream, bool kv_fp8 = false, float kv_scale = 1.f,
+                 bool causal = true) {
   if (max_seq_len < 0 || num_splits < 0 || num_splits > 1024)
     return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d / num_splits %d out of range", max_seq_len, num_splits);
   if (num_tokens == 0) return ok();
@@ -209,6 +210,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   pa.shard0 = shard0;
   pa.nshard = nshard;
   pa.rows_per_group = plan.rows_per_group;
+  pa.noncausal = causal ? 0 : 1;
   pa.hdr = hdr;
   pa.row_counts = row_counts;
   pa.out = out;
@@ -252,6 +254,7 @@ int dense_decode(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe
   da.unit_penalty = plan.unit_penalty;
   da.gang = plan.gang;
   da.wait_ns = g_wait_budget_ns.load(std::memory_order_relaxed);
+  da.noncausal = causal ? 0 : 1;
   da.split_desc = reinterpret_cast<int4*>(ws + plan.off_desc);
   da.part_lse = reinterpret_cast<float*>(ws + plan.off_plse);
   da.part_o = reinterpret_cast<float*>(ws + plan.off_po);
@@ -513,6 +516,126 @@ int mla_sparse_dcp_decode_fused(const void* q_nope, int64_t q_nope_row_stride, c
                        page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests,
                        num_tokens, num_heads, topk_indices, topk, topk_valid, dcp_world, scale, out, out_dtype, lse,
                        kept_counts, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Where the two-stage call keeps its pieces inside its workspace (byte
+// offsets, 256-byte aligned): the first stage's dense workspace at 0 (its
+// status word is the call's), the second stage's sparse workspace, the two
+// stages' fp32 results and LSEs (the merge's two partials), and the device
+// inputs the prep kernel derives.
+struct TwoStageLayout {
+  size_t sparse, parts, lses, lists, valid, ctx, total;
+};
+
+TwoStageLayout two_stage_layout(int32_t num_requests, int32_t num_tokens, int32_t num_heads, int32_t max_query_len,
+                                int32_t max_seq_len) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t T = num_tokens > 0 ? (size_t)num_tokens : 0, H = num_heads > 0 ? (size_t)num_heads : 0;
+  const size_t B = num_requests > 0 ? (size_t)num_requests : 0;
+  const size_t W = max_query_len > 0 ? (size_t)max_query_len : 1;
+  TwoStageLayout L;
+  L.sparse = al(dense_workspace_bytes(num_requests, num_tokens, num_heads, max_query_len, max_seq_len, 1, 0));
+  L.parts = L.sparse + al(mla::make_sparse_plan(num_tokens, num_heads, (int32_t)W, current_sm_count()).total);
+  L.lses = L.parts + al(2 * T * H * mla::kNope * sizeof(float));
+  L.lists = L.lses + al(2 * T * H * sizeof(float));
+  L.valid = L.lists + al(T * W * sizeof(int32_t));
+  L.ctx = L.valid + al(T * sizeof(int32_t));
+  L.total = L.ctx + al(B * sizeof(int32_t));
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_dcp_decode_two_stage_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,
+                                               int32_t max_query_len, int32_t max_seq_len) {
+  return two_stage_layout(num_requests, num_tokens, num_heads, max_query_len, max_seq_len).total;
+}
+
+int mla_dcp_decode_two_stage(const void* q_nope, int64_t q_nope_row_stride, const void* q_pe, int64_t q_pe_row_stride,
+                             const void* const* kv_caches, const int64_t* num_blocks, int32_t page_size,
+                             int32_t kv_cache_dtype, const int32_t* const* block_tables, int32_t block_table_stride,
+                             const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_requests,
+                             int32_t num_tokens, int32_t num_heads, int32_t max_query_len, int32_t max_seq_len,
+                             int32_t dcp_world, float scale, void* out, int32_t out_dtype, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (dcp_world < 1 || dcp_world > mla::kMaxShards)
+    return fail(MLA_ERR_INVALID_ARG, "dcp_world %d not in [1, %d] for the two-stage call", dcp_world,
+                mla::kMaxShards);
+  if (kv_caches == nullptr || num_blocks == nullptr || block_tables == nullptr)
+    return fail(MLA_ERR_INVALID_ARG, "kv_caches / num_blocks / block_tables arrays are NULL");
+  for (int r = 0; r < dcp_world; ++r) {
+    int rc = check_decode_common(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, kv_caches[r], num_blocks[r],
+                                 page_size, kv_cache_dtype, block_tables[r], block_table_stride, seq_lens,
+                                 query_start_loc, num_requests, num_tokens, num_heads, dcp_world, r, scale, out,
+                                 out_dtype, lse, workspace);
+    if (rc != MLA_OK) return rc;
+  }
+  if (max_seq_len < 0) return fail(MLA_ERR_INVALID_ARG, "max_seq_len %d < 0", max_seq_len);
+  if (num_tokens == 0) return ok();
+  if (max_query_len < 1 || max_query_len > 65536)
+    return fail(MLA_ERR_INVALID_ARG, "max_query_len %d not in [1, 65536]", max_query_len);
+  const TwoStageLayout L = two_stage_layout(num_requests, num_tokens, num_heads, max_query_len, max_seq_len);
+  if (workspace_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", workspace_bytes, L.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* parts = reinterpret_cast<float*>(ws + L.parts);
+  float* lses = reinterpret_cast<float*>(ws + L.lses);
+  const int64_t rows = (int64_t)num_tokens * num_heads;
+
+  mla::TwoStageArgs ta{};
+  ta.seq_lens = seq_lens;
+  ta.query_start_loc = query_start_loc;
+  ta.num_requests = num_requests;
+  ta.num_tokens = num_tokens;
+  ta.list_stride = max_query_len;
+  ta.ctx_lens = reinterpret_cast<int32_t*>(ws + L.ctx);
+  ta.new_keys = reinterpret_cast<int32_t*>(ws + L.lists);
+  ta.new_valid = reinterpret_cast<int32_t*>(ws + L.valid);
+  cudaError_t e = mla::launch_two_stage_prep(ta, st);
+  if (e != cudaSuccess) return cuda_fail(e, "two-stage prep launch");
+  count_launch();
+  // stage 1: every query row over its request's whole context, no mask
+  int rc = dense_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, dcp_world, 0, kv_caches, num_blocks,
+                        page_size, block_tables, block_table_stride, ta.ctx_lens, query_start_loc, num_requests,
+                        num_tokens, num_heads, max_query_len, max_seq_len, dcp_world, scale, parts, MLA_DTYPE_F32,
+                        lses, nullptr, 0, ws, L.sparse, stream, false, 1.f, /*causal=*/false);
+  if (rc != MLA_OK) return rc;
+  // stage 2: every query row over the new keys up to its own position
+  rc = sparse_decode(q_nope, q_nope_row_stride, q_pe, q_pe_row_stride, dcp_world, 0, kv_caches, num_blocks,
+                     page_size, block_tables, block_table_stride, seq_lens, query_start_loc, num_requests, num_tokens,
+                     num_heads, ta.new_keys, max_query_len, ta.new_valid, dcp_world, scale, parts + rows * mla::kNope,
+                     MLA_DTYPE_F32, lses + rows, nullptr, ws + L.sparse, L.parts - L.sparse, stream);
+  if (rc != MLA_OK) return rc;
+  e = mla::launch_fold_status(reinterpret_cast<mla::WorkspaceHeader*>(ws),
+                              reinterpret_cast<const mla::WorkspaceHeader*>(ws + L.sparse), st);
+  if (e != cudaSuccess) return cuda_fail(e, "status fold launch");
+  count_launch();
+  // the two stages' results merged by LSE (a row without context keys has
+  // lse -inf and output 0 from stage 1: weight 0)
+  mla::MergeArgs ma{};
+  ma.partials = parts;
+  ma.partial_f32 = 1;
+  ma.lses = lses;
+  ma.valid_counts = nullptr;
+  ma.w_uv = nullptr;
+  ma.dcp_world = 2;
+  ma.num_tokens = num_tokens;
+  ma.num_heads = num_heads;
+  ma.out = out;
+  ma.out_f32 = out_dtype == MLA_DTYPE_F32;
+  ma.lse_out = lse;
+  ma.num_sms = current_sm_count();
+  e = mla::launch_merge(ma, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  count_launch();
+  return ok();
 }
 
 int dcp_lse_merge(const void* partials, int32_t partial_dtype, const float* lses, const int32_t* valid_counts,

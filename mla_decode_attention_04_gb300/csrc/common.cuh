@@ -100,10 +100,13 @@ struct ReqFacts {
 
 // The facts of request b from its raw inputs q0 = query_start_loc[b],
 // q1 = query_start_loc[b + 1] and L = seq_lens[b].
+// causal = false: the non-causal context pass of the two-stage
+// decomposition, whose length L is the request's context only (q_len may
+// exceed it).
 __device__ __forceinline__ ReqFacts request_facts_of(int q0, int q1, int L, int num_tokens, int H, int D, int shard0,
-                                                     int nshard, int NR) {
+                                                     int nshard, int NR, bool causal = true) {
   ReqFacts f;
-  f.ok = !(q1 - q0 < 0 || q1 - q0 > L || q0 < 0 || q1 > num_tokens);
+  f.ok = !(q1 - q0 < 0 || (causal && q1 - q0 > L) || q0 < 0 || q1 > num_tokens);
   f.q0 = q0 < 0 ? 0 : q0;
   f.q_len = f.ok ? q1 - q0 : 0;
   f.seq_len = L;
@@ -115,9 +118,10 @@ __device__ __forceinline__ ReqFacts request_facts_of(int q0, int q1, int L, int 
 }
 
 __device__ __forceinline__ ReqFacts request_facts(const int32_t* seq_lens, const int32_t* query_start_loc, int b,
-                                                  int num_tokens, int H, int D, int shard0, int nshard, int NR) {
+                                                  int num_tokens, int H, int D, int shard0, int nshard, int NR,
+                                                  bool causal = true) {
   return request_facts_of(query_start_loc[b], query_start_loc[b + 1], seq_lens[b], num_tokens, H, D, shard0, nshard,
-                          NR);
+                          NR, causal);
 }
 
 // Walks a request's key-tile sequence (shard k's local keys as whole tiles,

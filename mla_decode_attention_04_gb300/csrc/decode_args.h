@@ -28,6 +28,9 @@ struct DecodeArgs {
   // budget of each pipeline wait in ns (2 s unless a test shortens it);
   // waits for copies already in flight when a role gave up have their own
   uint64_t wait_ns;
+  // 1: every row sees every key of its request (seq_lens then hold the
+  // context lengths: the first pass of the two-stage decomposition)
+  int32_t noncausal;
   void* out;  // [T, H, 512]
   int32_t out_f32;
   float* lse;  // [T, H]

@@ -57,4 +57,20 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 // W_UV-fused merge on tensor cores (CTAs per head, each over blocks of 32 tokens).
 cudaError_t launch_merge_wuv_tc(const MergeArgs& a, cudaStream_t stream);
 
+// Device inputs of the two-stage decomposition: ctx_lens[b] = L_b - q_len_b,
+// new_keys[t][j] = the j-th new-key position of token t (-1 past its own
+// position), new_valid[t] = its count.
+struct TwoStageArgs {
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int32_t num_requests, num_tokens;
+  int32_t list_stride;  // >= the largest q_len
+  int32_t* ctx_lens;    // [num_requests]
+  int32_t* new_keys;    // [num_tokens, list_stride]
+  int32_t* new_valid;   // [num_tokens]
+};
+cudaError_t launch_two_stage_prep(const TwoStageArgs& a, cudaStream_t stream);
+// main->status takes other's first failure when main has none.
+cudaError_t launch_fold_status(WorkspaceHeader* main, const WorkspaceHeader* other, cudaStream_t stream);
+
 }  // namespace mla

@@ -213,7 +213,8 @@ struct Source {
       f.nt = (r0 + kKeyTile - 1) / kKeyTile;
       return f;
     } else {
-      return request_facts_of(r0, r1, r2, a.num_tokens, a.num_heads, a.dcp_world, a.shard0, a.nshard, NR);
+      return request_facts_of(r0, r1, r2, a.num_tokens, a.num_heads, a.dcp_world, a.shard0, a.nshard, NR,
+                              !a.noncausal);
     }
   }
 };
@@ -1186,7 +1187,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
       if constexpr (SPARSE) {
         if (row < w.nrows) kend = w.key1;
       } else {
-        if (row < w.nrows) P_row = w.seq_len - w.q_len + (w.row0 + row) / H;
+        // the row's global position (non-causal: the request's last key, so
+        // the row sees them all)
+        if (row < w.nrows) P_row = a.noncausal ? w.seq_len - 1 : w.seq_len - w.q_len + (w.row0 + row) / H;
         cur_sh.start(w.seq_len, a.dcp_world, a.shard0);
         cur_sh.seek(w.t0, w.seq_len, a.dcp_world, a.shard0, nshard);
         lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
   const int nthreads = gridDim.x * blockDim.x, tid = blockIdx.x * blockDim.x + threadIdx.x;
   for (int b = tid; b < a.num_requests; b += nthreads) {
     const ReqFacts f = request_facts(a.seq_lens, a.query_start_loc, b, a.num_tokens, H, a.dcp_world, a.shard0,
-                                     a.nshard, a.rows_per_group);
+                                     a.nshard, a.rows_per_group, !a.noncausal);
     if (!f.ok) record_check(a.hdr, kCheckBadQueryLayout);
     if (f.nt == 0 && f.q_len > 0) {
       // no local key: the rows' final result (no decode unit covers them)
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256) prep_kernel(PrepArgs a) {
     }
     if (a.row_counts) {  // one-shard calls only
       for (int i = 0; i < f.q_len; ++i) {
-        const int P = f.seq_len - f.q_len + i;
+        const int P = a.noncausal ? f.seq_len - 1 : f.seq_len - f.q_len + i;
         a.row_counts[f.q0 + i] = min(visible_keys(P, a.dcp_world, a.shard0), f.local_len);
       }
     }

@@ -15,6 +15,7 @@ struct PrepArgs {
   int32_t num_requests, num_tokens, num_heads, dcp_world;
   int32_t shard0, nshard;  // the shards the decode covers (one, or all D when fused)
   int32_t rows_per_group;
+  int32_t noncausal;  // every row sees every key of its request
   WorkspaceHeader* hdr;
   int32_t* row_counts;  // may be NULL
   // rows of requests without local keys get their final result here
