@@ -657,6 +657,54 @@ def cpu_baseline(args, batch=2):
             "nproc": os.cpu_count(), "cpu_model": cpu_model()}
 
 
+def oracle_full_step(w, threads):
+    """The oracle's whole step on workload w, dense or sparse: every shard's
+    attention, the LSE merge (with the sparse counts) and W_UV."""
+    import oracle
+    from mla_decode_attention_04_gb300 import workloads as wl
+    qn, qp = wl.bf16_bits(w.q_nope), wl.bf16_bits(w.q_pe)
+    L, qsl = w.seq_lens.numpy(), w.query_start_loc.numpy()
+    parts, lses, counts = [], [], []
+    for r, sh in enumerate(w.shards):
+        cache, table = wl.bf16_bits(sh.cache), sh.block_table.numpy()
+        if w.topk is None:
+            o, l, c = oracle.dcp_decode(qn, qp, cache, table, L, qsl, w.dcp_world, r, w.scale, threads=threads)
+        else:
+            o, l, c = oracle.sparse_dcp_decode(qn, qp, cache, table, L, qsl, w.topk.numpy(), w.topk_valid.numpy(),
+                                               w.dcp_world, r, w.scale, threads=threads)
+        parts.append(o), lses.append(l), counts.append(c)
+    merged, lse = oracle.lse_merge(np.stack(parts), np.stack(lses), np.stack(counts))
+    if w.w_uv is not None:
+        merged = oracle.wuv_project(merged, wl.bf16_bits(w.w_uv))
+    return merged, lse
+
+
+def run_cpu_full(args):
+    """The fp64 oracle's step on every benchmark workload at full size, on all
+    host cores (one step each), and on one thread over the first requests
+    of each (a bounded sample): one JSON line per workload."""
+    import oracle
+    from mla_decode_attention_04_gb300 import workloads as wl
+    threads = oracle.default_threads()
+    for name in CONFIG_NAMES:
+        w = wl.NAMED[name](device="cpu")
+        t0 = time.perf_counter()
+        oracle_full_step(w, threads)
+        dt = time.perf_counter() - t0
+        n1 = {"long_context": 1, "sparse_mixed": 4}.get(name, 8)
+        w1 = wl.NAMED[name](device="cpu", **({"batch": n1} if name != "sparse_mixed" else {"n_decode": n1, "n_prefill": 0}))
+        t0 = time.perf_counter()
+        oracle_full_step(w1, 1)
+        dt1 = time.perf_counter() - t0
+        print(json.dumps({"cpu_full": name, "workload": DESCR[name], "threads": threads, "nproc": os.cpu_count(),
+                          "cpu_model": cpu_model(), "seconds_per_step": dt, "query_tok_s": w.num_tokens / dt,
+                          "one_thread": {"requests": n1, "query_tokens": w1.num_tokens, "seconds": dt1,
+                                         "query_tok_s": w1.num_tokens / dt1,
+                                         "sample": f"the first {n1} requests drawn the same way, 1 thread"}}),
+              flush=True)
+        del w, w1
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -694,12 +742,16 @@ def run_profile_case(name, repeat, route="fused"):
     command the ncu summaries under profiles/ are captured from."""
     from mla_decode_attention_04_gb300 import pipeline, workloads as wl
     w = wl.NAMED[name](device="cuda")
-    fused = route == "fused"
-    step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
+    fused = route in ("fused", "fp8")
+    if route == "fp8":
+        _, views = wl.fp8_cache(w, FP8_SCALE)
+        step = pipeline.fused_step_for_workload(w, fp8_caches=views, kv_scale=FP8_SCALE)
+    else:
+        step = pipeline.fused_step_for_workload(w) if fused else pipeline.step_for_workload(w)
     for _ in range(repeat):
         step.run()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_case": name, "repeat": repeat, "route": "fused" if fused else "shards"}), flush=True)
+    print(json.dumps({"profile_case": name, "repeat": repeat, "route": route}), flush=True)
 
 
 def main():
@@ -711,11 +763,17 @@ def main():
     ap.add_argument("--configs", default="all", help="all | headline | comma list of workload names")
     ap.add_argument("--profile-case", default=None, help="run one workload's step untimed (for ncu), print no bench line")
     ap.add_argument("--repeat", type=int, default=3, help="steps of --profile-case")
-    ap.add_argument("--route", default="fused", choices=["fused", "shards"],
-                    help="--profile-case: one shard-fused decode launch, or D shard calls + merge")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="time the fp64 oracle on every workload at full size (all cores) and on a one-thread sample")
+    ap.add_argument("--route", default="fused", choices=["fused", "shards", "fp8"],
+                    help="--profile-case: one shard-fused decode launch, D shard calls + merge, or the fused launch "
+                         "over an FP8 copy of the cache")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args.profile_case, args.repeat, args.route)
+        return
+    if args.cpu_full:
+        run_cpu_full(args)
         return
     if args.warmup < 3:
         args.warmup = 3
