@@ -73,8 +73,7 @@ template <int NR> struct TmemPlan {
   static_assert(kColO + 4 * NR <= 512, "TMEM budget");
 };
 template <int NR, bool KV8 = false> struct Pipe {
-  // FP8 caches: 2 bf16 stages, next to 2 staging buffers of raw FP8 tiles
-  static constexpr int kStages = (NR == 64 || KV8) ? 2 : 3;
+  static constexpr int kStages = NR == 64 ? 2 : 3;
   // a unit's Q rows travel through one ring slot, row r at r * kQRowBytes:
   // with room to spare, a 16-byte pad puts consecutive rows in different
   // banks for the softmax warps' row reads (64 padded rows would not fit)
@@ -88,15 +87,18 @@ template <int NR, bool KV8 = false> struct Pipe {
   static constexpr int kPLoBytes = kPLoInChunk ? 0 : kStages * kPBytes;
   static constexpr int kOffQSmem = kStages * kStageBytes;
   static constexpr int kOffPLo = kOffQSmem + kQSmemBytes;
-  // FP8 staging buffer: the tile's 576 code bytes per row as 4 boxes of 128
-  // columns (64 rows x 128 B, 128-byte swizzle, 8 KB each) and one of the
-  // last 64 columns (64 rows x 64 B, no swizzle)
-  static constexpr int kStgBufs = KV8 ? 2 : 0;
-  static constexpr int kStgBytes = 4 * 8192 + 4096;
-  static constexpr int kOffStg = kOffPLo + kPLoBytes;
-  static constexpr int kOffShared = kOffStg + kStgBufs * kStgBytes;
+  static constexpr int kOffShared = kOffPLo + kPLoBytes;
   static_assert(!KV8 || NR <= 32, "FP8 caches use units of up to 32 rows");
 };
+// FP8 caches: a tile's raw codes land in the upper half of the very stage
+// they are widened into, as 4 boxes of 128 columns (64 rows x 128 B,
+// 128-byte swizzle, 8 KB each, 1024-aligned) and one of the last 64 columns
+// (64 rows x 64 B, no swizzle).  Widening part m writes chunks 2m, 2m+1 (part
+// 3 also chunk 8): parts 0-2 overwrite only raw parts already widened, part 3
+// overwrites its own codes, which every thread reads before any writes.
+__host__ __device__ constexpr int raw_part_off(int m) { return 36864 + 8192 * m; }
+constexpr int kRawTailOff = 36864 + 4 * 8192;
+static_assert(kRawTailOff + 4096 == 9 * 8192, "raw codes end at the stage's end");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -130,14 +132,13 @@ __host__ __device__ constexpr int part_chunks(int m) { return m == kParts - 1 ? 
 struct TcShared {
   uint64_t full[kMaxStages][kParts];
   uint64_t empty[kMaxStages][kParts];
-  uint64_t stg_full[2][kParts], stg_empty[2][kParts];  // FP8 staging (parts as the stages')
+  uint64_t stg_full[kMaxStages][kParts];  // FP8: a stage part's raw codes have landed
   uint64_t drain[2];  // completion of every MMA of the QK^T / PV thread, at exit
   uint64_t s_full[2], s_free[2], p_ready, pv_done, unit_done, q_ready;
   uint32_t tmem_base;
   int32_t any_rescale[2];
   int32_t wait_ok;  // result of the softmax group's last mbarrier wait
-  int32_t conv_ok;  // result of the FP8 converters' last waits for a staged part
-  int32_t conv_q_ok;  // result of the FP8 converters' last waits for a Q slot
+  int32_t conv_ok;  // result of the FP8 converters' last wait for a part's codes
   int32_t prod_ok;  // result of the sparse producer group's last wait
   float alpha[64], inv_l[64];
   // per-tile partial row maxima [tile parity][key slice * NR + row] (the
@@ -166,7 +167,7 @@ struct Roles {
   static constexpr int kMmaWarp = kProducerWarps;          // issues QK^T (and owns TMEM)
   static constexpr int kSoftmaxWarp0 = kProducerWarps + 1;  // four consecutive warps
   static constexpr int kPvWarp = kProducerWarps + 5;        // issues PV
-  // FP8 caches: warps widening each staged FP8 tile to bf16 in its stage
+  // FP8 caches: warps widening each FP8 tile to bf16 in its stage
   // (and filling the units' Q slots)
   static constexpr int kConvWarps = KV8 ? 4 : 0;
   static constexpr int kConvWarp0 = kProducerWarps + 6;
@@ -452,7 +453,9 @@ __device__ __forceinline__ const CUtensorMap* kv8_tail_map_of(const KvMaps& maps
 // bf16 read as the bf16 2^(e-127) * 1.mmm (or its subnormal 0.mmm * 2^-126 for
 // e = 0), so one multiply by 2^120 gives the code's value 2^(e-7) * 1.mmm (or
 // m * 2^-9); the sign bit moves to bit 15.  Exact: the products have at most
-// 4 significant bits and bf16 arithmetic keeps subnormal operands.
+// 4 significant bits and bf16 arithmetic keeps subnormal operands.  (This GPU
+// widens E4M3 to f16 in one instruction, but not to bf16; the f16 route would
+// need the bf16 queries in f16 and measured no faster here.)
 __device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
   const __nv_bfloat162 k = __floats2bfloat162_rn(0x1p120f, 0x1p120f);
   const uint32_t w0 = __byte_perm(x, 0u, 0x4140), w1 = __byte_perm(x, 0u, 0x4342);
@@ -502,7 +505,6 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
   uint8_t* kv = base;                           // [kStages][9][kChunk]
   uint8_t* q_smem = base + PP::kOffQSmem;       // NR = 64: Q chunks 0-2 as the QK^T A operand [3][128 rows][128 B]
   uint8_t* p_lo_buf = base + PP::kOffPLo;       // NR = 64: P lo per stage
-  uint8_t* stg = base + PP::kOffStg;            // FP8: [2][kStgBytes] raw tiles
   TcShared& sh = *reinterpret_cast<TcShared*>(base + PP::kOffShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -525,11 +527,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
         mbar_init(&sh.empty[s][m], 1);
       }
     if (KV8)
-      for (int b = 0; b < 2; ++b)
-        for (int m = 0; m < kParts; ++m) {
-          mbar_init(&sh.stg_full[b][m], 1);
-          mbar_init(&sh.stg_empty[b][m], 1);
-        }
+      for (int b = 0; b < kStages; ++b)
+        for (int m = 0; m < kParts; ++m) mbar_init(&sh.stg_full[b][m], 1);
     mbar_init(&sh.drain[0], 1);
     mbar_init(&sh.drain[1], 1);
     for (int b = 0; b < 2; ++b) {
@@ -585,7 +584,7 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
   // release, which follows its consumption.  Every arming of a part is
   // recorded, a plain arrival too: a parity wait on an older round would
   // alias once the barrier has completed two more.
-  uint32_t armed[kMaxStages] = {0, 0, 0}, armed_stg[2] = {0, 0};
+  uint32_t armed[kMaxStages] = {0, 0, 0}, armed_stg[kMaxStages] = {0, 0, 0};
   auto note_armed = [](uint32_t& word, int m, uint32_t parity) {
     word = (word & ~(3u << (2 * m))) | ((2u | (parity & 1u)) << (2 * m));
   };
@@ -599,6 +598,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0;
+    int q_st = -1;  // FP8: the last Q slot armed and its phase (see below)
+    uint32_t q_ph = 0;
     if constexpr (!SPARSE) {
       // The whole warp walks the units; lane l holds the page id of block-
       // table column (cache_col + l), refilled 32 columns at a time, so the
@@ -611,8 +612,12 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
       const int nsub = ps >= kKeyTile ? 1 : kKeyTile / ps;  // pages per tile
       Unit w = w0;
       int cache_b = -1, cache_k = -1, cache_col = 0, my_page = -1;
-      int stg_b = 0;         // FP8 staging buffer of the next tile
-      uint32_t stg_ph = 0;   // its round parity
+      // FP8: per stage, the parity of its next key-tile use (Q slots do not
+      // touch its raw-code barriers), and the last Q slot armed (stage, phase):
+      // the converter warps' arrivals complete the stages' full phases of key
+      // tiles, so a Q slot's record is kept apart and dropped once this warp
+      // refills that stage (the slot was read then)
+      uint32_t kv_ph[kMaxStages] = {0, 0, 0};
       // the unit's Q rows: one slot of the ring (NR <= 32: a bulk copy per
       // row half; NR = 64: 9 TMA tiles of 64 rows x 64 dims)
       auto issue_q = [&](const Unit& u, int st, uint32_t ph) -> bool {
@@ -629,7 +634,12 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
               mbar_arrive_expect_tx(&sh.full[st][0], (uint32_t)u.nrows * (kRow * 2));
             // every part's record moves to this round, so none keeps an
             // older round's parity that the barrier has since passed twice
-            for (int m = 0; m < kParts; ++m) note_armed(armed[st], m, ph);
+            if (KV8) {
+              q_st = st;
+              q_ph = ph;
+            } else {
+              for (int m = 0; m < kParts; ++m) note_armed(armed[st], m, ph);
+            }
             for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[st][m]);
           }
         }
@@ -648,17 +658,17 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
       };
       // The Q slot of the CTA's first unit (stage 0, free at the start) is
       // filled by the softmax warps, so this warp goes straight to the key
-      // tiles and both start out at once.  FP8 caches: the converter warps
-      // fill every later Q slot.  This warp waits only for the staging
-      // buffers there, so it may run more than one ring round ahead of the
-      // stages' releases, where a parity wait on a stage's empty barrier
-      // could not tell the round it needs from the one before.
+      // tiles and both start out at once.  This warp is the only one that
+      // fills the ring after that (Q slots, key tiles, FP8 codes), one
+      // position at a time in ring order, each after the release of the
+      // round before: a parity wait on a stage's empty barrier can then never
+      // see a round two ahead of the one it waits for.
       bool first = true;
       for (bool more = more0; ok && more; more = it.next(a, w)) {
         if (w.n_kt > 0) {
           if (first) {
             first = false;
-          } else if (!KV8 && !issue_q(w, stage, phase)) {
+          } else if (!issue_q(w, stage, phase)) {
             ok = false;
             break;
           }
@@ -707,30 +717,33 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
             }
           }
           if (KV8) {
-            // FP8: the tile's codes into a staging buffer, part by part (the
-            // converter warps widen part m into the stage's part m)
+            // FP8: the tile's codes into the upper half of its own stage once
+            // the stage's previous round is released (all four parts: the
+            // converter widens over the whole stage); the converter warps
+            // widen part m into the stage's part m
             if (lane == 0) {
-              uint8_t* dst = stg + stg_b * PP::kStgBytes;
+              uint8_t* dst = kv + stage * kStageBytes;
               const uint32_t rows = ps >= kKeyTile ? kKeyTile : ps;
               const int off = ps >= kKeyTile ? k % ps : 0;
               const CUtensorMap* tmap = kv8_tail_map_of(maps, loc.k);
-              for (int m = 0; m < kParts; ++m) {
-                if (!wait(&sh.stg_empty[stg_b][m], stg_ph ^ 1, kSiteProducerStaging)) {
-                  ok = false;
-                  break;
-                }
-                mbar_arrive_expect_tx(&sh.stg_full[stg_b][m],
+              for (int m = 0; m < kParts && ok; ++m)
+                if (!wait(&sh.empty[stage][m], phase ^ 1, kSiteProducerStage)) ok = false;
+              if (ok && stage == q_st) q_st = -1;  // that Q slot was read: its copies are in
+              for (int m = 0; m < kParts && ok; ++m) {
+                mbar_arrive_expect_tx(&sh.stg_full[stage][m],
                                       (uint32_t)(nvalid * rows * (m == kParts - 1 ? 128 + 64 : 128)));
-                note_armed(armed_stg[stg_b], m, stg_ph);
+                note_armed(armed_stg[stage], m, kv_ph[stage]);
                 for (int i = 0; i < nsub; ++i) {
                   if (pages[i] < 0) continue;
-                  tma_load_3d(dst + m * 8192 + i * ps * 128, map, m * 128, off, pages[i], &sh.stg_full[stg_b][m], pol);
+                  tma_load_3d(dst + raw_part_off(m) + i * ps * 128, map, m * 128, off, pages[i],
+                              &sh.stg_full[stage][m], pol);
                   if (m == kParts - 1)
-                    tma_load_3d(dst + 4 * 8192 + i * ps * 64, tmap, 512, off, pages[i], &sh.stg_full[stg_b][m], pol);
+                    tma_load_3d(dst + kRawTailOff + i * ps * 64, tmap, 512, off, pages[i], &sh.stg_full[stage][m],
+                                pol);
                 }
               }
             }
-            if (++stg_b == 2) { stg_b = 0; stg_ph ^= 1; }
+            kv_ph[stage] ^= 1;
           } else if (lane == 0) {
             // part by part, each as soon as the value product frees it
             uint8_t* dst = kv + stage * kStageBytes;
@@ -849,7 +862,10 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
     }
     // exit: every copy this thread issued has landed (its armed phases done)
     drain_armed(sh.full, armed, kStages);
-    if (KV8) drain_armed(sh.stg_full, armed_stg, 2);
+    if (KV8) {
+      drain_armed(sh.stg_full, armed_stg, kStages);
+      if (lane == 0 && q_st >= 0) mbar_wait(&sh.full[q_st][0], q_ph, kDrainNs);
+    }
   } else if (warp == R::kMmaWarp || warp == R::kPvWarp) {
     // --------------------------------------------------------------- MMA
     // One thread cannot issue tcgen05.mma fast enough to keep the tensor
@@ -945,117 +961,80 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
     }
   } else if (KV8 && warp >= R::kConvWarp0) {
     // ---------------------------------------------------------- FP8 widen
-    // Each staged FP8 part becomes the same part of its bf16 stage, in the
-    // stage's 128-byte-swizzled chunk layout.  Thread ct of the 128 takes row
-    // ct / 2 and half ct & 1 of the part's 128 code columns (4 pieces of 16
-    // codes -> 8 bf16 pieces), and of the last part's 64 tail columns (2
-    // pieces -> 4 bf16 pieces).  One thread waits, a named barrier hands the
-    // verdict to the others, each of which then observes the completed phase.
+    // Each part of a tile's codes (in the upper half of the tile's own stage)
+    // becomes the same part of the stage in bf16, in the 128-byte-swizzled
+    // chunk layout the bf16 path's TMA writes, part by part so that the score
+    // product starts on a tile's first chunks while its last ones widen.
+    // Thread ct of the 128 takes row ct / 2 and half ct & 1 of the part's 128
+    // code columns (4 pieces of 16 codes -> 8 bf16 pieces), and of the last
+    // part's 64 tail columns (2 pieces -> 4 bf16 pieces).  Parts 0-2 write
+    // over codes already widened only; part 3 writes over its own codes, so
+    // every thread loads all of part 3 before a barrier and writes after it.
+    // One thread waits for a part's codes, a named barrier hands the verdict
+    // to the others, each of which then observes the completed phase.  The
+    // producer waited for the stage's release before loading the codes, so
+    // these warps wait for nothing else (they only widen in place; they fill
+    // no ring slot).
     const int ct = (int)threadIdx.x - R::kConvWarp0 * 32;
     const int r = ct >> 1, h = ct & 1;
-    int stage = 0, stg_b = 0;
-    uint32_t phase = 0, stg_ph = 0;
-    // These warps fill the ring in its order, so a stage's empty barrier
-    // is at most one round behind the wait.  The Q slot of every unit but
-    // the first goes in here too: a bulk copy per row half, on the slot's
-    // part-0 full barrier (parts 1-3 get a plain arrival).  Thread 0 keeps
-    // the last such slot until a later round of its stage is released
-    // (its copies have landed then): at exit it waits for that phase.
-    bool first = true;
-    int q_st = -1;
-    uint32_t q_ph = 0;
+    int stage = 0;
+    uint32_t kv_ph[kMaxStages] = {0, 0, 0};  // per stage: parity of its next key-tile use
     Unit w = w0;
+    auto widen = [&](const uint4& x, uint8_t* drow, int p0, int p1) {
+      uint32_t o[8];
+      e4m3x4_to_bf16x2(x.x, o[0], o[1]);
+      e4m3x4_to_bf16x2(x.y, o[2], o[3]);
+      e4m3x4_to_bf16x2(x.z, o[4], o[5]);
+      e4m3x4_to_bf16x2(x.w, o[6], o[7]);
+      *reinterpret_cast<uint4*>(drow + ((p0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(drow + ((p1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    };
     for (bool more = more0; ok && more; more = it.next(a, w)) {
       if (w.n_kt == 0) continue;
-      if (!first) {
-        if (ct == 0) {
-          bool g = true;
-          for (int m = 0; m < kParts && g; ++m) g = wait(&sh.empty[stage][m], phase ^ 1, kSiteConvertQ);
-          if (g) {
-            mbar_arrive_expect_tx(&sh.full[stage][0], (uint32_t)w.nrows * (kRow * 2));
-            for (int m = 1; m < kParts; ++m) mbar_arrive(&sh.full[stage][m]);
-            q_st = stage;
-            q_ph = phase;
-          }
-          sh.conv_q_ok = g ? 1 : 0;
-        }
-        named_bar_sync(2, 128);
-        if (!sh.conv_q_ok) {
-          ok = false;
-          break;
-        }
-        if (ct < w.nrows) {
-          const int64_t grow = (int64_t)w.q0 * a.num_heads + w.row0 + ct;
-          uint8_t* qdst = kv + stage * kStageBytes + ct * PP::kQRowBytes;
-          bulk_load(qdst, a.q_nope + grow * a.q_nope_stride, kNope * 2, &sh.full[stage][0]);
-          bulk_load(qdst + kNope * 2, a.q_pe + grow * a.q_pe_stride, kRope * 2, &sh.full[stage][0]);
-        }
-      }
-      first = false;
-      if (++stage == kStages) { stage = 0; phase ^= 1; }  // the unit's Q slot
+      if (++stage == kStages) stage = 0;  // the unit's Q slot
       for (int kt = 0; kt < w.n_kt && ok; ++kt) {
-        const uint8_t* src = stg + stg_b * PP::kStgBytes;
-        uint8_t* dst = kv + stage * kStageBytes;
+        uint8_t* st_base = kv + stage * kStageBytes;
         for (int m = 0; m < kParts; ++m) {
-          if (ct == 0) {
-            sh.conv_ok = (wait(&sh.stg_full[stg_b][m], stg_ph, kSiteConvert) &&
-                          wait(&sh.empty[stage][m], phase ^ 1, kSiteConvert))
-                             ? 1
-                             : 0;
-            if (sh.conv_ok && stage == q_st) q_st = -1;  // the Q slot was read: its copies are in
-          }
+          if (ct == 0) sh.conv_ok = wait(&sh.stg_full[stage][m], kv_ph[stage], kSiteConvert) ? 1 : 0;
           named_bar_sync(2, 128);
           if (!sh.conv_ok) {
             ok = false;
             break;
           }
-          mbar_wait(&sh.stg_full[stg_b][m], stg_ph);  // returns at once
+          mbar_wait(&sh.stg_full[stage][m], kv_ph[stage]);  // returns at once
           // columns [128 m, 128 m + 128): code piece v (codes 16v..16v+15)
           // -> bf16 chunk 2m + v / 4, pieces 2 (v % 4) and 2 (v % 4) + 1
+          const uint8_t* src = st_base + raw_part_off(m);
+          uint4 x[4];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const int v = 4 * h + v4;
-            const uint4 x = *reinterpret_cast<const uint4*>(src + m * 8192 + r * 128 + ((v ^ (r & 7)) << 4));
-            uint32_t o[8];
-            e4m3x4_to_bf16x2(x.x, o[0], o[1]);
-            e4m3x4_to_bf16x2(x.y, o[2], o[3]);
-            e4m3x4_to_bf16x2(x.z, o[4], o[5]);
-            e4m3x4_to_bf16x2(x.w, o[6], o[7]);
-            uint8_t* drow = dst + (2 * m + (v >> 2)) * kChunk + r * 128;
-            const int w0 = 2 * (v & 3);
-            *reinterpret_cast<uint4*>(drow + ((w0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(drow + (((w0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          for (int v4 = 0; v4 < 4; ++v4)
+            x[v4] = *reinterpret_cast<const uint4*>(src + r * 128 + (((4 * h + v4) ^ (r & 7)) << 4));
+          uint4 y[2];
           if (m == kParts - 1) {
             // columns [512, 576): tail piece v -> bf16 chunk 8, pieces 2v, 2v + 1
 #pragma unroll
+            for (int v2 = 0; v2 < 2; ++v2)
+              y[v2] = *reinterpret_cast<const uint4*>(st_base + kRawTailOff + r * 64 + (2 * h + v2) * 16);
+            named_bar_sync(2, 128);  // every thread has its codes: the writes may cover them
+          }
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            widen(x[v4], st_base + (2 * m + h) * kChunk + r * 128, 2 * v4, 2 * v4 + 1);
+          if (m == kParts - 1) {
+#pragma unroll
             for (int v2 = 0; v2 < 2; ++v2) {
               const int v = 2 * h + v2;
-              const uint4 x = *reinterpret_cast<const uint4*>(src + 4 * 8192 + r * 64 + v * 16);
-              uint32_t o[8];
-              e4m3x4_to_bf16x2(x.x, o[0], o[1]);
-              e4m3x4_to_bf16x2(x.y, o[2], o[3]);
-              e4m3x4_to_bf16x2(x.z, o[4], o[5]);
-              e4m3x4_to_bf16x2(x.w, o[6], o[7]);
-              uint8_t* drow = dst + 8 * kChunk + r * 128;
-              *reinterpret_cast<uint4*>(drow + (((2 * v) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(drow + (((2 * v + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+              widen(y[v2], st_base + 8 * kChunk + r * 128, 2 * v, 2 * v + 1);
             }
           }
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
-          if (ct == 0) {
-            mbar_arrive(&sh.full[stage][m]);
-            mbar_arrive(&sh.stg_empty[stg_b][m]);
-          }
+          if (ct == 0) mbar_arrive(&sh.full[stage][m]);
         }
-        if (++stg_b == 2) { stg_b = 0; stg_ph ^= 1; }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        kv_ph[stage] ^= 1;
+        if (++stage == kStages) stage = 0;
       }
     }
-    // exit: the last Q slot's copies have landed, read or not (no round of
-    // its stage after it was filled, so the phase is the barrier's own)
-    if (ct == 0 && q_st >= 0) mbar_wait(&sh.full[q_st][0], q_ph, kDrainNs);
   } else {
     // ----------------------------------------------------------- softmax
     const int sw = warp - R::kSoftmaxWarp0;   // 0..3
