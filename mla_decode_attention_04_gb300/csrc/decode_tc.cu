@@ -103,10 +103,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Where a pipeline wait gave up (the workspace header's diagnostic word).
+// (2 and 15 are unused: earlier FP8 staging waits, kept so the numbers of
+// the others stay stable)
 enum WaitSite : int32_t {
-  kSiteProducerQ = 1, kSiteProducerStaging, kSiteProducerStage, kSiteSparseQ, kSiteSparsePart, kSiteQkQ,
-  kSiteQkSFree, kSiteQkFull, kSitePvReady, kSiteConvert, kSiteSoftmaxQ, kSiteSoftmaxS, kSiteSoftmaxPv,
-  kSiteSoftmaxUnit, kSiteConvertQ
+  kSiteProducerQ = 1, kSiteProducerStage = 3, kSiteSparseQ, kSiteSparsePart, kSiteQkQ, kSiteQkSFree, kSiteQkFull,
+  kSitePvReady, kSiteConvert, kSiteSoftmaxQ, kSiteSoftmaxS, kSiteSoftmaxPv, kSiteSoftmaxUnit
 };
 // Budget of a wait for copies or MMAs already issued when a role gave up
 // (they complete by themselves; the bound only keeps the kernel finite).

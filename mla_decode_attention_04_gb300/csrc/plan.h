@@ -51,7 +51,8 @@ inline DecodePlan make_decode_plan(int32_t B, int32_t T, int32_t H, int32_t max_
   if (max_query_len < 1) max_query_len = 1;  // the backend's capture-time clamp
   if (D < 1) D = 1;
   p.rows_per_group = rows_per_unit((int64_t)max_query_len * H);
-  // an FP8 cache's staging buffers leave room for units of up to 32 rows
+  // an FP8 cache adds four converter warps, whose registers the 64-row
+  // softmax cannot spare: units of up to 32 rows
   if (kv_fp8 && p.rows_per_group > 32) p.rows_per_group = 32;
   p.unit_penalty = kUnitPenalty;
   const int64_t NR = p.rows_per_group;
