@@ -113,3 +113,37 @@ def test_two_stage_status_reports_the_second_stage():
     s.block_table[0, 3] = good
     _two_stage(w, workspace=ws)
     assert mla.workspace_status(ws) == (mla.MLA_OK, 0)
+
+
+def test_two_stage_replays_in_a_cuda_graph():
+    """The call allocates nothing and reads its lengths on the device: one
+    captured call replays bit for bit like the eager call, also after the
+    lengths change within the captured bounds."""
+    w = wl.custom([300, 41, 1000, 7], [2, 1, 4, 3], 16, 2, page_size=16, seed=21).to("cuda")
+    ws = _workspace(w)
+    out = torch.empty((w.num_tokens, w.num_heads, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((w.num_tokens, w.num_heads), dtype=torch.float32, device="cuda")
+
+    def call():
+        mla.mla_dcp_decode_two_stage(w.q_nope, w.q_pe, [s.cache for s in w.shards], [s.block_table for s in w.shards],
+                                     w.seq_lens, w.query_start_loc, w.max_query_len, w.max_seq_len, w.scale,
+                                     out=out, lse=lse, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for lens in ([300, 41, 1000, 7], [290, 12, 999, 3]):
+        w.seq_lens.copy_(torch.tensor(lens, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        o_graph, l_graph = out.clone(), lse.clone()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(o_graph, out) and torch.equal(l_graph, lse)
+        assert mla.workspace_status(ws) == (mla.MLA_OK, 0)
