@@ -94,8 +94,7 @@ def test_tiny_fp8_shards_and_fused(num_splits, out_dtype):
     assert_lse_close(to_np(lse), ref["lse"], "fp8 fused lse")
 
 
-@pytest.mark.parametrize("name", ["page_32", "d8_ragged_shards", "prefill_from_empty", "heads_17_ragged_groups",
-                                  "heads_128", "empty_request"])
+@pytest.mark.parametrize("name", sorted(EDGE))
 def test_fp8_edge_shapes(name):
     w = wl.custom(seed=sorted(EDGE).index(name), **EDGE[name]).to("cuda")
     _, views, host8 = _fp8(w, 0.125)
