@@ -1344,8 +1344,9 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
       }
       named_bar_sync(1, 128);
       // O^T's 4 NR columns (column m NR + n: dims of block m, row n), 64
-      // columns (registers) per TMEM round trip in loads of CW
-      constexpr int PER = 64 / CW;
+      // columns (registers) per TMEM round trip in loads of CW (32 with
+      // FP8 caches, whose converter warps leave fewer registers per thread)
+      constexpr int PER = (KV8 ? 32 : 64) / CW;
 #pragma unroll 1
       for (int q0 = 0; q0 < 4 * NR / CW; q0 += PER) {
         uint32_t o[PER][CW];
@@ -1359,22 +1360,33 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
 #pragma unroll
             for (int n = 0; n < CW; ++n) o[p][n] = 0u;
         }
+        // rows n0 .. n0 + CW - 1 of one 128-dim block, to one base address
+        // at a fixed row stride, 8 values then their 8 stores at a time with
+        // no branch between them (a per-value row test and shared-memory
+        // load made this a serial chain of ~80 cycles per value)
 #pragma unroll
         for (int p = 0; p < PER; ++p) {
           const int col0 = (q0 + p) * CW;
+          const int n0 = col0 % NR;
           const int dim = (col0 / NR) * 128 + quarter * 32 + lane;
+          const int cnt = min(CW, w.nrows - n0);  // rows of this block the unit has
+          const int64_t r0 = partial ? chunk_slot(w.cta0, w.split, NR, it.S) + n0 : grow(n0);
+          float* dst32 = (partial ? a.part_o : static_cast<float*>(a.out)) + r0 * kNope + dim;
+          __nv_bfloat16* dst16 = static_cast<__nv_bfloat16*>(a.out) + r0 * kNope + dim;
+          const bool f32 = partial || a.out_f32;
 #pragma unroll
-          for (int e = 0; e < CW; ++e) {
-            const int n = col0 % NR + e;
-            if (n >= w.nrows) break;
-            const float v = __uint_as_float(o[p][e]) * sh.inv_l[n];
-            if (partial) {
-              const int64_t slot = chunk_slot(w.cta0, w.split, NR, it.S) + n;
-              a.part_o[slot * kNope + dim] = v;
-            } else if (a.out_f32) {
-              static_cast<float*>(a.out)[grow(n) * kNope + dim] = v;
+          for (int g = 0; g < CW; g += 8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(o[p][g + e]) * sh.inv_l[n0 + g + e];
+            if (f32) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (g + e < cnt) dst32[(int64_t)(g + e) * kNope] = v[e];
             } else {
-              static_cast<__nv_bfloat16*>(a.out)[grow(n) * kNope + dim] = __float2bfloat16_rn(v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (g + e < cnt) dst16[(int64_t)(g + e) * kNope] = __float2bfloat16_rn(v[e]);
             }
           }
         }
