@@ -111,6 +111,9 @@ const char *mla_last_error(void);
  *  out      device [num_tokens, num_heads, 512] of out_dtype (BF16 or F32).
  *  lse      device float32 [num_tokens, num_heads].
  *  row_counts device int32 [num_tokens], or NULL.
+ *  scale    softmax scale, finite and > 0 (1/sqrt(192) for 128 + 64 q-k dims); the
+ *           kernels take a row's largest score from the unscaled dot
+ *           products, which needs a positive scale.
  *  num_splits  0 = automatic split-KV plan, else an upper bound on the KV
  *           chunks per request (fix it for CUDA-graph capture).
  *  workspace   device scratch of at least mla_dcp_decode_workspace_size()
@@ -127,7 +130,8 @@ const char *mla_last_error(void);
  *  the KV chunks of row groups the decode split over several CTAs).
  *  Errors: INVALID_ARG (NULL/misaligned pointers, sizes < 0, dcp_rank not in
  *  [0, dcp_world), num_heads not in [1, 128], num_tokens * num_heads >=
- *  2^31), UNSUPPORTED (page size), WORKSPACE, CUDA.  num_tokens == 0 is a
+ *  2^31, scale not finite and positive), UNSUPPORTED (page size),
+ *  WORKSPACE, CUDA.  num_tokens == 0 is a
  *  successful no-op.
  * ---------------------------------------------------------------------- */
 size_t mla_dcp_decode_workspace_size(int32_t num_requests, int32_t num_tokens, int32_t num_heads,

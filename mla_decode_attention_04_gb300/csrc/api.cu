@@ -90,7 +90,8 @@ int check_decode_common(const void* q_nope, int64_t q_nope_row_stride, const voi
     return fail(MLA_ERR_INVALID_ARG, "misaligned pointer (q/cache/out need 16-byte alignment)");
   if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_F32)
     return fail(MLA_ERR_INVALID_ARG, "out_dtype %d: BF16 or F32", out_dtype);
-  if (!std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale is not finite");
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "scale %g: a finite positive softmax scale is required", scale);
   if (workspace == nullptr || !aligned(workspace, 256))
     return fail(MLA_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
   return MLA_OK;

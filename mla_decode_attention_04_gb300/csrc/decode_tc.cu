@@ -1208,21 +1208,17 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
           valid = max(0, min(lim - kbase, kKeyTile));
           tile_valid = min(cur_sh.Lr - kbase, kKeyTile);
         }
-        float pmax = -INFINITY;
-        if (kslice * KPT + KPT <= valid) {  // this thread sees every key of its slice (all tiles but a row's last)
+        // the slice's largest raw score (masked keys -> -inf), as four
+        // independent chains; scaled once (the scale is positive)
+        if (kslice * KPT + KPT > valid) {  // not every key of the slice visible: a row's last tiles
 #pragma unroll
-          for (int e = 0; e < KPT; ++e) {
-            s[e] *= scale_log2;
-            pmax = fmaxf(pmax, s[e]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < KPT; ++e) {
-            const float v = kslice * KPT + e < valid ? s[e] * scale_log2 : -INFINITY;
-            s[e] = v;
-            pmax = fmaxf(pmax, v);
-          }
+          for (int e = 0; e < KPT; ++e)
+            if (kslice * KPT + e >= valid) s[e] = -INFINITY;
         }
+        float pm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < KPT; ++e) pm[e & 3] = fmaxf(pm[e & 3], s[e]);
+        const float pmax = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale_log2;
         sh.red[j & 1][kslice * NR + row] = pmax;
         tc_fence_before();
         named_bar_sync(1, 128);
@@ -1245,15 +1241,18 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
           const int roff = (row >> 3) * 1024 + (row & 7) * 128;
           uint8_t* prow = kv + stage * kStageBytes + kPChunk * kChunk + roff;
           uint8_t* prow_lo = PP::kPLoInChunk ? prow + PP::kPBytes : p_lo_buf + stage * PP::kPBytes + roff;
-          float sum = 0.f;
+          // P = 2^(s scale_log2 - m_ref) in one fused multiply-add per key
+          // (a row with no visible key so far: every s is -inf, P = 0)
+          const float neg_m = m_ref > -INFINITY ? -m_ref : -INFINITY;
+          float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int c8 = 0; c8 < KPT / 8; ++c8) {
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float p0 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e] - m_ref) : 0.f;
-              const float p1 = m_ref > -INFINITY ? fast_exp2(s[8 * c8 + 2 * e + 1] - m_ref) : 0.f;
-              sum += p0 + p1;
+              const float p0 = fast_exp2(fmaf(s[8 * c8 + 2 * e], scale_log2, neg_m));
+              const float p1 = fast_exp2(fmaf(s[8 * c8 + 2 * e + 1], scale_log2, neg_m));
+              sum4[e] += p0 + p1;
               if (p_split) {
                 // hi = P truncated to bf16 (its top 16 bits, one byte permute
                 // for the pair), lo = bf16(P - hi): hi + lo carries P to 2^-16
@@ -1271,7 +1270,8 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
             *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             if (p_split) *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
-          l_sum += sum;  // this thread's part of the row sum (same alpha for every part)
+          // this thread's part of the row sum (same alpha for every part)
+          l_sum += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         }
         // value rows of keys past the chunk end: zero them (P is 0 there, and
         // 0 * (garbage) must not reach the accumulator)

@@ -77,6 +77,8 @@ def _decode(lib, **kw):
     (dict(sn=500), mla.MLA_ERR_INVALID_ARG),
     (dict(odt=7), mla.MLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), mla.MLA_ERR_INVALID_ARG),
+    (dict(scale=0.0), mla.MLA_ERR_INVALID_ARG),
+    (dict(scale=-0.07), mla.MLA_ERR_INVALID_ARG),
     (dict(ws=None), mla.MLA_ERR_WORKSPACE),
     (dict(ws=A + 64), mla.MLA_ERR_WORKSPACE),
     (dict(wsb=16), mla.MLA_ERR_WORKSPACE),
