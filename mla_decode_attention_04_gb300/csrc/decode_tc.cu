@@ -40,6 +40,8 @@
 // max only moves when a tile's max exceeds it by more than 2^8.
 #include <string.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "decode_args.h"
 #include "decode_kernels.h"
@@ -1245,31 +1247,38 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
           // (a row with no visible key so far: every s is -inf, P = 0)
           const float neg_m = m_ref > -INFINITY ? -m_ref : -INFINITY;
           float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+          // the tile's P, with the hi/lo choice (uniform) outside the loop
+          auto write_p = [&](auto split_tag) {
+            constexpr bool kSplit = decltype(split_tag)::value;
 #pragma unroll
-          for (int c8 = 0; c8 < KPT / 8; ++c8) {
-            uint32_t hi[4], lo[4];
+            for (int c8 = 0; c8 < KPT / 8; ++c8) {
+              uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = fast_exp2(fmaf(s[8 * c8 + 2 * e], scale_log2, neg_m));
-              const float p1 = fast_exp2(fmaf(s[8 * c8 + 2 * e + 1], scale_log2, neg_m));
-              sum4[e] += p0 + p1;
-              if (p_split) {
-                // hi = P truncated to bf16 (its top 16 bits, one byte permute
-                // for the pair), lo = bf16(P - hi): hi + lo carries P to 2^-16
-                const uint32_t t0 = __float_as_uint(p0) & 0xffff0000u, t1 = __float_as_uint(p1) & 0xffff0000u;
-                hi[e] = __byte_perm(t0, t1, 0x7632);
-                const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __uint_as_float(t0), p1 - __uint_as_float(t1));
-                lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
-              } else {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              for (int e = 0; e < 4; ++e) {
+                const float p0 = fast_exp2(fmaf(s[8 * c8 + 2 * e], scale_log2, neg_m));
+                const float p1 = fast_exp2(fmaf(s[8 * c8 + 2 * e + 1], scale_log2, neg_m));
+                sum4[e] += p0 + p1;
+                if constexpr (kSplit) {
+                  // hi = P truncated to bf16 (its top 16 bits, one byte permute
+                  // for the pair), lo = bf16(P - hi): hi + lo carries P to 2^-16
+                  const uint32_t t0 = __float_as_uint(p0) & 0xffff0000u, t1 = __float_as_uint(p1) & 0xffff0000u;
+                  hi[e] = __byte_perm(t0, t1, 0x7632);
+                  const __nv_bfloat162 l2 =
+                      __floats2bfloat162_rn(p0 - __uint_as_float(t0), p1 - __uint_as_float(t1));
+                  lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+                } else {
+                  const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                  hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
               }
+              const int piece = kslice * (KPT / 8) + c8;  // 16-byte piece (8 keys) of the row
+              const int off = (piece ^ (row & 7)) << 4;
+              *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              if constexpr (kSplit) *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
-            const int piece = kslice * (KPT / 8) + c8;  // 16-byte piece (8 keys) of the row
-            const int off = (piece ^ (row & 7)) << 4;
-            *reinterpret_cast<uint4*>(prow + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            if (p_split) *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
+          };
+          if (p_split) write_p(std::true_type{});
+          else write_p(std::false_type{});
           // this thread's part of the row sum (same alpha for every part)
           l_sum += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         }
