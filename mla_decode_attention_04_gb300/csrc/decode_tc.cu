@@ -1179,6 +1179,20 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
       float m_ref = -INFINITY, l_sum = 0.f;
 
       for (int kt = 0; kt < w.n_kt; ++kt, ++j) {
+        // keys of the tile this row sees / that exist (before S is ready:
+        // off the score product's path)
+        int valid, tile_valid;
+        if constexpr (SPARSE) {
+          const int kbase = w.key0 + kt * kKeyTile;
+          valid = max(0, min(kend - kbase, kKeyTile));
+          tile_valid = min(w.key1 - kbase, kKeyTile);
+        } else {
+          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, nshard))
+            lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
+          const int kbase = (w.t0 + kt - cur_sh.t_begin) * kKeyTile;
+          valid = max(0, min(lim - kbase, kKeyTile));
+          tile_valid = min(cur_sh.Lr - kbase, kKeyTile);
+        }
         if (!group_wait(&sh.s_full[j % SB], (j / SB) & 1, kSiteSoftmaxS)) { ok = false; break; }
         // this thread's KPT columns of its lane's row of S
         float s[KPT];
@@ -1198,18 +1212,6 @@ __global__ void __launch_bounds__(Roles<SPARSE, NR, KV8>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.s_free[j % SB]);
-        int valid, tile_valid;  // keys of the tile this row sees / that exist
-        if constexpr (SPARSE) {
-          const int kbase = w.key0 + kt * kKeyTile;
-          valid = max(0, min(kend - kbase, kKeyTile));
-          tile_valid = min(w.key1 - kbase, kKeyTile);
-        } else {
-          if (cur_sh.seek(w.t0 + kt, w.seq_len, a.dcp_world, a.shard0, nshard))
-            lim = P_row >= 0 ? min(visible_keys(P_row, a.dcp_world, a.shard0 + cur_sh.k), cur_sh.Lr) : 0;
-          const int kbase = (w.t0 + kt - cur_sh.t_begin) * kKeyTile;
-          valid = max(0, min(lim - kbase, kKeyTile));
-          tile_valid = min(cur_sh.Lr - kbase, kKeyTile);
-        }
         // the slice's largest raw score (masked keys -> -inf), as four
         // independent chains; scaled once (the scale is positive)
         if (kslice * KPT + KPT > valid) {  // not every key of the slice visible: a row's last tiles
