@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(128) split_merge_kernel(SplitMergeArgs a) {
   grid_dep_launch();
   grid_dep_wait();  // the decode's partials and table are complete and visible
   constexpr int R = kSplitMergeRows;
-  constexpr int kAhead = 4;  // chunks whose loads go out with the table entry's
+  constexpr int kAhead = 2;  // chunks whose loads go out with the table entry's (a pair has 2, mostly)
   const int NR = a.rows_per_group;
   const int slices = NR / R;
   const int c = blockIdx.x / slices, n0 = (blockIdx.x % slices) * R;
