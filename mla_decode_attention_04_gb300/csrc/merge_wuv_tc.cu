@@ -91,7 +91,22 @@ __global__ void __launch_bounds__(kThreads, 2) merge_wuv_tc_kernel(const __grid_
     for (int b = 0; b < kWBufs; ++b) load_w_chunk(&w_map, w_s + b * kWChunk, h, b, &sh.w_full[b]);
   }
   grid_dep_sync();
-  // merge weights: warp per token, lanes over shards
+  // merge weights.  One partial (the shard-fused route's merged rows): the
+  // weight is 1 for a row with keys and its LSE passes through, one thread
+  // per token.  Otherwise a warp per token, lanes over shards.
+  if (D == 1) {
+    if (tid < kNT) {
+      const int t = t0 + tid;
+      float l = -INFINITY;
+      if (t < T) {
+        const bool part = a.valid_counts ? a.valid_counts[t] > 0 : true;
+        if (part) l = a.lses[(int64_t)t * H + h];
+        if (!(l > -INFINITY)) l = -INFINITY;  // NaN from a non-participating shard never enters
+        if (a.lse_out) a.lse_out[(int64_t)t * H + h] = l;
+      }
+      sh.wgt[tid][0] = l > -INFINITY ? 1.f : 0.f;
+    }
+  } else {
   for (int n = warp; n < kNT; n += kThreads / 32) {
     const int t = t0 + n;
     float m = -INFINITY;
@@ -114,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 2) merge_wuv_tc_kernel(const __grid_
     const float L = m > -INFINITY ? m + __logf(z) : -INFINITY;
     for (int r = lane; r < D; r += 32) sh.wgt[n][r] = L > -INFINITY ? __expf(sh.wgt[n][r] - L) : 0.f;
     if (lane == 0 && a.lse_out && t < T) a.lse_out[(int64_t)t * H + h] = L;
+  }
   }
   tc_fence_before();
   __syncthreads();
